@@ -1,0 +1,115 @@
+"""CPU oracle for the fused RoPE + causal attention forward.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the bench's CPU
+baseline leg may import this package; the product path never does.  The
+arithmetic lives in ``oracle.c`` (plain C, float64); this file compiles it
+with gcc on first use and wraps it with ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, OpenMP, IEEE float64, no FMA contraction)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            u16p = ctypes.POINTER(ctypes.c_uint16)
+            i32p = ctypes.POINTER(ctypes.c_int)
+            f64p = ctypes.POINTER(ctypes.c_double)
+            lib.oracle_attn_rows.restype = ctypes.c_int
+            lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p] + [ctypes.c_int] * 6 + [
+                ctypes.c_double, ctypes.c_double, ctypes.c_longlong, ctypes.c_int, i32p, i32p, i32p, f64p, f64p]
+            lib.oracle_pruned_terms.restype = ctypes.c_longlong
+            lib.oracle_pruned_terms.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double]
+            lib.oracle_window_widths.restype = None
+            lib.oracle_window_widths.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, f64p]
+            lib.oracle_threads.restype = ctypes.c_int
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a, t):
+    return a.ctypes.data_as(ctypes.POINTER(t))
+
+
+def threads() -> int:
+    return int(_load().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def attn_rows(q, k, v, rows_b, rows_h, rows_i, *, causal=True, rope_base=None, window_k=None, pos_offset=0):
+    """O [n, D] and LSE [n] (float64) for the selected query rows.
+
+    q: uint16 bf16 bits [B, S, Hq, D]; k, v: [B, S, Hkv, D].
+    rope_base None/<=0 turns RoPE off; window_k None/<=0/inf turns the window off.
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, S, Hkv, D) and v.shape == k.shape
+    rb = np.ascontiguousarray(rows_b, dtype=np.int32)
+    rh = np.ascontiguousarray(rows_h, dtype=np.int32)
+    ri = np.ascontiguousarray(rows_i, dtype=np.int32)
+    n = len(ri)
+    o = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = lib.oracle_attn_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+                              B, Hq, Hkv, S, D, int(bool(causal)),
+                              float(rope_base) if rope_base else 0.0,
+                              float(window_k) if window_k else 0.0, int(pos_offset), n,
+                              _ptr(rb, ctypes.c_int), _ptr(rh, ctypes.c_int), _ptr(ri, ctypes.c_int),
+                              _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return o, lse
+
+
+def attn_full(q, k, v, **kw):
+    """O [B, S, Hq, D] and LSE [B, Hq, S] (float64) for every query row."""
+    B, S, Hq, D = q.shape
+    bb, hh, ii = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(S), indexing="ij")
+    o, lse = attn_rows(q, k, v, bb.ravel(), hh.ravel(), ii.ravel(), **kw)
+    return o.reshape(B, Hq, S, D).transpose(0, 2, 1, 3).copy(), lse.reshape(B, Hq, S)
+
+
+def pruned_terms(S: int, D: int, rope_base: float, window_k: float) -> int:
+    """Cell-by-cell count of pruned (cell, pair) terms over the causal S x S triangle."""
+    return int(_load().oracle_pruned_terms(S, D, float(rope_base), float(window_k)))
+
+
+def window_widths(D: int, rope_base: float, window_k: float) -> np.ndarray:
+    w = np.zeros(D // 2, dtype=np.float64)
+    _load().oracle_window_widths(D, float(rope_base), float(window_k) if window_k else 0.0, _ptr(w, ctypes.c_double))
+    return w

@@ -1,0 +1,224 @@
+/*
+ * CPU oracle for the fused RoPE + causal attention forward (prefill).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the bench's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library; the two meet only in the seeded bf16 input bits.
+ *
+ * What it computes, in float64, straight from the definitions on the source
+ * pages, one query row at a time, with the whole score row materialised
+ * (no online recurrence, no tiling, no reordering):
+ *
+ *   theta_r  = base^(-2r/D), r = 0..D/2-1                (RoFormer; the RoPE
+ *              convention is the NeoX half split: "AttnFuse", sec. 4.1 Fused RoPE)
+ *   rotation of x at position p, pair (r, r+D/2), angle a = p*theta_r:
+ *              x'_r       = x_r cos a - x_{r+D/2} sin a
+ *              x'_{r+D/2} = x_{r+D/2} cos a + x_r sin a
+ *   window   : W_r = floor(k * 2*pi / theta_r); the pair-r terms of cell (i,j)
+ *              are kept iff the distance i-j <= W_r ("ATFlash", The idea:
+ *              w_r = k*lambda_r, lambda_r = 2*pi/theta_r, terms beyond w_r are zero)
+ *   score    : s_ij = (1/sqrt(D)) * sum_r keep_r(i-j) * (q'_{i,r} k'_{j,r}
+ *                                   + q'_{i,r+D/2} k'_{j,r+D/2})
+ *   mask     : keys j > i are excluded before the softmax when causal
+ *              ("Attention block decomposition", Things that break;
+ *              "Flash Attention: Causal Prefill D=128", reverse traversal mask)
+ *   softmax  : m_i = max_j s_ij, p_ij = exp(s_ij - m_i), l_i = sum_j p_ij
+ *   output   : O_i = sum_j p_ij V_j / l_i,  LSE_i = m_i + ln l_i
+ *              ("AttnFuse", sec. 4.4: the forward keeps L = m + log l per row)
+ *   GQA      : query head h reads KV head floor(h / (Hq/Hkv))
+ *              ("AttnFuse", sec. 6.5 Llama-3-8B: Hq=32, Hkv=8)
+ *
+ * Positions are p = index + pos_offset for both Q and K (pos_offset is 0
+ * except in the relative-position shift test).
+ *
+ * Built with -ffp-contract=off so that x86 and Arm builds round alike.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static const double ORACLE_TWO_PI = 6.283185307179586476925286766559;
+
+static double bf16_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* theta_r = base^(-2r/D) */
+static void rope_thetas(int D, double base, double* theta) {
+    for (int r = 0; r < D / 2; ++r) theta[r] = pow(base, -2.0 * (double)r / (double)D);
+}
+
+/* W_r = floor(k * 2*pi / theta_r); +inf when the window is off (k <= 0 or k infinite). */
+void oracle_window_widths(int D, double rope_base, double window_k, double* w_out) {
+    double theta[512];
+    rope_thetas(D, rope_base, theta);
+    for (int r = 0; r < D / 2; ++r) {
+        if (!(window_k > 0.0) || isinf(window_k))
+            w_out[r] = INFINITY;
+        else
+            w_out[r] = floor(window_k * ORACLE_TWO_PI / theta[r]);
+    }
+}
+
+/* Rotate one bf16 vector x (length D, stride 1) at position pos into out (float64). */
+static void rope_rotate(const uint16_t* x, int D, const double* theta, double pos, int rope_on, double* out) {
+    int h = D / 2;
+    for (int r = 0; r < h; ++r) {
+        double a = bf16_to_f64(x[r]);
+        double b = bf16_to_f64(x[r + h]);
+        if (rope_on) {
+            double ang = pos * theta[r];
+            double c = cos(ang), s = sin(ang);
+            out[r] = a * c - b * s;
+            out[r + h] = b * c + a * s;
+        } else {
+            out[r] = a;
+            out[r + h] = b;
+        }
+    }
+}
+
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/*
+ * Attention output for a list of query rows.
+ *   q: [B][S][Hq][D] bf16 bits, k, v: [B][S][Hkv][D] bf16 bits (BSHD).
+ *   rows n = 0..n_rows-1 select (row_b[n], row_h[n], row_i[n]).
+ *   o_out: [n_rows][D] float64, lse_out: [n_rows] float64 (natural log).
+ *   rope_base <= 0: RoPE off.  window_k <= 0 or infinite: window off.
+ * Returns 0, or -1 on bad arguments (window without RoPE and causal masking,
+ * Hq not a multiple of Hkv, out-of-range rows).
+ */
+int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     int B, int Hq, int Hkv, int S, int D,
+                     int causal, double rope_base, double window_k, long long pos_offset,
+                     int n_rows, const int* row_b, const int* row_h, const int* row_i,
+                     double* o_out, double* lse_out) {
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 1024) return -1;
+    int rope_on = rope_base > 0.0;
+    int window_on = window_k > 0.0 && !isinf(window_k);
+    if (window_on && !(rope_on && causal)) return -1;
+    for (int n = 0; n < n_rows; ++n)
+        if (row_b[n] < 0 || row_b[n] >= B || row_h[n] < 0 || row_h[n] >= Hq || row_i[n] < 0 || row_i[n] >= S)
+            return -1;
+
+    const int G = Hq / Hkv;
+    const int half = D / 2;
+    double theta[512], W[512];
+    if (rope_on) rope_thetas(D, rope_base, theta);
+    oracle_window_widths(D, rope_on ? rope_base : 10000.0, window_on ? window_k : 0.0, W);
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+
+    /* Rows are handled one (batch, KV head) group at a time, so each group's
+       keys are rotated once and shared by its rows. */
+    char* done = (char*)calloc((size_t)n_rows, 1);
+    int* idx = (int*)malloc(sizeof(int) * (size_t)(n_rows > 0 ? n_rows : 1));
+    for (int first = 0; first < n_rows; ++first) {
+        if (done[first]) continue;
+        const int b = row_b[first];
+        const int g = row_h[first] / G;
+        int cnt = 0, max_key = 0;
+        for (int n = first; n < n_rows; ++n) {
+            if (!done[n] && row_b[n] == b && row_h[n] / G == g) {
+                idx[cnt++] = n;
+                done[n] = 1;
+                int last = causal ? row_i[n] : S - 1;
+                if (last > max_key) max_key = last;
+            }
+        }
+        const int nkeys = max_key + 1;
+        double* krot = (double*)malloc(sizeof(double) * (size_t)nkeys * (size_t)D);
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j < nkeys; ++j) {
+            const uint16_t* kj = k + (((size_t)b * S + j) * Hkv + g) * (size_t)D;
+            rope_rotate(kj, D, theta, (double)(j + pos_offset), rope_on, krot + (size_t)j * D);
+        }
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int t = 0; t < cnt; ++t) {
+            const int n = idx[t];
+            const int h = row_h[n], i = row_i[n];
+            const int last = causal ? i : S - 1;
+            double qrot[1024];
+            const uint16_t* qi = q + (((size_t)b * S + i) * Hq + h) * (size_t)D;
+            rope_rotate(qi, D, theta, (double)(i + pos_offset), rope_on, qrot);
+
+            /* 1. the full score row */
+            double* s = (double*)malloc(sizeof(double) * (size_t)(last + 1));
+            for (int j = 0; j <= last; ++j) {
+                const double* kj = krot + (size_t)j * D;
+                const double dist = (double)(i - j);
+                double acc = 0.0;
+                for (int r = 0; r < half; ++r) {
+                    if (window_on && !(dist <= W[r])) continue; /* pair r pruned at this distance */
+                    acc += qrot[r] * kj[r] + qrot[r + half] * kj[r + half];
+                }
+                s[j] = acc * inv_sqrt_d;
+            }
+            /* 2. row maximum */
+            double m = s[0];
+            for (int j = 1; j <= last; ++j)
+                if (s[j] > m) m = s[j];
+            /* 3. exponentials and their sum */
+            double l = 0.0;
+            for (int j = 0; j <= last; ++j) {
+                s[j] = exp(s[j] - m);
+                l += s[j];
+            }
+            /* 4. weighted sum of values, divided once by the sum */
+            double* o = o_out + (size_t)n * D;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            for (int j = 0; j <= last; ++j) {
+                const uint16_t* vj = v + (((size_t)b * S + j) * Hkv + g) * (size_t)D;
+                for (int d = 0; d < D; ++d) o[d] += s[j] * bf16_to_f64(vj[d]);
+            }
+            for (int d = 0; d < D; ++d) o[d] /= l;
+            lse_out[n] = m + log(l);
+            free(s);
+        }
+        free(krot);
+    }
+    free(idx);
+    free(done);
+    return 0;
+}
+
+/*
+ * Number of pruned (cell, pair) terms over the causal S x S triangle, counted
+ * cell by cell with the same keep rule the attention above uses: pair r of
+ * cell (i, j), j <= i, is pruned iff i - j > W_r.
+ */
+long long oracle_pruned_terms(int S, int D, double rope_base, double window_k) {
+    double W[512];
+    oracle_window_widths(D, rope_base, window_k, W);
+    long long count = 0;
+#pragma omp parallel for reduction(+ : count) schedule(dynamic, 16)
+    for (int i = 0; i < S; ++i)
+        for (int j = 0; j <= i; ++j) {
+            const double dist = (double)(i - j);
+            for (int r = 0; r < D / 2; ++r)
+                if (!(dist <= W[r])) ++count;
+        }
+    return count;
+}

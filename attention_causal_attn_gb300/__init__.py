@@ -1,0 +1,147 @@
+"""Python binding of libattn.so, the sm_103a fused RoPE + causal attention forward.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library (include/attn.h).  PyTorch supplies device memory and streams.  There
+is no fallback: if the library is missing or the device is not an sm_103
+GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import numpy as np
+
+from ._build import INCLUDE, LIB, build
+
+__all__ = ["attn_fwd", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+           "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
+
+ATTN_STATUS = {
+    "ATTN_OK": 0, "ATTN_ERR_NULL": -1, "ATTN_ERR_SHAPE": -2, "ATTN_ERR_ALIGN": -3,
+    "ATTN_ERR_UNSUPPORTED": -4, "ATTN_ERR_CUDA": -5, "ATTN_ERR_TIMEOUT": -6, "ATTN_ERR_OOM": -7,
+    "ATTN_ERR_NO_DEVICE": -8,
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {attn_error_string(code)} ({code})")
+        self.code = code
+
+
+def load_library(path: str | None = None):
+    """Load libattn.so (built by build()); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with attention_causal_attn_gb300.build()")
+        lib = ctypes.CDLL(p)
+        vp, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        lib.attn_fwd.restype = i
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
+        lib.attn_build_tables.restype = i
+        lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
+        lib.attn_check.restype = i
+        lib.attn_check.argtypes = [vp]
+        lib.attn_error_string.restype = ctypes.c_char_p
+        lib.attn_error_string.argtypes = [i]
+        lib.attn_release_cache.restype = None
+        lib.attn_release_cache.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/*.h."""
+    names = []
+    for fn in sorted(os.listdir(INCLUDE)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(INCLUDE, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def attn_error_string(code: int) -> str:
+    return load_library().attn_error_string(int(code)).decode()
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def attn_fwd(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=None, window_k=None,
+             return_lse: bool = True, stream=None):
+    """Fused RoPE + causal attention forward on BSHD bf16 CUDA tensors.
+
+    q [B, S, Hq, D], k and v [B, S, Hkv, D].  Returns (o, lse): o [B, S, Hq, D]
+    bf16 and lse [B, Hq, S] float32 (None when return_lse is False).  Runs on
+    `stream` (default: the current stream of q's device).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (BSHD)")
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, S, Hkv, D] with q's B, S and D")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()
+                                and tuple(lse.shape) == (B, Hq, S)):
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, Hq, S]")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr() if lse is not None else None,
+                          B, Hq, Hkv, S, D, int(bool(causal)),
+                          float(rope_base) if rope_base else 0.0,
+                          float(window_k) if window_k else 0.0,
+                          _stream_handle(stream, q.device))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_build_tables(S: int, D: int, rope_base: float, window_k=None, pos_offset: int = 0):
+    """Host RoPE tables cos/sin [S, D/2] (float32) and window widths W_r [D/2] (int32)."""
+    cos = np.zeros((S, D // 2), dtype=np.float32)
+    sin = np.zeros((S, D // 2), dtype=np.float32)
+    win = np.zeros(D // 2, dtype=np.int32)
+    rc = load_library().attn_build_tables(S, D, float(rope_base), float(window_k) if window_k else 0.0,
+                                          int(pos_offset), cos.ctypes.data, sin.ctypes.data, win.ctypes.data)
+    if rc != 0:
+        raise AttnError(rc, "attn_build_tables")
+    return cos, sin, win
+
+
+def attn_check(stream=None, device=None) -> None:
+    """Synchronise the stream and raise if a kernel reported a bounded-wait timeout."""
+    import torch
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        rc = load_library().attn_check(_stream_handle(stream, dev))
+    if rc != 0:
+        raise AttnError(rc, "attn_check")
+
+
+def attn_release_cache() -> None:
+    load_library().attn_release_cache()

@@ -1,0 +1,546 @@
+// Fused RoPE + causal attention forward for sm_103a (tcgen05 / TMEM / TMA).
+//
+// One persistent CTA per SM walks a host-built list of work units.  A unit is
+// two 128-row query tiles ("stages") that share one KV head, so every K/V tile
+// loaded into shared memory (and, with RoPE, every rotation of it) serves 256
+// query rows:
+//   - MHA: the two stages are consecutive query tiles of one head;
+//   - GQA: the two stages are two query heads of one KV group at the same tile.
+//
+// Warp roles (14 warps):
+//   warps 0-3   softmax stage 0: online softmax on S0 in TMEM, P0 back to TMEM,
+//               O0 rescale, epilogue (O/l -> bf16 -> global, LSE)
+//   warps 4-7   softmax stage 1 (same, on S1/P1/O1)
+//   warps 8-11  RoPE: rotate each loaded Q tile once and each loaded K tile in
+//               place ("AttnFuse", sec. 4.1: Q rotated once before the loop, K
+//               rotated tile by tile inside it), writing fp16 operands
+//   warp 12     TMA producer: Q tiles, then K/V tiles from the diagonal down to
+//               tile 0 ("Flash Attention: Causal Prefill D=128", reverse
+//               traversal isolates the causal mask to the first tile)
+//   warp 13     tcgen05 issuer (one thread) and TMEM owner
+//
+// TMEM (512 columns x 128 lanes x 32 bit): S0 [0,128), S1 [128,256), O0 [256,
+// 256+D), O1 [384, 384+D).  P_s (bf16, two per column) overwrites the first 64
+// columns of S_s once the softmax has read them; the PV product takes P from
+// TMEM as its A operand.
+//
+// Per stage, the issue order is PV_s(n+1) then S_s(n): the next QK^T of a stage
+// is queued behind the PV that reads its P, and the commit that reports S_s(n)
+// also covers PV_s(n+1), so the softmax may rescale O_s as soon as S_s(n) is
+// reported.  Softmax of one stage overlaps the tensor-core work of the other
+// (FlashAttention-3 style ping-pong, "AttnFuse" sec. 7 / "Fused Kernels on
+// Tensor Cores", FlashAttention-3 paragraph).
+//
+// Online softmax ("Flash Attention: Causal Prefill D=128", Online softmax):
+// scores stay raw in TMEM; with c = log2(e)/sqrt(D), P = exp2(S*c - m*c),
+// l = alpha*l + rowsum(P), O = alpha*O + P V, alpha = exp2((m_old - m_new)*c).
+// The running max used for P is only moved (and O, l rescaled) when the true
+// row max exceeds it by more than 8 in log2 units; P then stays below 2^8 and
+// the final O/l and LSE = ln2*(m*c + log2 l) are unchanged up to rounding.
+// One thread owns one query row (TMEM lane), so the row sums need no
+// cross-lane reduction at all.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kBlockM = 128;  // query rows per stage
+constexpr int kBlockN = 128;  // keys per KV tile
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr int kNumThreads = 448;
+constexpr int kWarpRope = 8;
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
+constexpr uint32_t kSubTileBytes = 128u * 128u;  // 128 rows x 128 B: one 64-wide bf16 column block
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// status word bits (OR-ed by the CTA whose wait ran out)
+constexpr int kStatusProducer = 1, kStatusRope = 2, kStatusMma = 4, kStatusSoftmax = 8, kStatusDrain = 16;
+
+struct FwdParams {
+    CUtensorMap tm_q;  // [B][S][Hq][D] bf16, box {64, 1, 128, 1}, 128B swizzle
+    CUtensorMap tm_k;  // [B][S][Hkv][D]
+    CUtensorMap tm_v;
+    __nv_bfloat16* o;   // [B][S][Hq][D]
+    float* lse;         // [B][Hq][S] or null
+    const float2* rope; // [S][D/2] (cos, sin), null when RoPE is off
+    const uint2* tasks; // unit words, see decode_unit
+    const int* task_off;// [gridDim.x + 1]: CTA c runs tasks[task_off[c] .. task_off[c+1])
+    int* status;
+    int B, Hq, Hkv, S;
+    float scale_log2;   // log2(e) / sqrt(D)
+    unsigned long long wait_limit_ns;
+};
+
+// barrier slots
+enum : int {
+    BAR_Q_FULL = 0,   // [2] TMA landed Q_s
+    BAR_Q_ROT = 2,    // [2] Q_s rotated (RoPE)
+    BAR_Q_EMPTY = 4,  // [2] last QK^T of the unit read Q_s
+    BAR_K_FULL = 6,   // [kKStages]
+    BAR_K_ROT = BAR_K_FULL + kKStages,
+    BAR_K_EMPTY = BAR_K_ROT + kKStages,
+    BAR_V_FULL = BAR_K_EMPTY + kKStages,  // [kVStages]
+    BAR_V_EMPTY = BAR_V_FULL + kVStages,
+    BAR_S_FULL = BAR_V_EMPTY + kVStages,  // [2] S_s(n) in TMEM (and PV_s(n+1) done)
+    BAR_P_FULL = BAR_S_FULL + 2,          // [2] P_s(n) in TMEM, O_s rescaled
+    BAR_O_FULL = BAR_P_FULL + 2,          // [2] last PV of the unit done
+    BAR_O_FREE = BAR_O_FULL + 2,          // [2] epilogue finished reading O_s
+    BAR_DRAIN = BAR_O_FREE + 2,
+    NUM_BARS = BAR_DRAIN + 1
+};
+
+template <int D>
+struct SmemLayout {
+    static constexpr uint32_t kTileBytes = 128u * D * 2u;
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = kQ + 2 * kTileBytes;
+    static constexpr uint32_t kV = kK + kKStages * kTileBytes;
+    static constexpr uint32_t kBars = kV + kVStages * kTileBytes;
+    static constexpr uint32_t kMisc = kBars + 8 * NUM_BARS;
+    static constexpr uint32_t kBytes = kMisc + 16;
+    static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+struct Unit {
+    int b, kvh;
+    int h[2], row0[2], nhi[2];
+    bool valid[2];
+    int nmax;
+};
+
+// Unit word: x = qtile0 | qtile1 << 16 (0xFFFF = no stage), y = h0 | h1 << 8 | b << 16.
+__device__ __forceinline__ Unit decode_unit(uint2 w, const FwdParams& p, bool causal) {
+    Unit u;
+    const int qt[2] = {static_cast<int>(w.x & 0xFFFFu), static_cast<int>(w.x >> 16)};
+    u.h[0] = static_cast<int>(w.y & 0xFFu);
+    u.h[1] = static_cast<int>((w.y >> 8) & 0xFFu);
+    u.b = static_cast<int>(w.y >> 16);
+    u.kvh = u.h[0] / (p.Hq / p.Hkv);
+    const int last_tile = (p.S - 1) / kBlockN;
+    u.nmax = -1;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        u.valid[s] = qt[s] != 0xFFFF && qt[s] * kBlockM < p.S;
+        u.row0[s] = qt[s] * kBlockM;
+        u.nhi[s] = causal ? qt[s] : last_tile;
+        if (u.valid[s] && u.nhi[s] > u.nmax) u.nmax = u.nhi[s];
+    }
+    return u;
+}
+
+__device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int i) { return bar0 + 8u * static_cast<uint32_t>(i); }
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, int t_begin, int t_end,
+                              const WaitCtl& ctl) {
+    using L = SmemLayout<D>;
+    int kit = 0, vit = 0;
+    int qit[2] = {0, 0};
+    for (int ti = t_begin; ti < t_end; ++ti) {
+        const Unit u = decode_unit(p.tasks[ti], p, causal);
+        for (int s = 0; s < 2; ++s) {
+            if (!u.valid[s]) continue;
+            if (!mbar_wait(bar_at(bar0, BAR_Q_EMPTY + s), (qit[s] & 1) ^ 1, ctl, kStatusProducer)) return;
+            const uint32_t fb = bar_at(bar0, BAR_Q_FULL + s);
+            mbar_arrive_expect_tx(fb, L::kTileBytes);
+            for (int sub = 0; sub < D / 64; ++sub)
+                tma_load_4d(sm + L::kQ + s * L::kTileBytes + sub * kSubTileBytes, &p.tm_q, fb, sub * 64, u.h[s],
+                            u.row0[s], u.b);
+            ++qit[s];
+        }
+        for (int n = u.nmax; n >= 0; --n) {
+            const int ks = kit % kKStages;
+            if (!mbar_wait(bar_at(bar0, BAR_K_EMPTY + ks), ((kit / kKStages) & 1) ^ 1, ctl, kStatusProducer)) return;
+            const uint32_t kb = bar_at(bar0, BAR_K_FULL + ks);
+            mbar_arrive_expect_tx(kb, L::kTileBytes);
+            for (int sub = 0; sub < D / 64; ++sub)
+                tma_load_4d(sm + L::kK + ks * L::kTileBytes + sub * kSubTileBytes, &p.tm_k, kb, sub * 64, u.kvh,
+                            n * kBlockN, u.b);
+            ++kit;
+            const int vs = vit % kVStages;
+            if (!mbar_wait(bar_at(bar0, BAR_V_EMPTY + vs), ((vit / kVStages) & 1) ^ 1, ctl, kStatusProducer)) return;
+            const uint32_t vb = bar_at(bar0, BAR_V_FULL + vs);
+            mbar_arrive_expect_tx(vb, L::kTileBytes);
+            for (int sub = 0; sub < D / 64; ++sub)
+                tma_load_4d(sm + L::kV + vs * L::kTileBytes + sub * kSubTileBytes, &p.tm_v, vb, sub * 64, u.kvh,
+                            n * kBlockN, u.b);
+            ++vit;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ RoPE
+// Rotate one 128-row tile in place.  The tile is stored as D/64 column blocks
+// of [128 rows][128 B] with the 128-byte swizzle (16-byte chunk c of row r
+// sits at chunk c ^ (r & 7)).  Pair (r, r + D/2) has both members at the same
+// swizzled offset in column blocks 0 and 1 for D = 128, and in chunks c and
+// c + 4 of the single block for D = 64.  Input bf16, math fp32, output fp16.
+template <int D>
+__device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, int pos0, const FwdParams& p, int t) {
+    constexpr int kHalf = D / 2;
+    constexpr int kChunks = kHalf / 8;  // 16-byte chunks per half row
+    for (int it = t; it < kBlockM * kChunks; it += 128) {
+        const int row = it / kChunks;
+        const int c = it % kChunks;
+        const int pos = min(pos0 + row, p.S - 1);  // rows past S are zero-filled; any angle leaves them zero
+        uint32_t lo_off, hi_off;
+        if (D == 128) {
+            lo_off = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
+            hi_off = lo_off + kSubTileBytes;
+        } else {
+            lo_off = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
+            hi_off = static_cast<uint32_t>(row * 128 + (((c + 4) ^ (row & 7)) << 4));
+        }
+        uint4 lo = *reinterpret_cast<const uint4*>(tile + lo_off);
+        uint4 hi = *reinterpret_cast<const uint4*>(tile + hi_off);
+        const float4* cs = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(pos) * kHalf + c * 8);
+        float4 t4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t4[k] = __ldg(cs + k);
+        const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
+        const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+        uint32_t lo_out[4], hi_out[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            // elements 2k (low half of the word) and 2k+1 (high half)
+            const float x0 = bf16_lo(lw[k]), x1 = bf16_hi(lw[k]);
+            const float y0 = bf16_lo(hw[k]), y1 = bf16_hi(hw[k]);
+            const float c0 = t4[k].x, s0 = t4[k].y, c1 = t4[k].z, s1 = t4[k].w;
+            const float xr0 = x0 * c0 - y0 * s0, yr0 = y0 * c0 + x0 * s0;
+            const float xr1 = x1 * c1 - y1 * s1, yr1 = y1 * c1 + x1 * s1;
+            lo_out[k] = pack_f16x2(xr0, xr1);
+            hi_out[k] = pack_f16x2(yr0, yr1);
+        }
+        *reinterpret_cast<uint4*>(tile + lo_off) = make_uint4(lo_out[0], lo_out[1], lo_out[2], lo_out[3]);
+        *reinterpret_cast<uint4*>(tile + hi_off) = make_uint4(hi_out[0], hi_out[1], hi_out[2], hi_out[3]);
+    }
+}
+
+template <int D>
+__device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_t bar0, int t_begin, int t_end,
+                          const WaitCtl& ctl, int t) {
+    using L = SmemLayout<D>;
+    int kit = 0;
+    int qit[2] = {0, 0};
+    for (int ti = t_begin; ti < t_end; ++ti) {
+        const Unit u = decode_unit(p.tasks[ti], p, causal);
+        for (int s = 0; s < 2; ++s) {
+            if (!u.valid[s]) continue;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_at(bar0, BAR_Q_FULL + s), qit[s] & 1, ctl, kStatusRope)))
+                return;
+            rope_rotate_tile<D>(smg + L::kQ + s * L::kTileBytes, u.row0[s], p, t);
+            fence_proxy_async_smem();
+            mbar_arrive(bar_at(bar0, BAR_Q_ROT + s));
+            ++qit[s];
+        }
+        for (int n = u.nmax; n >= 0; --n) {
+            const int ks = kit % kKStages;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(bar_at(bar0, BAR_K_FULL + ks), (kit / kKStages) & 1, ctl, kStatusRope)))
+                return;
+            rope_rotate_tile<D>(smg + L::kK + ks * L::kTileBytes, n * kBlockN, p, t);
+            fence_proxy_async_smem();
+            mbar_arrive(bar_at(bar0, BAR_K_ROT + ks));
+            ++kit;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int D, bool ROPE>
+__device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, uint32_t tmem, int t_begin,
+                         int t_end, const WaitCtl& ctl) {
+    using L = SmemLayout<D>;
+    // QK^T: A = Q tile, B = K tile, both K-major; fp16 after rotation, bf16 otherwise.
+    constexpr uint32_t kIdescQK = umma_idesc_f16(ROPE ? 0u : 1u, 0u, kBlockM, kBlockN);
+    // PV: A = P (bf16, TMEM), B = V tile [keys][D] with D contiguous: MN-major.
+    constexpr uint32_t kIdescPV = umma_idesc_f16(1u, 1u, kBlockM, D);
+    const int kbar_ready = ROPE ? BAR_K_ROT : BAR_K_FULL;
+    const int qbar_ready = ROPE ? BAR_Q_ROT : BAR_Q_FULL;
+
+    int kit = 0, vit = 0;
+    int qit[2] = {0, 0}, pit[2] = {0, 0}, oit[2] = {0, 0};
+    bool ok = true;
+    for (int ti = t_begin; ti < t_end && ok; ++ti) {
+        const Unit u = decode_unit(p.tasks[ti], p, causal);
+        bool first_pv[2] = {true, true};
+        for (int n = u.nmax; n >= -1 && ok; --n) {
+            const int ks = kit % kKStages;
+            const int vs = vit % kVStages;
+            const bool do_s = n >= 0;
+            const bool do_pv = n + 1 <= u.nmax;
+            if (do_s) {
+                ok = mbar_wait(bar_at(bar0, kbar_ready + ks), (kit / kKStages) & 1, ctl, kStatusMma);
+                if (!ok) break;
+            }
+            if (do_pv) {
+                ok = mbar_wait(bar_at(bar0, BAR_V_FULL + vs), (vit / kVStages) & 1, ctl, kStatusMma);
+                if (!ok) break;
+            }
+            tc_fence_after();
+            for (int s = 0; s < 2 && ok; ++s) {
+                if (!u.valid[s]) continue;
+                const uint32_t tS = tmem + static_cast<uint32_t>(s * 128);
+                const uint32_t tO = tmem + 256u + static_cast<uint32_t>(s * 128);
+                if (do_pv && n + 1 <= u.nhi[s]) {
+                    ok = mbar_wait(bar_at(bar0, BAR_P_FULL + s), pit[s] & 1, ctl, kStatusMma);
+                    if (!ok) break;
+                    ++pit[s];
+                    if (first_pv[s]) {
+                        ok = mbar_wait(bar_at(bar0, BAR_O_FREE + s), (oit[s] & 1) ^ 1, ctl, kStatusMma);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vbase = sm + L::kV + vs * L::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        const uint64_t bdesc = sw128_desc(vbase + kk * 2048u, kSubTileBytes, 1024u);
+                        umma_ts(tO, tS + kk * 8u, bdesc, kIdescPV, (first_pv[s] && kk == 0) ? 0u : 1u);
+                    }
+                    first_pv[s] = false;
+                }
+                if (do_s && n <= u.nhi[s]) {
+                    if (n == u.nhi[s]) {
+                        ok = mbar_wait(bar_at(bar0, qbar_ready + s), qit[s] & 1, ctl, kStatusMma);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const uint32_t qbase = sm + L::kQ + s * L::kTileBytes;
+                    const uint32_t kbase = sm + L::kK + ks * L::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * kSubTileBytes + (kk % 4) * 32u;
+                        umma_ss(tS, sw128_desc(qbase + off, 16u, 1024u), sw128_desc(kbase + off, 16u, 1024u),
+                                kIdescQK, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar_at(bar0, BAR_S_FULL + s));
+                    if (n == 0) {
+                        tc_commit(bar_at(bar0, BAR_Q_EMPTY + s));
+                        ++qit[s];
+                    }
+                }
+            }
+            if (!ok) break;
+            if (do_s) {
+                tc_commit(bar_at(bar0, BAR_K_EMPTY + ks));
+                ++kit;
+            }
+            if (do_pv) {
+                tc_commit(bar_at(bar0, BAR_V_EMPTY + vs));
+                ++vit;
+            }
+        }
+        if (!ok) break;
+        for (int s = 0; s < 2; ++s) {
+            if (!u.valid[s]) continue;
+            tc_commit(bar_at(bar0, BAR_O_FULL + s));
+            ++oit[s];
+        }
+    }
+    // Drain: every issued MMA must finish before TMEM is released.  This wait
+    // ignores the abort flag but keeps its own time limit.
+    tc_commit(bar_at(bar0, BAR_DRAIN));
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar_at(bar0, BAR_DRAIN), 0)) {
+        if (global_timer_ns() - t0 > ctl.limit_ns) {
+            atomicOr(ctl.status, kStatusDrain);
+            break;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+template <int D, bool CAUSAL>
+__device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint32_t tmem, int t_begin, int t_end,
+                             const WaitCtl& ctl, int t) {
+    const uint32_t lane_base = static_cast<uint32_t>(t & ~31);  // this warp's TMEM lane quarter
+    const uint32_t trow = tmem + (lane_base << 16);
+    const uint32_t colS = static_cast<uint32_t>(stage * 128);
+    const uint32_t colO = 256u + static_cast<uint32_t>(stage * 128);
+    const float c = p.scale_log2;
+    const int last_tile = (p.S - 1) / kBlockN;
+    int sit = 0, oit = 0;
+    for (int ti = t_begin; ti < t_end; ++ti) {
+        const Unit u = decode_unit(p.tasks[ti], p, CAUSAL);
+        if (!u.valid[stage]) continue;
+        const int row = u.row0[stage] + t;
+        float m_used = -INFINITY;
+        float l = 0.f;
+        for (int n = u.nhi[stage]; n >= 0; --n) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(bar_at(bar0, BAR_S_FULL + stage), sit & 1, ctl, kStatusSoftmax << stage)))
+                return;
+            ++sit;
+            tc_fence_after();
+            int limit = kBlockN;  // keys [0, limit) of this tile are visible to this row
+            if (CAUSAL && n == u.nhi[stage]) limit = t + 1;
+            if (n == last_tile) limit = min(limit, p.S - n * kBlockN);
+            // pass 1: masked row maximum of the raw scores
+            float mx = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < kBlockN; cc += 64) {
+                uint32_t r[64];
+                tmem_load_64(trow + colS + cc, r);
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (cc + j < limit) mx = fmaxf(mx, __uint_as_float(r[j]));
+            }
+            const float m_new = fmaxf(m_used, mx);
+            if (n == u.nhi[stage]) {
+                m_used = m_new;
+            } else {
+                const bool need = (m_new - m_used) * c > kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = ex2_approx((m_used - m_new) * c);
+                        m_used = m_new;
+                        l *= alpha;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t r[32];
+                        tmem_load_32(trow + colO + cc, r);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+                        tmem_store_32(trow + colO + cc, r);
+                    }
+                }
+            }
+            // pass 2: P = exp2(S*c - m*c), masked keys 0; l += rowsum(P); P -> bf16 pairs in TMEM
+            const float mc = m_used * c;
+            float sum = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kBlockN; cc += 32) {
+                uint32_t r[32];
+                tmem_load_32(trow + colS + cc, r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const float p0 = (cc + j < limit) ? ex2_approx(fmaf(__uint_as_float(r[j]), c, -mc)) : 0.f;
+                    const float p1 = (cc + j + 1 < limit) ? ex2_approx(fmaf(__uint_as_float(r[j + 1]), c, -mc)) : 0.f;
+                    sum += p0 + p1;
+                    pk[j / 2] = pack_bf16x2(p0, p1);
+                }
+                tmem_store_16(trow + colS + cc / 2, pk);
+            }
+            l += sum;
+            tmem_store_wait();
+            tc_fence_before();
+            mbar_arrive(bar_at(bar0, BAR_P_FULL + stage));
+        }
+        // epilogue: O / l in bf16, LSE in natural log
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar_at(bar0, BAR_O_FULL + stage), oit & 1, ctl, kStatusSoftmax << stage)))
+            return;
+        ++oit;
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const bool row_ok = row < p.S;
+        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.S + row) * p.Hq + u.h[stage]) * D;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+            uint32_t r[32];
+            tmem_load_32(trow + colO + cc, r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv_l, __uint_as_float(r[2 * j + 1]) * inv_l);
+            if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            }
+        }
+        if (row_ok && p.lse != nullptr)
+            p.lse[(static_cast<size_t>(u.b) * p.Hq + u.h[stage]) * p.S + row] =
+                (m_used * c + log2f(l)) * 0.69314718055994531f;
+        tc_fence_before();
+        mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, bool CAUSAL, bool ROPE>
+__global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using L = SmemLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sm = smem_addr(smg);
+    const uint32_t bar0 = sm + L::kBars;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smg + L::kMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smg + L::kMisc + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_at(bar0, BAR_Q_FULL + s), 1);
+            mbar_init(bar_at(bar0, BAR_Q_ROT + s), 128);
+            mbar_init(bar_at(bar0, BAR_Q_EMPTY + s), 1);
+            mbar_init(bar_at(bar0, BAR_S_FULL + s), 1);
+            mbar_init(bar_at(bar0, BAR_P_FULL + s), 128);
+            mbar_init(bar_at(bar0, BAR_O_FULL + s), 1);
+            mbar_init(bar_at(bar0, BAR_O_FREE + s), 128);
+        }
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(bar_at(bar0, BAR_K_FULL + i), 1);
+            mbar_init(bar_at(bar0, BAR_K_ROT + i), 128);
+            mbar_init(bar_at(bar0, BAR_K_EMPTY + i), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(bar_at(bar0, BAR_V_FULL + i), 1);
+            mbar_init(bar_at(bar0, BAR_V_EMPTY + i), 1);
+        }
+        mbar_init(bar_at(bar0, BAR_DRAIN), 1);
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns};
+    const int t_begin = p.task_off[blockIdx.x];
+    const int t_end = p.task_off[blockIdx.x + 1];
+
+    if (warp < 8) {
+        softmax_role<D, CAUSAL>(p, warp / 4, bar0, tmem, t_begin, t_end, ctl, threadIdx.x % 128);
+    } else if (warp < kWarpTma) {
+        if (ROPE) rope_role<D>(p, CAUSAL, smg, bar0, t_begin, t_end, ctl, threadIdx.x - kWarpRope * 32);
+    } else if (warp == kWarpTma) {
+        if (lane == 0) producer_role<D>(p, CAUSAL, sm, bar0, t_begin, t_end, ctl);
+        __syncwarp();
+    } else {
+        if (lane == 0) mma_role<D, ROPE>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace attn

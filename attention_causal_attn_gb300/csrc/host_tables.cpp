@@ -1,0 +1,128 @@
+#include "host_tables.h"
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <numeric>
+#include <queue>
+#include <tuple>
+
+namespace attn_host {
+
+namespace {
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr int kTile = 128;
+constexpr uint32_t kNoTile = 0xFFFFu;
+}  // namespace
+
+std::vector<double> rope_thetas(int D, double base) {
+    std::vector<double> th(static_cast<size_t>(D / 2));
+    for (int r = 0; r < D / 2; ++r) th[r] = std::pow(base, -2.0 * static_cast<double>(r) / static_cast<double>(D));
+    return th;
+}
+
+std::vector<float> rope_table(int S, int D, double base, long long pos_offset) {
+    const int half = D / 2;
+    const std::vector<double> th = rope_thetas(D, base);
+    std::vector<float> t(static_cast<size_t>(S) * half * 2);
+    for (int p = 0; p < S; ++p) {
+        const double pos = static_cast<double>(p + pos_offset);
+        for (int r = 0; r < half; ++r) {
+            const double a = pos * th[r];
+            t[(static_cast<size_t>(p) * half + r) * 2 + 0] = static_cast<float>(std::cos(a));
+            t[(static_cast<size_t>(p) * half + r) * 2 + 1] = static_cast<float>(std::sin(a));
+        }
+    }
+    return t;
+}
+
+std::vector<int32_t> window_widths(int D, double base, double k) {
+    std::vector<int32_t> w(static_cast<size_t>(D / 2), INT32_MAX);
+    if (!(k > 0.0) || std::isinf(k)) return w;
+    const std::vector<double> th = rope_thetas(D, base);
+    for (int r = 0; r < D / 2; ++r) {
+        const double x = std::floor(k * kTwoPi / th[r]);
+        w[r] = x >= static_cast<double>(INT32_MAX) ? INT32_MAX : static_cast<int32_t>(std::max(0.0, x));
+    }
+    return w;
+}
+
+Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas) {
+    struct U {
+        uint32_t x, y;
+        double cost;
+        int b, kvh, h, qt;
+    };
+    const int nqt = (S + kTile - 1) / kTile;
+    const int G = Hq / Hkv;
+    auto tile_cost = [&](int qt) { return 2.0 * ((causal ? qt : nqt - 1) + 1); };
+    std::vector<U> units;
+    if (G >= 2) {
+        // two query heads of one KV group at the same query tile
+        for (int b = 0; b < B; ++b)
+            for (int g = 0; g < Hkv; ++g)
+                for (int qt = 0; qt < nqt; ++qt)
+                    for (int h = g * G; h < (g + 1) * G; h += 2) {
+                        const bool pair = h + 1 < (g + 1) * G;
+                        U u;
+                        u.x = static_cast<uint32_t>(qt) | ((pair ? static_cast<uint32_t>(qt) : kNoTile) << 16);
+                        u.y = static_cast<uint32_t>(h) | (static_cast<uint32_t>(pair ? h + 1 : h) << 8) |
+                              (static_cast<uint32_t>(b) << 16);
+                        u.cost = tile_cost(qt) * (pair ? 2 : 1) + 4.0;
+                        u.b = b, u.kvh = g, u.h = h, u.qt = qt;
+                        units.push_back(u);
+                    }
+    } else {
+        // two consecutive query tiles of one head
+        for (int b = 0; b < B; ++b)
+            for (int h = 0; h < Hq; ++h)
+                for (int t = 0; 2 * t < nqt; ++t) {
+                    const int q0 = 2 * t, q1 = 2 * t + 1;
+                    const bool pair = q1 < nqt;
+                    U u;
+                    u.x = static_cast<uint32_t>(q0) | ((pair ? static_cast<uint32_t>(q1) : kNoTile) << 16);
+                    u.y = static_cast<uint32_t>(h) | (static_cast<uint32_t>(h) << 8) | (static_cast<uint32_t>(b) << 16);
+                    u.cost = tile_cost(q0) + (pair ? tile_cost(q1) : 0.0) + 4.0;
+                    u.b = b, u.kvh = h, u.h = h, u.qt = q0;
+                    units.push_back(u);
+                }
+    }
+    Schedule sc;
+    const int n = static_cast<int>(units.size());
+    sc.ctas = std::max(1, std::min(num_ctas, n));
+    // longest-processing-time-first into the least loaded CTA
+    std::vector<int> order(n);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return units[a].cost > units[b].cost; });
+    using Load = std::pair<double, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int c = 0; c < sc.ctas; ++c) heap.push({0.0, c});
+    std::vector<std::vector<int>> bins(sc.ctas);
+    std::vector<double> load(sc.ctas, 0.0);
+    for (int i : order) {
+        Load top = heap.top();
+        heap.pop();
+        bins[top.second].push_back(i);
+        top.first += units[i].cost;
+        load[top.second] = top.first;
+        heap.push(top);
+    }
+    sc.offsets.push_back(0);
+    for (int c = 0; c < sc.ctas; ++c) {
+        auto& bin = bins[c];
+        std::stable_sort(bin.begin(), bin.end(), [&](int a, int b) {
+            const U &ua = units[a], &ub = units[b];
+            return std::make_tuple(ua.b, ua.kvh, ua.h, -ua.qt) < std::make_tuple(ub.b, ub.kvh, ub.h, -ub.qt);
+        });
+        for (int i : bin) {
+            sc.words.push_back(units[i].x);
+            sc.words.push_back(units[i].y);
+        }
+        sc.offsets.push_back(static_cast<int32_t>(sc.words.size() / 2));
+    }
+    sc.max_cost = *std::max_element(load.begin(), load.end());
+    sc.mean_cost = std::accumulate(load.begin(), load.end(), 0.0) / sc.ctas;
+    return sc;
+}
+
+}  // namespace attn_host

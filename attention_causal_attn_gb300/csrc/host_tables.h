@@ -1,0 +1,37 @@
+// Host-side tables and the static tile schedule of the attention forward.
+// Plain C++ (no CUDA): compiled by the host compiler and unit-tested through
+// the C ABI without a GPU.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+namespace attn_host {
+
+// theta_r = base^(-2r/D), r = 0..D/2-1 (RoFormer's frequencies, NeoX pairing r <-> r + D/2).
+std::vector<double> rope_thetas(int D, double base);
+
+// (cos, sin) of (p + pos_offset) * theta_r for p = 0..S-1, interleaved as
+// [S][D/2][2] float32, computed in float64.
+std::vector<float> rope_table(int S, int D, double base, long long pos_offset);
+
+// W_r = floor(k * 2*pi / theta_r) clamped to [0, INT32_MAX]; INT32_MAX when
+// the window is off (k <= 0 or infinite).  ("ATFlash", The idea.)
+std::vector<int32_t> window_widths(int D, double base, double k);
+
+// One work unit = two 128-row query tiles sharing a KV head, encoded as the
+// kernel reads it: x = qtile0 | qtile1 << 16 (0xFFFF: no second tile),
+// y = h0 | h1 << 8 | b << 16.
+struct Schedule {
+    std::vector<uint32_t> words;  // 2 per unit, in per-CTA order
+    std::vector<int32_t> offsets; // ctas + 1 prefix offsets into units
+    int ctas = 0;
+    double max_cost = 0, mean_cost = 0;  // per-CTA estimated cost
+};
+
+// Cost-guided static schedule ("Flash Attention: Causal Prefill D=128", Step 4:
+// estimated cost 2(bm+1) + 4 per query tile, heaviest units first into the
+// lightest CTA, then each CTA's list ordered by batch/head for K/V locality).
+Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas);
+
+}  // namespace attn_host

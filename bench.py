@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""Benchmark of the fused RoPE + causal attention forward (prefill).
+
+One step = one call of the whole hot path (attn_fwd) over one batch of the
+workload.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Metric: causal attention forward TFLOP/s, counting the useful causal QK^T and
+PV work 2*B*Hq*S^2*D per step ("Flash Attention: Causal Prefill D=128",
+Performance measurements: TFLOPS = 2*B*H*S*S*D / (ms*1e9)).  With N > 1
+(torchrun) every rank runs its own independent batch of the same shape (the
+path shards by batch and head with no exchange), `value` is the job total.
+
+--impl reference times the float64 CPU oracle on the host cores instead, one
+bounded sample of query rows per step, on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "causal attn fwd TFLOP/s at S=8192 D=128 bf16; % of GB300 dense BF16 peak"
+DEFAULT_WORKLOAD = "rope_causal_s8192"
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0  # GB300 dense bf16/fp16 tensor peak (the 2:4-sparse figure is twice this)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def useful_flops(w):
+    return 2.0 * w["B"] * w["Hq"] * w["S"] * w["S"] * w["D"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(name, w):
+    cfg = {"workload": name, "B": w["B"], "Hq": w["Hq"], "Hkv": w["Hkv"], "S": w["S"], "D": w["D"],
+           "causal": w["causal"], "rope_base": w["rope_base"], "window_k": w["window_k"],
+           "outlier_channels": w["outliers"], "layout": "BSHD", "inputs": "seeded iid N(0,1) bf16"}
+    return cfg
+
+
+# --------------------------------------------------------------------- CPU oracle timing
+def time_oracle(q, k, v, w, budget_s, seed=si.MASTER_SEED):
+    """Time the float64 oracle on a bounded sample of query rows; returns (TFLOP/s, seconds, sample, threads)."""
+    import oracle
+    B, Hq, Hkv, S = w["B"], w["Hq"], w["Hkv"], w["S"]
+    heads = si.sample_heads(seed, B, Hq, Hkv, 8)
+    nrows = 4
+    spent = 0.0
+    total_flops = 0.0
+    total_time = 0.0
+    rows_done = 0
+    while True:
+        rows = si.sample_rows(seed + nrows, S, nrows)
+        rb = np.repeat([b for b, _ in heads], len(rows))
+        rh = np.repeat([h for _, h in heads], len(rows))
+        ri = np.tile(rows, len(heads))
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, rb, rh, ri, causal=w["causal"], rope_base=w["rope_base"],
+                         window_k=w["window_k"])
+        dt = time.perf_counter() - t0
+        keys = (ri.astype(np.float64) + 1.0) if w["causal"] else np.full(len(ri), float(S))
+        total_flops += float(np.sum(4.0 * w["D"] * keys))
+        total_time += dt
+        rows_done += len(ri)
+        spent += dt
+        if spent >= budget_s or nrows >= S:
+            break
+        nrows = min(S, max(nrows * 2, int(nrows * min(8.0, 0.5 * budget_s / max(dt, 1e-3)))))
+    sample = (f"{rows_done} query rows of {len(heads)} seeded (batch, head) pairs, useful work "
+              f"4*D*(keys) per row, {total_time:.1f} s")
+    return total_flops / total_time / 1e12, total_time, sample, oracle.threads()
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- our arm
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import attention_causal_attn_gb300 as attn
+
+    attn.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    B, Hq, Hkv, S, D = w["B"], w["Hq"], w["Hkv"], w["S"], w["D"]
+    seed = si.MASTER_SEED + rank  # every rank its own independent batch
+    q_h, k_h, v_h = si.make_qkv(B, Hq, Hkv, S, D, outliers=w["outliers"], seed=seed)
+    to_pinned = lambda a: torch.from_numpy(a).view(torch.bfloat16).pin_memory()
+    q_p, k_p, v_p = to_pinned(q_h), to_pinned(k_h), to_pinned(v_h)
+    q, k, v = q_p.to(dev), k_p.to(dev), v_p.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(causal=w["causal"], rope_base=w["rope_base"], window_k=w["window_k"], stream=stream)
+
+    def step():
+        attn.attn_fwd(q, k, v, o, lse, **kw)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    attn.attn_check(stream=stream, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # device-timed region: K back-to-back steps, events on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_end.record(stream)
+        barrier()
+    attn.attn_check(stream=stream, device=dev)
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    # end-to-end through the public API with pinned host buffers
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        qd = q_p.to(dev, non_blocking=True)
+        kd = k_p.to(dev, non_blocking=True)
+        vd = v_p.to(dev, non_blocking=True)
+        attn.attn_fwd(qd, kd, vd, o, lse, **kw)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    times = torch.tensor([elapsed_ms, e2e_ms, float(np.mean(launch_ms))], device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms, launch_avg_ms = times.tolist()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, secs, sample, threads = time_oracle(q_h, k_h, v_h, w, args.cpu_budget)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    flops = useful_flops(w)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (launch_avg_ms * 1e-3) / 1e12
+    in_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
+    out_bytes = o.numel() * 2 + lse.numel() * 4
+    cfg = workload_config(args.workload, w)
+    cfg["l2"] = f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step vs 129 MB L2), no flush"
+    cfg["timing"] = f"CUDA events on the launching stream, {args.steps} steps after {max(args.warmup, 3)} warm-up"
+    traffic = load_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": cfg,
+        "pct_of_peak": {"measured_bf16_burst": round(value / world / peak, 4),
+                        "nominal_dense_bf16": round(value / world / NOMINAL_DENSE_BF16_TFLOPS, 4),
+                        "peak_kind": peak_kind},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "attn_fwd_kernel", "peak_source": f"bf16_tflops ({peak_kind}, burst)",
+                     "algorithmic": "2*B*Hq*S^2*D useful causal FLOPs per launch"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    return line
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and workload, if present."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_kernel_{workload}.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha") == kernel_source_sha():
+            return d.get("dram_bytes_per_launch")
+    return None
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_causal_attn_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".inc", ".h", ".cpp")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args, w, rank):
+    if rank != 0:
+        return None
+    q_h, k_h, v_h = si.make_qkv(w["B"], w["Hq"], w["Hkv"], w["S"], w["D"], outliers=w["outliers"])
+    per_step = max(0.5, args.ref_budget / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        time_oracle(q_h, k_h, v_h, w, per_step, seed=si.MASTER_SEED + 1000 + i)
+    vals, secs, sample, threads = [], 0.0, "", 1
+    for i in range(args.steps):
+        tf, s, sample, threads = time_oracle(q_h, k_h, v_h, w, per_step, seed=si.MASTER_SEED + i)
+        vals.append(tf)
+        secs += s
+    value = float(np.mean(vals))
+    flops = useful_flops(w)
+    cfg = workload_config(args.workload, w)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": flops / (value * 1e12) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {sample}; ms_per_step extrapolated from the sampled rate"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--window-k", type=float, default=None, help="override the workload's window multiplier")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle time for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = dict(si.WORKLOADS[args.workload])
+    if args.window_k is not None:
+        w["window_k"] = args.window_k if args.window_k > 0 else None
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, w, rank)
+    else:
+        line = run_ours(args, w, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,115 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) fused RoPE + causal attention forward.
+ *
+ * One operation: the prefill attention forward of a decoder layer,
+ *
+ *   O = softmax(mask(RoPE(Q) RoPE(K)^T / sqrt(D))) V,   LSE_i = m_i + ln l_i,
+ *
+ * with RoPE applied to Q and K pair by pair as their tiles are loaded
+ * ("AttnFuse: A Composable DSL for Compiling Attentions to Fused GPU Kernels",
+ * sec. 4.1 Fused RoPE), the causal mask applied before the softmax, an exp2
+ * online softmax with scale log2(e)/sqrt(D) ("Flash Attention: Causal Prefill
+ * D=128", Online softmax: what must remain invariant), P.V accumulated in fp32
+ * with P rounded to bf16, and one LSE value per query row ("AttnFuse", sec. 4.4
+ * Backward Pass: the forward keeps L = m + log l).  An optional per-RoPE-pair
+ * distance window drops pair r's QK terms beyond w_r = k * 2*pi/theta_r
+ * ("ATFlash — Per-RoPE-Wavelength Attention Windows", The idea).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are BSHD: q and o are [B][S][Hq][D], k and v are [B][S][Hkv][D],
+ *     contiguous, bfloat16, device pointers, 16-byte aligned.
+ *   - lse is float32 [B][Hq][S] (natural log), device pointer, or NULL.
+ *   - Query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
+ *   - RoPE pairs dimension r with r + D/2 (NeoX half split), theta_r =
+ *     base^(-2r/D), positions 0..S-1 for both Q and K.
+ *   - The caller owns every buffer it passes.  The library owns only cached
+ *     device tables (cos/sin, tile schedules) that it builds on the first call
+ *     for a given shape and frees in attn_release_cache().
+ *   - stream is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  attn_fwd is asynchronous on that stream.
+ *   - Return values are attn_status codes; attn_error_string() names them.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = -1,        /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = -2,       /* B, S, H or D out of range, or Hq not a multiple of Hkv */
+    ATTN_ERR_ALIGN = -3,       /* a tensor pointer is not 16-byte aligned */
+    ATTN_ERR_UNSUPPORTED = -4, /* a combination the kernel does not implement */
+    ATTN_ERR_CUDA = -5,        /* a CUDA runtime or driver call failed */
+    ATTN_ERR_TIMEOUT = -6,     /* a bounded in-kernel wait ran out (see attn_check) */
+    ATTN_ERR_OOM = -7,         /* the library could not allocate its cached tables */
+    ATTN_ERR_NO_DEVICE = -8    /* no sm_103 device is current */
+} attn_status;
+
+/*
+ * attn_fwd — fused RoPE + causal attention forward (prefill).
+ *
+ *   q, k, v     bf16 device tensors, BSHD, see above.
+ *   o           bf16 device output [B][S][Hq][D]; rows are O_i / l_i rounded to bf16.
+ *   lse         float32 device output [B][Hq][S], ln(sum_j exp(s_ij)) over the
+ *               kept keys, or NULL to skip it.
+ *   B, S        batch and sequence length, 1 <= B, 1 <= S <= 2^24.
+ *   Hq, Hkv     query and key/value heads, 1 <= Hkv <= Hq <= 255, Hq % Hkv == 0.
+ *   D           head dimension, 64 or 128.
+ *   causal      1: key j is excluded for query i when j > i; 0: full attention.
+ *   rope_base   theta base (e.g. 10000, 500000); <= 0 turns RoPE off.
+ *   window_k    per-pair window multiplier k > 0 (pair r keeps distances
+ *               i - j <= floor(k * 2*pi / theta_r)); <= 0 or +inf turns it off.
+ *               The window needs RoPE on and causal = 1, else ATTN_ERR_UNSUPPORTED.
+ *   stream      cudaStream_t (as void*).
+ *
+ * Returns ATTN_OK once the kernel is enqueued.  Argument errors are found on
+ * the host before anything is launched.  The first call for a new (device,
+ * S, D, rope_base, window_k, B, Hq, Hkv) builds and uploads tables
+ * synchronously; later calls only launch.  Precision: with RoPE on, the
+ * rotated Q and K are rounded to fp16 for the QK^T product (inputs must keep
+ * |x| < 46000 so the rotated values stay finite); with RoPE off, Q and K go
+ * to the tensor cores as the given bf16 values.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int S, int D, int causal,
+             double rope_base, double window_k, void* stream);
+
+/*
+ * attn_build_tables — the host-side RoPE and window tables the kernel uses.
+ *
+ *   cos_out, sin_out  host float32 [S][D/2]: cos and sin of (p + pos_offset) *
+ *                     theta_r for p = 0..S-1, computed in float64 and rounded.
+ *                     Either may be NULL.  Requires rope_base > 0.
+ *   win_out           host int32 [D/2]: W_r = floor(k * 2*pi / theta_r),
+ *                     clamped to [0, 2^31-1]; 2^31-1 when the window is off.
+ *                     May be NULL.
+ * Pure host computation; returns ATTN_ERR_SHAPE / ATTN_ERR_UNSUPPORTED on bad
+ * arguments.  ("ATFlash", The idea: w_r = k * lambda_r, lambda_r = 2*pi/theta_r.)
+ */
+int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
+                      float* cos_out, float* sin_out, int* win_out);
+
+/*
+ * attn_check — synchronise `stream`, then read and clear the device status
+ * word that the kernels raise when a bounded wait inside them runs out.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA if the stream failed.
+ */
+int attn_check(void* stream);
+
+/* attn_error_string — a static, human-readable name for an attn_status code. */
+const char* attn_error_string(int status);
+
+/*
+ * attn_release_cache — free every cached device table on every device the
+ * library has used.  No attn_fwd call may be in flight.
+ */
+void attn_release_cache(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -1,0 +1,88 @@
+"""The C ABI without a GPU: symbols, host-side argument checks, host tables."""
+import ctypes
+import math
+import subprocess
+
+import numpy as np
+import pytest
+
+import attention_causal_attn_gb300 as attn
+import oracle
+
+
+@pytest.fixture(scope="module")
+def lib():
+    attn.build()
+    return attn.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = attn.header_functions()
+    assert set(names) == {"attn_fwd", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
+    out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_error_strings(lib):
+    for name, code in attn.ATTN_STATUS.items():
+        assert attn.attn_error_string(code).startswith(name)
+    assert "unknown" in attn.attn_error_string(12345)
+
+
+def _call(lib, q=16, k=16, v=16, o=16, lse=0, B=1, Hq=2, Hkv=2, S=128, D=64, causal=1, base=10000.0, win=0.0):
+    return lib.attn_fwd(q, k, v, o, lse or None, B, Hq, Hkv, S, D, causal, base, win, None)
+
+
+def test_argument_errors_are_caught_on_the_host(lib):
+    E = attn.ATTN_STATUS
+    assert _call(lib, q=0) == E["ATTN_ERR_NULL"]
+    assert _call(lib, o=0) == E["ATTN_ERR_NULL"]
+    assert _call(lib, B=0) == E["ATTN_ERR_SHAPE"]
+    assert _call(lib, S=0) == E["ATTN_ERR_SHAPE"]
+    assert _call(lib, D=96) == E["ATTN_ERR_SHAPE"]
+    assert _call(lib, Hq=6, Hkv=4) == E["ATTN_ERR_SHAPE"]
+    assert _call(lib, Hq=2, Hkv=4) == E["ATTN_ERR_SHAPE"]
+    assert _call(lib, Hq=256, Hkv=1) == E["ATTN_ERR_SHAPE"]
+    assert _call(lib, q=24) == E["ATTN_ERR_ALIGN"]
+    assert _call(lib, lse=18) == E["ATTN_ERR_ALIGN"]
+    assert _call(lib, causal=2) == E["ATTN_ERR_UNSUPPORTED"]
+    assert _call(lib, base=0.0, win=1.0) == E["ATTN_ERR_UNSUPPORTED"]  # window needs RoPE
+    assert _call(lib, causal=0, win=1.0) == E["ATTN_ERR_UNSUPPORTED"]  # window needs causal
+    assert _call(lib, base=math.inf) == E["ATTN_ERR_UNSUPPORTED"]
+
+
+def test_rope_tables_are_float64_cos_sin_rounded(lib):
+    S, D, base = 300, 128, 10000.0
+    c, s, _ = attn.attn_build_tables(S, D, base, None, pos_offset=7)
+    theta = [base ** (-2.0 * r / D) for r in range(D // 2)]
+    for p in (0, 1, 17, 299):
+        for r in range(D // 2):
+            a = (p + 7) * theta[r]
+            assert c[p, r] == np.float32(math.cos(a)) and s[p, r] == np.float32(math.sin(a))
+
+
+@pytest.mark.parametrize("base,k", [(10000.0, 1.0), (500000.0, 4.0), (500000.0, 1.0)])
+def test_window_widths_match_oracle_and_closed_form(lib, base, k):
+    _, _, w = attn.attn_build_tables(16, 128, base, k)
+    np.testing.assert_array_equal(w.astype(np.float64), oracle.window_widths(128, base, k))
+    # the library's widths give the page's closed-form pruned count
+    S = 2048
+    closed = sum(max(0, S - 1 - int(x)) * (max(0, S - 1 - int(x)) + 1) // 2 for x in w)
+    assert closed == oracle.pruned_terms(S, 128, base, k)
+
+
+def test_window_off_widths_are_int_max(lib):
+    _, _, w = attn.attn_build_tables(16, 64, 10000.0, None)
+    assert np.all(w == np.iinfo(np.int32).max)
+    _, _, w = attn.attn_build_tables(16, 64, 10000.0, math.inf)
+    assert np.all(w == np.iinfo(np.int32).max)
+
+
+def test_build_tables_rejects_bad_arguments(lib):
+    with pytest.raises(attn.AttnError):
+        attn.attn_build_tables(16, 128, 0.0)
+    with pytest.raises(attn.AttnError):
+        attn.attn_build_tables(16, 80, 10000.0)

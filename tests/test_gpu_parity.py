@@ -1,0 +1,112 @@
+"""GPU parity: the sm_103a kernel through the C ABI against the float64 oracle.
+
+Tolerances (the attention prefill gate): O max-abs <= 2e-2 and mean-abs <=
+2e-3; LSE |error| <= 1e-3 * max(1, |LSE|).  Small cases compare every row;
+the benchmark-sized workloads compare 256 seeded query rows of 8 seeded heads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_causal_attn_gb300 as attn
+import oracle
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_REL = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    attn.build()
+    oracle.build()
+    yield
+    torch.cuda.synchronize()
+
+
+def _dev(a):
+    return torch.from_numpy(a).view(torch.bfloat16).cuda()
+
+
+def _check(o, lse, o_ref, lse_ref, tag=""):
+    o = np.asarray(o, dtype=np.float64)
+    err = np.abs(o - o_ref)
+    assert np.isfinite(o).all(), f"{tag}: non-finite output"
+    assert err.max() <= O_MAX, f"{tag}: max|dO| {err.max():.3e}"
+    assert err.mean() <= O_MEAN, f"{tag}: mean|dO| {err.mean():.3e}"
+    if lse is not None:
+        lerr = np.abs(np.asarray(lse, np.float64) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+        assert lerr.max() <= LSE_REL, f"{tag}: max rel dLSE {lerr.max():.3e}"
+    return err.max()
+
+
+SMALL = [
+    # B, Hq, Hkv, S, D, causal, rope_base
+    (1, 2, 2, 128, 64, True, 10000.0),    # the tiny benchmark configuration
+    (2, 4, 4, 384, 128, True, None),      # odd number of query tiles (last unit has one stage)
+    (1, 4, 2, 300, 128, True, 10000.0),   # GQA pairs, ragged tail
+    (2, 3, 1, 257, 64, True, 500000.0),   # group of 3: one paired unit and one single-head unit
+    (1, 2, 2, 1, 128, True, 10000.0),     # S = 1
+    (1, 2, 2, 2, 64, True, None),         # S = 2
+    (1, 2, 1, 200, 128, False, None),     # full attention, ragged
+    (2, 2, 2, 129, 64, False, 10000.0),   # full attention with RoPE, one key past a tile
+    (1, 8, 8, 1024, 128, True, 10000.0),  # eight query tiles per head
+    (1, 4, 4, 640, 128, False, 500000.0),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base", SMALL)
+def test_small_all_rows(B, Hq, Hkv, S, D, causal, base):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=101 + S)
+    o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=causal, rope_base=base)
+    attn.attn_check()
+    o_ref, lse_ref = oracle.attn_full(q, k, v, causal=causal, rope_base=base)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"S={S} D={D}")
+
+
+def test_no_lse_and_side_stream_and_determinism():
+    B, Hq, Hkv, S, D = 1, 4, 2, 513, 128
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=5)
+    qd, kd, vd = _dev(q), _dev(k), _dev(v)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1 = attn.attn_fwd(qd, kd, vd, causal=True, rope_base=10000.0, stream=s)
+        o2, none = attn.attn_fwd(qd, kd, vd, causal=True, rope_base=10000.0, return_lse=False, stream=s)
+    attn.attn_check(stream=s)
+    assert none is None
+    assert torch.equal(o1, o2)  # same schedule, same arithmetic: bitwise reproducible
+    o_ref, lse_ref = oracle.attn_full(q, k, v, causal=True, rope_base=10000.0)
+    _check(o1.float().cpu().numpy(), l1.cpu().numpy(), o_ref, lse_ref)
+
+
+def _sampled(B, Hq, Hkv, S, D, causal, base, outliers=0.0, nrows=256, nheads=8, seed=si.MASTER_SEED):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, outliers=outliers, seed=seed)
+    o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=causal, rope_base=base)
+    attn.attn_check()
+    rows = si.sample_rows(seed, S, nrows)
+    heads = si.sample_heads(seed, B, Hq, Hkv, nheads)
+    rb = np.repeat([b for b, _ in heads], len(rows))
+    rh = np.repeat([h for _, h in heads], len(rows))
+    ri = np.tile(rows, len(heads))
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, rb, rh, ri, causal=causal, rope_base=base)
+    idx_b = torch.from_numpy(rb).long().cuda()
+    idx_h = torch.from_numpy(rh).long().cuda()
+    idx_i = torch.from_numpy(ri).long().cuda()
+    o_s = o[idx_b, idx_i, idx_h].float().cpu().numpy()
+    l_s = lse[idx_b, idx_h, idx_i].cpu().numpy()
+    del o, lse
+    torch.cuda.empty_cache()
+    return _check(o_s, l_s, o_ref, lse_ref, f"S={S}")
+
+
+def test_plain_causal_s4096_sampled():
+    _sampled(4, 32, 32, 4096, 128, True, None)
+
+
+def test_rope_causal_s8192_sampled():
+    _sampled(4, 32, 32, 8192, 128, True, 10000.0)
+
+
+def test_gqa_outliers_s16384_sampled():
+    _sampled(1, 32, 8, 16384, 128, True, 500000.0, outliers=0.01)

@@ -351,6 +351,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
     ap.add_argument("--window-k", type=float, default=None, help="override the workload's window multiplier")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle time for --impl reference")
@@ -361,6 +362,8 @@ def main():
     w = dict(si.WORKLOADS[args.workload])
     if args.window_k is not None:
         w["window_k"] = args.window_k if args.window_k > 0 else None
+    if args.batch is not None:
+        w["B"] = args.batch
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

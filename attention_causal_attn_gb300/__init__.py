@@ -22,7 +22,7 @@ __all__ = ["attn_fwd", "attn_build_tables", "attn_check", "attn_error_string", "
 ATTN_STATUS = {
     "ATTN_OK": 0, "ATTN_ERR_NULL": -1, "ATTN_ERR_SHAPE": -2, "ATTN_ERR_ALIGN": -3,
     "ATTN_ERR_UNSUPPORTED": -4, "ATTN_ERR_CUDA": -5, "ATTN_ERR_TIMEOUT": -6, "ATTN_ERR_OOM": -7,
-    "ATTN_ERR_NO_DEVICE": -8,
+    "ATTN_ERR_NO_DEVICE": -8, "ATTN_ERR_SCRATCH": -9,
 }
 
 _lock = threading.Lock()
@@ -48,6 +48,8 @@ def load_library(path: str | None = None):
         vp, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
         lib.attn_fwd.restype = i
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
+        lib.attn_fwd_noalloc.restype = i
+        lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i

@@ -241,6 +241,118 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     return rope ? launch<64, false, true>(prm, grid, st, di) : launch<64, false, false>(prm, grid, st, di);
 }
 
+// ---------------------------------------------------------------------------
+// attn_fwd_noalloc: the same forward for callers that may not allocate device
+// memory.  Its RoPE table and tile schedule live in one file-scope device
+// array instead of cudaMalloc'd buffers.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB, held by every device that loads the library
+
+// Host code may not use this name as a device address (it is a host-side
+// stand-in); the device address comes from cudaGetSymbolAddress below.
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDev {
+    bool ready = false;
+    unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    // what the scratch currently holds (re-uploaded only when the request differs)
+    bool have = false;
+    int S = 0, D = 0, B = 0, Hq = 0, Hkv = 0, causal = 0, rope = 0, ctas = 0;
+    double base = 0.0;
+    size_t off_tasks = 0, off_offsets = 0;
+};
+NoAllocDev g_noalloc[kMaxDevices];
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                int Hkv, int S, int D, int causal, double rope_base, double window_k, void* stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_NULL;
+    if (B < 1 || B > 65535 || S < 1 || S > kMaxS || Hq < 1 || Hq > 255 || Hkv < 1 || Hkv > Hq || Hq % Hkv != 0)
+        return ATTN_ERR_SHAPE;
+    if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return ATTN_ERR_ALIGN;
+    if (causal != 0 && causal != 1) return ATTN_ERR_UNSUPPORTED;
+    if (std::isnan(window_k) || std::isnan(rope_base)) return ATTN_ERR_UNSUPPORTED;
+    if (rope_base > 0.0 && !std::isfinite(rope_base)) return ATTN_ERR_UNSUPPORTED;
+    const bool rope = rope_base > 0.0;
+    const bool window = window_k > 0.0 && !std::isinf(window_k);
+    if (window) return ATTN_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int rc = probe_device(dev);
+    if (rc != ATTN_OK) return rc;
+    NoAllocDev& na = g_noalloc[dev];
+    cudaError_t e;
+    if (!na.ready) {
+        // once per device, with that device current
+        if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&na.scratch), g_noalloc_scratch)) != cudaSuccess)
+            return cuda_fail("cudaGetSymbolAddress(no-alloc scratch)", e);
+        na.ready = true;
+    }
+    const bool same = na.have && na.S == S && na.D == D && na.B == B && na.Hq == Hq && na.Hkv == Hkv &&
+                      na.causal == causal && na.rope == static_cast<int>(rope) && (!rope || na.base == rope_base);
+    if (!same) {
+        const size_t rope_bytes = rope ? static_cast<size_t>(S) * (D / 2) * sizeof(float2) : 0;
+        const attn_host::Schedule sc = attn_host::build_schedule(B, Hq, Hkv, S, causal != 0, g_dev[dev].sms);
+        const size_t off_tasks = align256(rope_bytes);
+        const size_t off_offsets = align256(off_tasks + sc.words.size() * sizeof(uint32_t));
+        const size_t total = off_offsets + sc.offsets.size() * sizeof(int32_t);
+        if (total > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH;
+        na.have = false;  // contents are in flux until the copies below are enqueued
+        // Pageable host sources: each copy returns once its source has been staged,
+        // so the host vectors may go out of scope; the copies are ordered on `st`.
+        if (rope) {
+            const std::vector<float> host = attn_host::rope_table(S, D, rope_base, 0);
+            if ((e = cudaMemcpyAsync(na.scratch, host.data(), rope_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+                return cuda_fail("cudaMemcpyAsync(no-alloc rope table)", e);
+        }
+        if ((e = cudaMemcpyAsync(na.scratch + off_tasks, sc.words.data(), sc.words.size() * sizeof(uint32_t),
+                                 cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(na.scratch + off_offsets, sc.offsets.data(), sc.offsets.size() * sizeof(int32_t),
+                                 cudaMemcpyHostToDevice, st)) != cudaSuccess)
+            return cuda_fail("cudaMemcpyAsync(no-alloc schedule)", e);
+        na.have = true;
+        na.S = S, na.D = D, na.B = B, na.Hq = Hq, na.Hkv = Hkv, na.causal = causal;
+        na.rope = static_cast<int>(rope), na.base = rope_base, na.ctas = sc.ctas;
+        na.off_tasks = off_tasks, na.off_offsets = off_offsets;
+    }
+
+    FwdParams prm;
+    if (!encode_bshd(&prm.tm_q, q, B, S, Hq, D) || !encode_bshd(&prm.tm_k, k, B, S, Hkv, D) ||
+        !encode_bshd(&prm.tm_v, v, B, S, Hkv, D))
+        return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.rope = rope ? reinterpret_cast<const float2*>(na.scratch) : nullptr;
+    prm.tasks = reinterpret_cast<const uint2*>(na.scratch + na.off_tasks);
+    prm.task_off = reinterpret_cast<const int*>(na.scratch + na.off_offsets);
+    prm.status = g_dev[dev].status;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.S = S;
+    prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    prm.wait_limit_ns = kWaitLimitNs;
+    DevInfo& di = g_dev[dev];
+    const int grid = na.ctas;
+    if (D == 128) {
+        if (causal) return rope ? launch<128, true, true>(prm, grid, st, di) : launch<128, true, false>(prm, grid, st, di);
+        return rope ? launch<128, false, true>(prm, grid, st, di) : launch<128, false, false>(prm, grid, st, di);
+    }
+    if (causal) return rope ? launch<64, true, true>(prm, grid, st, di) : launch<64, true, false>(prm, grid, st, di);
+    return rope ? launch<64, false, true>(prm, grid, st, di) : launch<64, false, false>(prm, grid, st, di);
+}
+
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
                                  float* cos_out, float* sin_out, int* win_out) {
     if (S < 1 || S > kMaxS || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
@@ -287,6 +399,8 @@ extern "C" const char* attn_error_string(int status) {
         case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a bounded in-kernel wait ran out";
         case ATTN_ERR_OOM: return "ATTN_ERR_OOM: table allocation failed";
         case ATTN_ERR_NO_DEVICE: return "ATTN_ERR_NO_DEVICE: no sm_103 device is current";
+        case ATTN_ERR_SCRATCH:
+            return "ATTN_ERR_SCRATCH: the request needs more than the 16 MiB static scratch of attn_fwd_noalloc";
         default: return "unknown attn status";
     }
 }

@@ -45,7 +45,8 @@ typedef enum {
     ATTN_ERR_CUDA = -5,        /* a CUDA runtime or driver call failed */
     ATTN_ERR_TIMEOUT = -6,     /* a bounded in-kernel wait ran out (see attn_check) */
     ATTN_ERR_OOM = -7,         /* the library could not allocate its cached tables */
-    ATTN_ERR_NO_DEVICE = -8    /* no sm_103 device is current */
+    ATTN_ERR_NO_DEVICE = -8,   /* no sm_103 device is current */
+    ATTN_ERR_SCRATCH = -9      /* attn_fwd_noalloc: tables exceed its static scratch */
 } attn_status;
 
 /*
@@ -55,7 +56,7 @@ typedef enum {
  *   o           bf16 device output [B][S][Hq][D]; rows are O_i / l_i rounded to bf16.
  *   lse         float32 device output [B][Hq][S], ln(sum_j exp(s_ij)) over the
  *               kept keys, or NULL to skip it.
- *   B, S        batch and sequence length, 1 <= B, 1 <= S <= 2^24.
+ *   B, S        batch and sequence length, 1 <= B <= 65535, 1 <= S <= 2^22.
  *   Hq, Hkv     query and key/value heads, 1 <= Hkv <= Hq <= 255, Hq % Hkv == 0.
  *   D           head dimension, 64 or 128.
  *   causal      1: key j is excluded for query i when j > i; 0: full attention.
@@ -76,6 +77,38 @@ typedef enum {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int Hq, int Hkv, int S, int D, int causal,
              double rope_base, double window_k, void* stream);
+
+/*
+ * attn_fwd_noalloc — attn_fwd for callers that must not allocate device memory.
+ *
+ * The source pages have no counterpart to this entry point.  It exists for
+ * callers that cannot call cudaMalloc: code running where an allocation would
+ * break a memory budget fixed up front, allocators that own every device byte
+ * (a framework's caching allocator, an inference server's arena), or code that
+ * must not add allocator traffic to a hot loop.
+ *
+ * Arguments, results and precision are those of attn_fwd.  Instead of cached
+ * cudaMalloc'd buffers, the RoPE table ([S][D/2] float2) and the tile schedule
+ * live in one 16 MiB array in device global memory that is part of the
+ * library: every GPU that loads libattn.so holds those 16 MiB until the
+ * process exits.  The call allocates no device memory and calls no
+ * allocating CUDA or PyTorch routine.
+ *   - Limit: the table plus schedule must fit in 16 MiB, e.g. S <= 16384 at
+ *     D = 128 with RoPE on; larger requests return ATTN_ERR_SCRATCH before
+ *     anything is enqueued.  The window must be off.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - The array keeps the last call's contents.  A call whose shape, RoPE base
+ *     and causal flag differ from the previous call on the device re-uploads
+ *     the tables with cudaMemcpyAsync on `stream` (from pageable host memory,
+ *     so the host waits for the staging); otherwise it only launches.
+ *   - All calls share the one array: calls on different streams that overlap
+ *     on the GPU race on it unless they use the same shape and options.
+ */
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int S, int D, int causal,
+                     double rope_base, double window_k, void* stream);
 
 /*
  * attn_build_tables — the host-side RoPE and window tables the kernel uses.

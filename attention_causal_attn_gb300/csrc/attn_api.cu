@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -116,7 +117,7 @@ int get_rope(int dev, int S, int D, double base, float2** out) {
             *out = e.table;
             return ATTN_OK;
         }
-    const std::vector<float> host = attn_host::rope_table(S, D, base, 0);
+    const std::vector<float> host = attn_host::rope_factor_table(S, D, base);
     float2* d = nullptr;
     cudaError_t e;
     if ((e = cudaMalloc(&d, host.size() * sizeof(float))) != cudaSuccess) return cuda_fail("cudaMalloc(rope)", e, ATTN_ERR_OOM);
@@ -302,17 +303,22 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     const bool same = na.have && na.S == S && na.D == D && na.B == B && na.Hq == Hq && na.Hkv == Hkv &&
                       na.causal == causal && na.rope == static_cast<int>(rope) && (!rope || na.base == rope_base);
     if (!same) {
-        const size_t rope_bytes = rope ? static_cast<size_t>(S) * (D / 2) * sizeof(float2) : 0;
-        const attn_host::Schedule sc = attn_host::build_schedule(B, Hq, Hkv, S, causal != 0, g_dev[dev].sms);
+        // size check first, from the shape alone
+        const size_t rope_bytes = rope ? attn_host::rope_factor_table_floats(S, D) * sizeof(float) : 0;
+        const long long units = attn_host::schedule_units(B, Hq, Hkv, S);
+        const long long ctas = std::min<long long>(units, g_dev[dev].sms);
         const size_t off_tasks = align256(rope_bytes);
-        const size_t off_offsets = align256(off_tasks + sc.words.size() * sizeof(uint32_t));
-        const size_t total = off_offsets + sc.offsets.size() * sizeof(int32_t);
-        if (total > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH;
+        const size_t need_tasks = static_cast<size_t>(units) * 2 * sizeof(uint32_t);
+        const size_t off_offsets = align256(off_tasks + need_tasks);
+        if (units > static_cast<long long>(kNoAllocScratchBytes) ||
+            off_offsets + static_cast<size_t>(ctas + 1) * sizeof(int32_t) > kNoAllocScratchBytes)
+            return ATTN_ERR_SCRATCH;
+        const attn_host::Schedule sc = attn_host::build_schedule(B, Hq, Hkv, S, causal != 0, g_dev[dev].sms);
         na.have = false;  // contents are in flux until the copies below are enqueued
         // Pageable host sources: each copy returns once its source has been staged,
         // so the host vectors may go out of scope; the copies are ordered on `st`.
         if (rope) {
-            const std::vector<float> host = attn_host::rope_table(S, D, rope_base, 0);
+            const std::vector<float> host = attn_host::rope_factor_table(S, D, rope_base);
             if ((e = cudaMemcpyAsync(na.scratch, host.data(), rope_bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
                 return cuda_fail("cudaMemcpyAsync(no-alloc rope table)", e);
         }

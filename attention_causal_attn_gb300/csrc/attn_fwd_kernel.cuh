@@ -44,6 +44,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "host_tables.h"
 #include "ptx.cuh"
 
 namespace attn {
@@ -69,7 +70,7 @@ struct FwdParams {
     CUtensorMap tm_v;
     __nv_bfloat16* o;   // [B][S][Hq][D]
     float* lse;         // [B][Hq][S] or null
-    const float2* rope; // [S][D/2] (cos, sin), null when RoPE is off
+    const float2* rope; // RoPE factor tables (see RopeGeom), null when RoPE is off
     const uint2* tasks; // unit words, see decode_unit
     const int* task_off;// [gridDim.x + 1]: CTA c runs tasks[task_off[c] .. task_off[c+1])
     int* status;
@@ -178,19 +179,70 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
 }
 
 // ------------------------------------------------------------------ RoPE
-// Rotate one 128-row tile in place.  The tile is stored as D/64 column blocks
-// of [128 rows][128 B] with the 128-byte swizzle (16-byte chunk c of row r
-// sits at chunk c ^ (r & 7)).  Pair (r, r + D/2) has both members at the same
-// swizzled offset in column blocks 0 and 1 for D = 128, and in chunks c and
-// c + 4 of the single block for D = 64.  Input bf16, math fp32, output fp16.
+// Rotation of one 128-row tile in place.  The tile is stored as D/64 column
+// blocks of [128 rows][128 B] with the 128-byte swizzle (16-byte chunk c of
+// row r sits at chunk c ^ (r & 7)).  Pair (r, r + D/2) has both members at the
+// same swizzled offset in column blocks 0 and 1 for D = 128, and in chunks c
+// and c + 4 of the single block for D = 64, so each thread rotates whole pairs
+// from two 16-byte loads.  Input bf16, math fp32, output fp16.
+//
+// Thread t owns chunk c = t % kChunks (pairs 8c..8c+7) of rows rr + kRows*i,
+// rr = t / kChunks.  The angle of row p = pos0 + kRows*i + rr comes from the
+// angle-addition rule: (cos, sin)(p theta) = base_i * rowfac_rr as complex
+// numbers, with base_0 = (cos, sin)(pos0 theta) read once per tile and
+// base_{i+1} = base_i * step, step = (cos, sin)(kRows theta).  The host
+// computes every factor in float64; the recurrence adds a few float32 ulps.
 template <int D>
-__device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, int pos0, const FwdParams& p, int t) {
-    constexpr int kHalf = D / 2;
-    constexpr int kChunks = kHalf / 8;  // 16-byte chunks per half row
-    for (int it = t; it < kBlockM * kChunks; it += 128) {
-        const int row = it / kChunks;
-        const int c = it % kChunks;
-        const int pos = min(pos0 + row, p.S - 1);  // rows past S are zero-filled; any angle leaves them zero
+struct RopeGeom {
+    static constexpr int kHalf = D / 2;
+    static constexpr int kChunks = kHalf / 8;     // 16-byte chunks per half row
+    static constexpr int kRows = 128 / kChunks;   // rows covered by one pass of the 128 threads
+    static constexpr int kIters = kChunks;        // passes per 128-row tile
+    static_assert(kRows == attn_host::rope_rows_per_pass(D), "host factor table must match the rotating threads");
+    static_assert(kRows * kIters == 128, "passes must cover the tile");
+};
+
+// Table layout (float2 = (cos, sin)): base[ntiles][D/2] | rowfac[kRows][D/2] | step[D/2].
+struct RopeConsts {
+    float cr[8], sr[8];  // rowfac of this thread's rr
+    float cs[8], ss[8];  // step
+};
+
+__device__ __forceinline__ void load8_float2(const float2* src, float (&c)[8], float (&s)[8]) {
+    const float4* p4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 v = __ldg(p4 + k);
+        c[2 * k] = v.x;
+        s[2 * k] = v.y;
+        c[2 * k + 1] = v.z;
+        s[2 * k + 1] = v.w;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void rope_load_consts(const FwdParams& p, int t, RopeConsts& k) {
+    using G = RopeGeom<D>;
+    const int ntiles = (p.S + kBlockM - 1) / kBlockM;
+    const int c = t % G::kChunks, rr = t / G::kChunks;
+    load8_float2(p.rope + (static_cast<size_t>(ntiles) + rr) * G::kHalf + 8 * c, k.cr, k.sr);
+    load8_float2(p.rope + (static_cast<size_t>(ntiles) + G::kRows) * G::kHalf + 8 * c, k.cs, k.ss);
+}
+
+template <int D>
+__device__ __forceinline__ void rope_load_base(const FwdParams& p, int tile, int t, float (&cb)[8], float (&sb)[8]) {
+    using G = RopeGeom<D>;
+    load8_float2(p.rope + static_cast<size_t>(tile) * G::kHalf + 8 * (t % G::kChunks), cb, sb);
+}
+
+template <int D>
+__device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts& k, float (&cb)[8], float (&sb)[8],
+                                                 int t) {
+    using G = RopeGeom<D>;
+    const int c = t % G::kChunks, rr = t / G::kChunks;
+#pragma unroll 2
+    for (int i = 0; i < G::kIters; ++i) {
+        const int row = rr + G::kRows * i;
         uint32_t lo_off, hi_off;
         if (D == 128) {
             lo_off = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
@@ -199,28 +251,35 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, int pos0, const 
             lo_off = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
             hi_off = static_cast<uint32_t>(row * 128 + (((c + 4) ^ (row & 7)) << 4));
         }
-        uint4 lo = *reinterpret_cast<const uint4*>(tile + lo_off);
-        uint4 hi = *reinterpret_cast<const uint4*>(tile + hi_off);
-        const float4* cs = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(pos) * kHalf + c * 8);
-        float4 t4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) t4[k] = __ldg(cs + k);
+        const uint4 lo = *reinterpret_cast<const uint4*>(tile + lo_off);
+        const uint4 hi = *reinterpret_cast<const uint4*>(tile + hi_off);
         const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
         const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
         uint32_t lo_out[4], hi_out[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            // elements 2k (low half of the word) and 2k+1 (high half)
-            const float x0 = bf16_lo(lw[k]), x1 = bf16_hi(lw[k]);
-            const float y0 = bf16_lo(hw[k]), y1 = bf16_hi(hw[k]);
-            const float c0 = t4[k].x, s0 = t4[k].y, c1 = t4[k].z, s1 = t4[k].w;
-            const float xr0 = x0 * c0 - y0 * s0, yr0 = y0 * c0 + x0 * s0;
-            const float xr1 = x1 * c1 - y1 * s1, yr1 = y1 * c1 + x1 * s1;
-            lo_out[k] = pack_f16x2(xr0, xr1);
-            hi_out[k] = pack_f16x2(yr0, yr1);
+        for (int q = 0; q < 4; ++q) {
+            float xr[2], yr[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int e = 2 * q + h;
+                const float cosv = cb[e] * k.cr[e] - sb[e] * k.sr[e];
+                const float sinv = sb[e] * k.cr[e] + cb[e] * k.sr[e];
+                const float x = h == 0 ? bf16_lo(lw[q]) : bf16_hi(lw[q]);
+                const float y = h == 0 ? bf16_lo(hw[q]) : bf16_hi(hw[q]);
+                xr[h] = x * cosv - y * sinv;
+                yr[h] = y * cosv + x * sinv;
+            }
+            lo_out[q] = pack_f16x2(xr[0], xr[1]);
+            hi_out[q] = pack_f16x2(yr[0], yr[1]);
         }
         *reinterpret_cast<uint4*>(tile + lo_off) = make_uint4(lo_out[0], lo_out[1], lo_out[2], lo_out[3]);
         *reinterpret_cast<uint4*>(tile + hi_off) = make_uint4(hi_out[0], hi_out[1], hi_out[2], hi_out[3]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float nc = cb[e] * k.cs[e] - sb[e] * k.ss[e];
+            sb[e] = sb[e] * k.cs[e] + cb[e] * k.ss[e];
+            cb[e] = nc;
+        }
     }
 }
 
@@ -228,25 +287,30 @@ template <int D>
 __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_t bar0, int t_begin, int t_end,
                           const WaitCtl& ctl, int t) {
     using L = SmemLayout<D>;
+    RopeConsts k;
+    rope_load_consts<D>(p, t, k);
     int kit = 0;
     int qit[2] = {0, 0};
+    float cb[8], sb[8];
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, causal);
         for (int s = 0; s < 2; ++s) {
             if (!u.valid[s]) continue;
+            rope_load_base<D>(p, u.row0[s] / kBlockM, t, cb, sb);
             if (!__all_sync(0xffffffffu, mbar_wait(bar_at(bar0, BAR_Q_FULL + s), qit[s] & 1, ctl, kStatusRope)))
                 return;
-            rope_rotate_tile<D>(smg + L::kQ + s * L::kTileBytes, u.row0[s], p, t);
+            rope_rotate_tile<D>(smg + L::kQ + s * L::kTileBytes, k, cb, sb, t);
             fence_proxy_async_smem();
             mbar_arrive(bar_at(bar0, BAR_Q_ROT + s));
             ++qit[s];
         }
         for (int n = u.nmax; n >= 0; --n) {
             const int ks = kit % kKStages;
+            rope_load_base<D>(p, n, t, cb, sb);
             if (!__all_sync(0xffffffffu,
                             mbar_wait(bar_at(bar0, BAR_K_FULL + ks), (kit / kKStages) & 1, ctl, kStatusRope)))
                 return;
-            rope_rotate_tile<D>(smg + L::kK + ks * L::kTileBytes, n * kBlockN, p, t);
+            rope_rotate_tile<D>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t);
             fence_proxy_async_smem();
             mbar_arrive(bar_at(bar0, BAR_K_ROT + ks));
             ++kit;
@@ -358,15 +422,83 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
+// Masked row maximum of 64 raw scores: keys at or past `limit` are ignored.
+template <bool MASKED>
+__device__ __forceinline__ float row_max64(const uint32_t (&r)[64], int col0, int limit, float mx) {
+    float m0 = mx, m1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) {
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q] = __uint_as_float(r[j + q]);
+            if (MASKED && col0 + j + q >= limit) v[q] = -INFINITY;
+        }
+        m0 = fmax3(m0, v[0], v[1]);
+        m1 = fmax3(m1, v[2], v[3]);
+    }
+    return fmaxf(m0, m1);
+}
+
+// P = exp2(S*c - m*c) for 32 scores (masked keys give exactly 0), the running
+// pair sum of P in fp32, and P packed to bf16 pairs (even key in the low half).
+template <bool MASKED>
+__device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0, int limit, uint64_t c2, uint64_t nmc2,
+                                           uint64_t& sum2, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        float a = __uint_as_float(r[j]), b = __uint_as_float(r[j + 1]);
+        if (MASKED) {
+            if (col0 + j >= limit) a = -INFINITY;
+            if (col0 + j + 1 >= limit) b = -INFINITY;
+        }
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(a, b), c2, nmc2), x0, x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        sum2 = f2_add(sum2, f2_pack(p0, p1));
+        pk[j / 2] = pack_bf16x2(p0, p1);
+    }
+}
+
+template <bool MASKED>
+__device__ __forceinline__ float tile_row_max(uint32_t taddr, int limit) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < kBlockN; cc += 64) {
+        uint32_t r[64];
+        tmem_load_64(taddr + cc, r);
+        mx = row_max64<MASKED>(r, cc, limit, mx);
+    }
+    return mx;
+}
+
+template <bool MASKED>
+__device__ __forceinline__ float tile_exp_to_p(uint32_t taddr, int limit, float c, float mc) {
+    const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+    uint64_t sum2 = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int cc = 0; cc < kBlockN; cc += 32) {
+        uint32_t r[32];
+        tmem_load_32(taddr + cc, r);
+        uint32_t pk[16];
+        exp_pack32<MASKED>(r, cc, limit, c2, nmc2, sum2, pk);
+        tmem_store_16(taddr + cc / 2, pk);
+    }
+    float s0, s1;
+    f2_unpack(sum2, s0, s1);
+    return s0 + s1;
+}
+
 template <int D, bool CAUSAL>
 __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint32_t tmem, int t_begin, int t_end,
                              const WaitCtl& ctl, int t) {
     const uint32_t lane_base = static_cast<uint32_t>(t & ~31);  // this warp's TMEM lane quarter
     const uint32_t trow = tmem + (lane_base << 16);
-    const uint32_t colS = static_cast<uint32_t>(stage * 128);
-    const uint32_t colO = 256u + static_cast<uint32_t>(stage * 128);
+    const uint32_t tS = trow + static_cast<uint32_t>(stage * 128);
+    const uint32_t tO = trow + 256u + static_cast<uint32_t>(stage * 128);
     const float c = p.scale_log2;
     const int last_tile = (p.S - 1) / kBlockN;
+    const bool ragged = (p.S % kBlockN) != 0;
     int sit = 0, oit = 0;
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, CAUSAL);
@@ -380,19 +512,15 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
                 return;
             ++sit;
             tc_fence_after();
-            int limit = kBlockN;  // keys [0, limit) of this tile are visible to this row
-            if (CAUSAL && n == u.nhi[stage]) limit = t + 1;
-            if (n == last_tile) limit = min(limit, p.S - n * kBlockN);
-            // pass 1: masked row maximum of the raw scores
-            float mx = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < kBlockN; cc += 64) {
-                uint32_t r[64];
-                tmem_load_64(trow + colS + cc, r);
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (cc + j < limit) mx = fmaxf(mx, __uint_as_float(r[j]));
-            }
+            // keys [0, limit) of this tile are visible to this row; only the
+            // diagonal tile (causal) and the ragged last tile have a limit < 128
+            const bool diag = CAUSAL && n == u.nhi[stage];
+            const bool tail = ragged && n == last_tile;
+            const bool masked = diag || tail;  // uniform across the warp
+            int limit = kBlockN;
+            if (diag) limit = t + 1;
+            if (tail) limit = min(limit, p.S - n * kBlockN);
+            const float mx = masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit);
             const float m_new = fmaxf(m_used, mx);
             if (n == u.nhi[stage]) {
                 m_used = m_new;
@@ -405,34 +533,24 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
                         m_used = m_new;
                         l *= alpha;
                     }
+                    const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t r[32];
-                        tmem_load_32(trow + colO + cc, r);
+                        tmem_load_32(tO + cc, r);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                        tmem_store_32(trow + colO + cc, r);
+                        for (int j = 0; j < 32; j += 2) {
+                            float x0, x1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2), x0, x1);
+                            r[j] = __float_as_uint(x0);
+                            r[j + 1] = __float_as_uint(x1);
+                        }
+                        tmem_store_32(tO + cc, r);
                     }
                 }
             }
-            // pass 2: P = exp2(S*c - m*c), masked keys 0; l += rowsum(P); P -> bf16 pairs in TMEM
             const float mc = m_used * c;
-            float sum = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < kBlockN; cc += 32) {
-                uint32_t r[32];
-                tmem_load_32(trow + colS + cc, r);
-                uint32_t pk[16];
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const float p0 = (cc + j < limit) ? ex2_approx(fmaf(__uint_as_float(r[j]), c, -mc)) : 0.f;
-                    const float p1 = (cc + j + 1 < limit) ? ex2_approx(fmaf(__uint_as_float(r[j + 1]), c, -mc)) : 0.f;
-                    sum += p0 + p1;
-                    pk[j / 2] = pack_bf16x2(p0, p1);
-                }
-                tmem_store_16(trow + colS + cc / 2, pk);
-            }
-            l += sum;
+            l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BAR_P_FULL + stage));
@@ -444,16 +562,20 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
         ++oit;
         tc_fence_after();
         const float inv_l = 1.0f / l;
+        const uint64_t il2 = f2_pack(inv_l, inv_l);
         const bool row_ok = row < p.S;
         __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.S + row) * p.Hq + u.h[stage]) * D;
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
             uint32_t r[32];
-            tmem_load_32(trow + colO + cc, r);
+            tmem_load_32(tO + cc, r);
             uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv_l, __uint_as_float(r[2 * j + 1]) * inv_l);
+            for (int j = 0; j < 16; ++j) {
+                float x0, x1;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il2), x0, x1);
+                pk[j] = pack_bf16x2(x0, x1);
+            }
             if (row_ok) {
                 uint4* dst = reinterpret_cast<uint4*>(orow + cc);
 #pragma unroll

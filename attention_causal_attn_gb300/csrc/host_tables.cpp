@@ -36,6 +36,33 @@ std::vector<float> rope_table(int S, int D, double base, long long pos_offset) {
     return t;
 }
 
+size_t rope_factor_table_floats(int S, int D) {
+    const size_t half = static_cast<size_t>(D / 2);
+    const size_t rows = static_cast<size_t>(rope_rows_per_pass(D));
+    const size_t ntiles = static_cast<size_t>((S + kTile - 1) / kTile);
+    return (ntiles + rows + 1) * half * 2;
+}
+
+std::vector<float> rope_factor_table(int S, int D, double base) {
+    const int half = D / 2;
+    const int rows = rope_rows_per_pass(D);
+    const int ntiles = (S + kTile - 1) / kTile;
+    const std::vector<double> th = rope_thetas(D, base);
+    std::vector<float> t(rope_factor_table_floats(S, D));
+    size_t o = 0;
+    auto put = [&](double pos) {
+        for (int r = 0; r < half; ++r) {
+            const double a = pos * th[r];
+            t[o++] = static_cast<float>(std::cos(a));
+            t[o++] = static_cast<float>(std::sin(a));
+        }
+    };
+    for (int m = 0; m < ntiles; ++m) put(static_cast<double>(m) * kTile);
+    for (int rr = 0; rr < rows; ++rr) put(static_cast<double>(rr));
+    put(static_cast<double>(rows));
+    return t;
+}
+
 std::vector<int32_t> window_widths(int D, double base, double k) {
     std::vector<int32_t> w(static_cast<size_t>(D / 2), INT32_MAX);
     if (!(k > 0.0) || std::isinf(k)) return w;
@@ -45,6 +72,13 @@ std::vector<int32_t> window_widths(int D, double base, double k) {
         w[r] = x >= static_cast<double>(INT32_MAX) ? INT32_MAX : static_cast<int32_t>(std::max(0.0, x));
     }
     return w;
+}
+
+long long schedule_units(int B, int Hq, int Hkv, int S) {
+    const long long nqt = (S + kTile - 1) / kTile;
+    const long long G = Hq / Hkv;
+    if (G >= 2) return static_cast<long long>(B) * Hkv * nqt * ((G + 1) / 2);
+    return static_cast<long long>(B) * Hq * ((nqt + 1) / 2);
 }
 
 Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas) {

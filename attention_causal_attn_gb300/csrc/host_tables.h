@@ -15,6 +15,21 @@ std::vector<double> rope_thetas(int D, double base);
 // [S][D/2][2] float32, computed in float64.
 std::vector<float> rope_table(int S, int D, double base, long long pos_offset);
 
+// Rows of a 128-row tile that one pass of 128 rotating threads covers: each
+// thread takes one 16-byte chunk (8 pairs) of the D/2 pairs of a row, so a
+// pass covers 128 / (D/16) = 2048/D rows (16 for D = 128, 32 for D = 64).
+// Shared with the kernel.
+constexpr int rope_rows_per_pass(int D) { return 2048 / D; }
+
+// The factor tables the kernel rotates with (float2 = (cos, sin), float32 from
+// float64), for positions p = 128*m + rows*i + rr, rows = rope_rows_per_pass(D):
+//   base[m][r]    = angle 128*m*theta_r,  m = 0..ceil(S/128)-1
+//   rowfac[rr][r] = angle rr*theta_r,     rr = 0..rows-1
+//   step[r]       = angle rows*theta_r
+// The kernel forms the angle of position p by complex multiplication of these factors.
+std::vector<float> rope_factor_table(int S, int D, double base);
+size_t rope_factor_table_floats(int S, int D);
+
 // W_r = floor(k * 2*pi / theta_r) clamped to [0, INT32_MAX]; INT32_MAX when
 // the window is off (k <= 0 or infinite).  ("ATFlash", The idea.)
 std::vector<int32_t> window_widths(int D, double base, double k);
@@ -33,5 +48,8 @@ struct Schedule {
 // estimated cost 2(bm+1) + 4 per query tile, heaviest units first into the
 // lightest CTA, then each CTA's list ordered by batch/head for K/V locality).
 Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas);
+
+// Number of work units build_schedule makes for a shape, without building it.
+long long schedule_units(int B, int Hq, int Hkv, int S);
 
 }  // namespace attn_host

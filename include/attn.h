@@ -88,14 +88,15 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * must not add allocator traffic to a hot loop.
  *
  * Arguments, results and precision are those of attn_fwd.  Instead of cached
- * cudaMalloc'd buffers, the RoPE table ([S][D/2] float2) and the tile schedule
+ * cudaMalloc'd buffers, the RoPE factor tables (about (S/128 + 17) * D * 4
+ * bytes) and the tile schedule (8 bytes per work unit of up to 256 query rows)
  * live in one 16 MiB array in device global memory that is part of the
  * library: every GPU that loads libattn.so holds those 16 MiB until the
  * process exits.  The call allocates no device memory and calls no
  * allocating CUDA or PyTorch routine.
- *   - Limit: the table plus schedule must fit in 16 MiB, e.g. S <= 16384 at
- *     D = 128 with RoPE on; larger requests return ATTN_ERR_SCRATCH before
- *     anything is enqueued.  The window must be off.
+ *   - Limit: tables plus schedule must fit in 16 MiB, about two million work
+ *     units (B * Hq * S up to roughly 5e8); larger requests return
+ *     ATTN_ERR_SCRATCH before anything is enqueued.  The window must be off.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
@@ -111,8 +112,11 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float
                      double rope_base, double window_k, void* stream);
 
 /*
- * attn_build_tables — the host-side RoPE and window tables the kernel uses.
+ * attn_build_tables — the host-side RoPE angles and window widths.
  *
+ * The kernel derives the same angles on the device by complex multiplication
+ * of per-tile, per-row and per-step factors computed from the same float64
+ * values, so its rotated operands agree with these tables to a few float32 ulps.
  *   cos_out, sin_out  host float32 [S][D/2]: cos and sin of (p + pos_offset) *
  *                     theta_r for p = 0..S-1, computed in float64 and rounded.
  *                     Either may be NULL.  Requires rope_base > 0.

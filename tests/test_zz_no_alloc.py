@@ -62,8 +62,8 @@ def test_noalloc_matches_attn_fwd_on_two_calls(B, Hq, Hkv, S, D, causal, base):
 def test_noalloc_rejects_requests_beyond_its_scratch():
     lib = attn.load_library()
     q = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: the size check comes first
-    # RoPE table for S = 65536, D = 128 is 32 MiB > 16 MiB
+    # 64 x 128 heads x 2^22 rows is 134M work units, 1 GiB of schedule > 16 MiB
     rc = lib.attn_fwd_noalloc(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), None,
-                              1, 1, 1, 65536, 128, 1, 10000.0, 0.0, None)
+                              64, 128, 128, 1 << 22, 128, 1, 10000.0, 0.0, None)
     assert rc == attn.ATTN_STATUS["ATTN_ERR_SCRATCH"]
     assert "static scratch" in attn.attn_error_string(rc)

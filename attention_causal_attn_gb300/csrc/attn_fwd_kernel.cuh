@@ -7,7 +7,7 @@
 //   - MHA: the two stages are consecutive query tiles of one head;
 //   - GQA: the two stages are two query heads of one KV group at the same tile.
 //
-// Warp roles (14 warps):
+// Warp roles (16 warps = 4 warpgroups, registers rebalanced with setmaxnreg):
 //   warps 0-3   softmax stage 0: online softmax on S0 in TMEM, P0 back to TMEM,
 //               O0 rescale, epilogue (O/l -> bf16 -> global, LSE)
 //   warps 4-7   softmax stage 1 (same, on S1/P1/O1)
@@ -18,6 +18,7 @@
 //               tile 0 ("Flash Attention: Causal Prefill D=128", reverse
 //               traversal isolates the causal mask to the first tile)
 //   warp 13     tcgen05 issuer (one thread) and TMEM owner
+//   warps 14-15 idle (they complete the fourth warpgroup)
 //
 // TMEM (512 columns x 128 lanes x 32 bit): S0 [0,128), S1 [128,256), O0 [256,
 // 256+D), O1 [384, 384+D).  P_s (bf16, two per column) overwrites the first 64
@@ -53,10 +54,14 @@ constexpr int kBlockM = 128;  // query rows per stage
 constexpr int kBlockN = 128;  // keys per KV tile
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-constexpr int kNumThreads = 448;
+constexpr int kNumThreads = 512;  // four warpgroups; launched at 128 registers per thread
 constexpr int kWarpRope = 8;
 constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
+// Register split per warpgroup (softmax x2, RoPE, producer/MMA): the sum of
+// 128 x budget over the four warpgroups must not exceed 512 x 128.
+constexpr uint32_t kRegsSoftmax = 152, kRegsRope = 120, kRegsOther = 88;
+static_assert(128 * (2 * kRegsSoftmax + kRegsRope + kRegsOther) <= kNumThreads * 128, "register split");
 constexpr uint32_t kSubTileBytes = 128u * 128u;  // 128 rows x 128 B: one 64-wide bf16 column block
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -147,6 +152,7 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
     int qit[2] = {0, 0};
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, causal);
+#pragma unroll
         for (int s = 0; s < 2; ++s) {
             if (!u.valid[s]) continue;
             if (!mbar_wait(bar_at(bar0, BAR_Q_EMPTY + s), (qit[s] & 1) ^ 1, ctl, kStatusProducer)) return;
@@ -187,11 +193,12 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
 // from two 16-byte loads.  Input bf16, math fp32, output fp16.
 //
 // Thread t owns chunk c = t % kChunks (pairs 8c..8c+7) of rows rr + kRows*i,
-// rr = t / kChunks.  The angle of row p = pos0 + kRows*i + rr comes from the
-// angle-addition rule: (cos, sin)(p theta) = base_i * rowfac_rr as complex
-// numbers, with base_0 = (cos, sin)(pos0 theta) read once per tile and
-// base_{i+1} = base_i * step, step = (cos, sin)(kRows theta).  The host
-// computes every factor in float64; the recurrence adds a few float32 ulps.
+// rr = t / kChunks.  Angles come from the angle-addition rule, as complex
+// numbers: the angle of row pos0 + rr is base(pos0) * rowfac(rr), with
+// base(pos0) = (cos, sin)(pos0 theta) read once per tile, and each pass
+// advances it by step = (cos, sin)(kRows theta).  The host computes every
+// factor in float64; the recurrence adds a few float32 ulps.  Pairs are
+// processed two at a time in packed fp32x2 arithmetic.
 template <int D>
 struct RopeGeom {
     static constexpr int kHalf = D / 2;
@@ -203,20 +210,19 @@ struct RopeGeom {
 };
 
 // Table layout (float2 = (cos, sin)): base[ntiles][D/2] | rowfac[kRows][D/2] | step[D/2].
+// Packed pairs of pairs: element q holds pairs (8c + 2q, 8c + 2q + 1).
 struct RopeConsts {
-    float cr[8], sr[8];  // rowfac of this thread's rr
-    float cs[8], ss[8];  // step
+    uint64_t cr[4], sr[4];  // rowfac of this thread's rr
+    uint64_t cs[4], ss[4];  // step
 };
 
-__device__ __forceinline__ void load8_float2(const float2* src, float (&c)[8], float (&s)[8]) {
+__device__ __forceinline__ void load8_packed(const float2* src, uint64_t (&c)[4], uint64_t (&s)[4]) {
     const float4* p4 = reinterpret_cast<const float4*>(src);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float4 v = __ldg(p4 + k);
-        c[2 * k] = v.x;
-        s[2 * k] = v.y;
-        c[2 * k + 1] = v.z;
-        s[2 * k + 1] = v.w;
+        const float4 v = __ldg(p4 + k);  // (cos, sin) of pairs 2k and 2k+1
+        c[k] = f2_pack(v.x, v.z);
+        s[k] = f2_pack(v.y, v.w);
     }
 }
 
@@ -225,21 +231,32 @@ __device__ __forceinline__ void rope_load_consts(const FwdParams& p, int t, Rope
     using G = RopeGeom<D>;
     const int ntiles = (p.S + kBlockM - 1) / kBlockM;
     const int c = t % G::kChunks, rr = t / G::kChunks;
-    load8_float2(p.rope + (static_cast<size_t>(ntiles) + rr) * G::kHalf + 8 * c, k.cr, k.sr);
-    load8_float2(p.rope + (static_cast<size_t>(ntiles) + G::kRows) * G::kHalf + 8 * c, k.cs, k.ss);
+    load8_packed(p.rope + (static_cast<size_t>(ntiles) + rr) * G::kHalf + 8 * c, k.cr, k.sr);
+    load8_packed(p.rope + (static_cast<size_t>(ntiles) + G::kRows) * G::kHalf + 8 * c, k.cs, k.ss);
 }
 
 template <int D>
-__device__ __forceinline__ void rope_load_base(const FwdParams& p, int tile, int t, float (&cb)[8], float (&sb)[8]) {
+__device__ __forceinline__ void rope_load_base(const FwdParams& p, int tile, int t, uint64_t (&cb)[4],
+                                               uint64_t (&sb)[4]) {
     using G = RopeGeom<D>;
-    load8_float2(p.rope + static_cast<size_t>(tile) * G::kHalf + 8 * (t % G::kChunks), cb, sb);
+    load8_packed(p.rope + static_cast<size_t>(tile) * G::kHalf + 8 * (t % G::kChunks), cb, sb);
+}
+
+// (c, s) <- (c, s) * (fc, fs) as complex numbers, two pairs per operand.
+__device__ __forceinline__ void cmul2(uint64_t& c, uint64_t& s, uint64_t fc, uint64_t fs) {
+    const uint64_t nc = f2_sub(f2_mul(c, fc), f2_mul(s, fs));
+    s = f2_fma(s, fc, f2_mul(c, fs));
+    c = nc;
 }
 
 template <int D>
-__device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts& k, float (&cb)[8], float (&sb)[8],
-                                                 int t) {
+__device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts& k, uint64_t (&cb)[4],
+                                                 uint64_t (&sb)[4], int t) {
     using G = RopeGeom<D>;
     const int c = t % G::kChunks, rr = t / G::kChunks;
+    // angle of this thread's first row
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cmul2(cb[q], sb[q], k.cr[q], k.sr[q]);
 #pragma unroll 2
     for (int i = 0; i < G::kIters; ++i) {
         const int row = rr + G::kRows * i;
@@ -258,28 +275,18 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
         uint32_t lo_out[4], hi_out[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            float xr[2], yr[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int e = 2 * q + h;
-                const float cosv = cb[e] * k.cr[e] - sb[e] * k.sr[e];
-                const float sinv = sb[e] * k.cr[e] + cb[e] * k.sr[e];
-                const float x = h == 0 ? bf16_lo(lw[q]) : bf16_hi(lw[q]);
-                const float y = h == 0 ? bf16_lo(hw[q]) : bf16_hi(hw[q]);
-                xr[h] = x * cosv - y * sinv;
-                yr[h] = y * cosv + x * sinv;
-            }
-            lo_out[q] = pack_f16x2(xr[0], xr[1]);
-            hi_out[q] = pack_f16x2(yr[0], yr[1]);
+            const uint64_t x = f2_pack(bf16_lo(lw[q]), bf16_hi(lw[q]));
+            const uint64_t y = f2_pack(bf16_lo(hw[q]), bf16_hi(hw[q]));
+            float a0, a1, b0, b1;
+            f2_unpack(f2_sub(f2_mul(x, cb[q]), f2_mul(y, sb[q])), a0, a1);  // x cos - y sin
+            f2_unpack(f2_fma(y, cb[q], f2_mul(x, sb[q])), b0, b1);           // y cos + x sin
+            lo_out[q] = pack_f16x2(a0, a1);
+            hi_out[q] = pack_f16x2(b0, b1);
         }
         *reinterpret_cast<uint4*>(tile + lo_off) = make_uint4(lo_out[0], lo_out[1], lo_out[2], lo_out[3]);
         *reinterpret_cast<uint4*>(tile + hi_off) = make_uint4(hi_out[0], hi_out[1], hi_out[2], hi_out[3]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float nc = cb[e] * k.cs[e] - sb[e] * k.ss[e];
-            sb[e] = sb[e] * k.cs[e] + cb[e] * k.ss[e];
-            cb[e] = nc;
-        }
+        for (int q = 0; q < 4; ++q) cmul2(cb[q], sb[q], k.cs[q], k.ss[q]);
     }
 }
 
@@ -291,9 +298,10 @@ __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_
     rope_load_consts<D>(p, t, k);
     int kit = 0;
     int qit[2] = {0, 0};
-    float cb[8], sb[8];
+    uint64_t cb[4], sb[4];
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, causal);
+#pragma unroll
         for (int s = 0; s < 2; ++s) {
             if (!u.valid[s]) continue;
             rope_load_base<D>(p, u.row0[s] / kBlockM, t, cb, sb);
@@ -350,6 +358,7 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                 if (!ok) break;
             }
             tc_fence_after();
+#pragma unroll
             for (int s = 0; s < 2 && ok; ++s) {
                 if (!u.valid[s]) continue;
                 const uint32_t tS = tmem + static_cast<uint32_t>(s * 128);
@@ -403,6 +412,7 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
             }
         }
         if (!ok) break;
+#pragma unroll
         for (int s = 0; s < 2; ++s) {
             if (!u.valid[s]) continue;
             tc_commit(bar_at(bar0, BAR_O_FULL + s));
@@ -489,6 +499,9 @@ __device__ __forceinline__ float tile_exp_to_p(uint32_t taddr, int limit, float 
     return s0 + s1;
 }
 
+// One body serves both stages (stage is a runtime value: a second copy of this
+// code measurably costs instruction-cache capacity).  Per-stage fields of the
+// unit are picked with selects so nothing is indexed at run time.
 template <int D, bool CAUSAL>
 __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint32_t tmem, int t_begin, int t_end,
                              const WaitCtl& ctl, int t) {
@@ -502,11 +515,14 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
     int sit = 0, oit = 0;
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, CAUSAL);
-        if (!u.valid[stage]) continue;
-        const int row = u.row0[stage] + t;
+        const bool valid = stage ? u.valid[1] : u.valid[0];
+        if (!valid) continue;
+        const int nhi = stage ? u.nhi[1] : u.nhi[0];
+        const int head = stage ? u.h[1] : u.h[0];
+        const int row = (stage ? u.row0[1] : u.row0[0]) + t;
         float m_used = -INFINITY;
         float l = 0.f;
-        for (int n = u.nhi[stage]; n >= 0; --n) {
+        for (int n = nhi; n >= 0; --n) {
             if (!__all_sync(0xffffffffu,
                             mbar_wait(bar_at(bar0, BAR_S_FULL + stage), sit & 1, ctl, kStatusSoftmax << stage)))
                 return;
@@ -514,7 +530,7 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
             tc_fence_after();
             // keys [0, limit) of this tile are visible to this row; only the
             // diagonal tile (causal) and the ragged last tile have a limit < 128
-            const bool diag = CAUSAL && n == u.nhi[stage];
+            const bool diag = CAUSAL && n == nhi;
             const bool tail = ragged && n == last_tile;
             const bool masked = diag || tail;  // uniform across the warp
             int limit = kBlockN;
@@ -522,7 +538,7 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
             if (tail) limit = min(limit, p.S - n * kBlockN);
             const float mx = masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit);
             const float m_new = fmaxf(m_used, mx);
-            if (n == u.nhi[stage]) {
+            if (n == nhi) {
                 m_used = m_new;
             } else {
                 const bool need = (m_new - m_used) * c > kRescaleThreshold;
@@ -564,7 +580,7 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
         const float inv_l = 1.0f / l;
         const uint64_t il2 = f2_pack(inv_l, inv_l);
         const bool row_ok = row < p.S;
-        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.S + row) * p.Hq + u.h[stage]) * D;
+        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.S + row) * p.Hq + head) * D;
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
             uint32_t r[32];
@@ -584,7 +600,7 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
             }
         }
         if (row_ok && p.lse != nullptr)
-            p.lse[(static_cast<size_t>(u.b) * p.Hq + u.h[stage]) * p.S + row] =
+            p.lse[(static_cast<size_t>(u.b) * p.Hq + head) * p.S + row] =
                 (m_used * c + log2f(l)) * 0.69314718055994531f;
         tc_fence_before();
         mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
@@ -606,6 +622,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
+#pragma unroll
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_at(bar0, BAR_Q_FULL + s), 1);
             mbar_init(bar_at(bar0, BAR_Q_ROT + s), 128);
@@ -646,15 +663,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_c
     const int t_end = p.task_off[blockIdx.x + 1];
 
     if (warp < 8) {
+        regs_increase<kRegsSoftmax>();
         softmax_role<D, CAUSAL>(p, warp / 4, bar0, tmem, t_begin, t_end, ctl, threadIdx.x % 128);
     } else if (warp < kWarpTma) {
+        regs_decrease<kRegsRope>();
         if (ROPE) rope_role<D>(p, CAUSAL, smg, bar0, t_begin, t_end, ctl, threadIdx.x - kWarpRope * 32);
-    } else if (warp == kWarpTma) {
-        if (lane == 0) producer_role<D>(p, CAUSAL, sm, bar0, t_begin, t_end, ctl);
-        __syncwarp();
     } else {
-        if (lane == 0) mma_role<D, ROPE>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);
-        __syncwarp();
+        regs_decrease<kRegsOther>();
+        if (warp == kWarpTma) {
+            if (lane == 0) producer_role<D>(p, CAUSAL, sm, bar0, t_begin, t_end, ctl);
+            __syncwarp();
+        } else if (warp == kWarpMma) {
+            if (lane == 0) mma_role<D, ROPE>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);
+            __syncwarp();
+        }
     }
 
     tc_fence_before();

@@ -338,6 +338,14 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
     const int kbar_ready = ROPE ? BAR_K_ROT : BAR_K_FULL;
     const int qbar_ready = ROPE ? BAR_Q_ROT : BAR_Q_FULL;
 
+    static_assert(kKStages == 2 && kVStages == 2, "descriptor selects below assume two stages");
+    // operand descriptors, built once; each MMA step only advances the start address
+    const uint64_t qdesc0 = sw128_desc(sm + L::kQ, 16u, 1024u);
+    const uint64_t qdesc1 = sw128_desc(sm + L::kQ + L::kTileBytes, 16u, 1024u);
+    const uint64_t kdesc0 = sw128_desc(sm + L::kK, 16u, 1024u);
+    const uint64_t kdesc1 = sw128_desc(sm + L::kK + L::kTileBytes, 16u, 1024u);
+    const uint64_t vdesc0 = sw128_desc(sm + L::kV, kSubTileBytes, 1024u);
+    const uint64_t vdesc1 = sw128_desc(sm + L::kV + L::kTileBytes, kSubTileBytes, 1024u);
     int kit = 0, vit = 0;
     int qit[2] = {0, 0}, pit[2] = {0, 0}, oit[2] = {0, 0};
     bool ok = true;
@@ -349,21 +357,20 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
             const int vs = vit % kVStages;
             const bool do_s = n >= 0;
             const bool do_pv = n + 1 <= u.nmax;
-            if (do_s) {
-                ok = mbar_wait(bar_at(bar0, kbar_ready + ks), (kit / kKStages) & 1, ctl, kStatusMma);
-                if (!ok) break;
-            }
-            if (do_pv) {
-                ok = mbar_wait(bar_at(bar0, BAR_V_FULL + vs), (vit / kVStages) & 1, ctl, kStatusMma);
-                if (!ok) break;
-            }
-            tc_fence_after();
+            // each wait sits right before the first MMA that needs it, so a PV
+            // never waits for the next K tile (or its rotation)
+            bool k_ready = false, v_ready = false;
 #pragma unroll
             for (int s = 0; s < 2 && ok; ++s) {
                 if (!u.valid[s]) continue;
                 const uint32_t tS = tmem + static_cast<uint32_t>(s * 128);
                 const uint32_t tO = tmem + 256u + static_cast<uint32_t>(s * 128);
                 if (do_pv && n + 1 <= u.nhi[s]) {
+                    if (!v_ready) {
+                        ok = mbar_wait(bar_at(bar0, BAR_V_FULL + vs), (vit / kVStages) & 1, ctl, kStatusMma);
+                        if (!ok) break;
+                        v_ready = true;
+                    }
                     ok = mbar_wait(bar_at(bar0, BAR_P_FULL + s), pit[s] & 1, ctl, kStatusMma);
                     if (!ok) break;
                     ++pit[s];
@@ -372,27 +379,34 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                         if (!ok) break;
                     }
                     tc_fence_after();
-                    const uint32_t vbase = sm + L::kV + vs * L::kTileBytes;
+                    const uint64_t vdesc = vs ? vdesc1 : vdesc0;
+                    // 16 keys per step: 2048 bytes of V, 8 TMEM columns of P
+                    umma_ts(tO, tS, vdesc, kIdescPV, first_pv[s] ? 0u : 1u);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint64_t bdesc = sw128_desc(vbase + kk * 2048u, kSubTileBytes, 1024u);
-                        umma_ts(tO, tS + kk * 8u, bdesc, kIdescPV, (first_pv[s] && kk == 0) ? 0u : 1u);
-                    }
+                    for (int kk = 1; kk < kBlockN / 16; ++kk)
+                        umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, 1u);
                     first_pv[s] = false;
                 }
                 if (do_s && n <= u.nhi[s]) {
+                    if (!k_ready) {
+                        ok = mbar_wait(bar_at(bar0, kbar_ready + ks), (kit / kKStages) & 1, ctl, kStatusMma);
+                        if (!ok) break;
+                        k_ready = true;
+                        tc_fence_after();
+                    }
                     if (n == u.nhi[s]) {
                         ok = mbar_wait(bar_at(bar0, qbar_ready + s), qit[s] & 1, ctl, kStatusMma);
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    const uint32_t qbase = sm + L::kQ + s * L::kTileBytes;
-                    const uint32_t kbase = sm + L::kK + ks * L::kTileBytes;
+                    const uint64_t qdesc = s ? qdesc1 : qdesc0;
+                    const uint64_t kdesc = ks ? kdesc1 : kdesc0;
+                    // 16 channels per step: 32 bytes inside a 128-byte row, next column block every 4 steps
+                    umma_ss(tS, qdesc, kdesc, kIdescQK, 0u);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * kSubTileBytes + (kk % 4) * 32u;
-                        umma_ss(tS, sw128_desc(qbase + off, 16u, 1024u), sw128_desc(kbase + off, 16u, 1024u),
-                                kIdescQK, kk > 0 ? 1u : 0u);
+                    for (int kk = 1; kk < D / 16; ++kk) {
+                        const uint32_t units = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
+                        umma_ss(tS, desc_advance(qdesc, units), desc_advance(kdesc, units), kIdescQK, 1u);
                     }
                     tc_commit(bar_at(bar0, BAR_S_FULL + s));
                     if (n == 0) {

@@ -172,6 +172,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// A descriptor moved by `units` x 16 bytes: only the 14-bit start-address
+// field changes (callers keep the sum below 2^14, i.e. inside shared memory).
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t units) {
+    uint32_t lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+    lo += units;
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, A/B format
 // (0 = fp16, 1 = bf16), B major-ness (0 = K-major, 1 = MN-major), M, N.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(uint32_t ab_format, uint32_t b_mn_major, uint32_t M,

@@ -110,3 +110,21 @@ def test_rope_causal_s8192_sampled():
 
 def test_gqa_outliers_s16384_sampled():
     _sampled(1, 32, 8, 16384, 128, True, 500000.0, outliers=0.01)
+
+
+@pytest.mark.parametrize("base", [None, 10000.0])
+def test_late_large_score_rescales_running_max(base):
+    """A key visited last (key 100: chunk 3 of tile 0, reverse traversal) whose
+    score exceeds every earlier one by ~10 in log2 units.  The running max must
+    move mid-tile: O, the P chunks already written and the partial sums are
+    rescaled (the softmax's rare path)."""
+    B, H, S, D = 1, 2, 640, 128
+    q = si.bf16_bits_to_f64(si.bshd_bf16(31, 1, B, S, H, D)) * 0.3 + 1.0
+    k = si.bf16_bits_to_f64(si.bshd_bf16(31, 2, B, S, H, D)) * 0.3
+    k[:, 100] = 0.7
+    v = si.bf16_bits_to_f64(si.bshd_bf16(31, 3, B, S, H, D))
+    q, k, v = (si.f64_to_bf16_bits(x.reshape(-1)).reshape(x.shape) for x in (q, k, v))
+    o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=True, rope_base=base)
+    attn.attn_check()
+    o_ref, lse_ref = oracle.attn_full(q, k, v, causal=True, rope_base=base)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "late large score")

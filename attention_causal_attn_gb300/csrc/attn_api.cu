@@ -33,6 +33,11 @@ struct RopeEntry {
     double base;
     float2* table;
 };
+struct WinEntry {
+    int dev, S, D;
+    double base, k;
+    short2* table;
+};
 struct SchedEntry {
     int dev, B, Hq, Hkv, S, causal, ctas;
     uint2* tasks;
@@ -42,7 +47,7 @@ struct DevInfo {
     bool probed = false, ok = false;
     int sms = 0;
     int* status = nullptr;
-    unsigned configured = 0;  // kernel variants whose smem attribute was set
+    unsigned configured = 0;  // kernel variants whose smem attribute was set (bit per variant)
 };
 
 std::mutex g_mu;
@@ -61,6 +66,7 @@ int cuda_fail(const char* what, cudaError_t e, int code = ATTN_ERR_CUDA) {
 }
 std::vector<RopeEntry> g_rope;
 std::vector<SchedEntry> g_sched;
+std::vector<WinEntry> g_win;
 DevInfo g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -79,17 +85,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [B][S][H][D] bf16 as a 4-D tensor (innermost first: D, H, S, B); box
 // {64, 1, 128, 1} = 128 rows of one head and 64 channels, 128-byte swizzle.
 // Rows past S read as zero.
-bool encode_bshd(CUtensorMap* m, const void* base, int B, int S, int H, int D) {
+bool encode_bshd(CUtensorMap* m, const void* base, int B, int S, int H, int D, int box_inner = 64,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
                                    static_cast<cuuint64_t>(S) * H * D * 2};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, 128, 1};
     const cuuint32_t elem[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, elem,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -130,6 +137,26 @@ int get_rope(int dev, int S, int D, double base, float2** out) {
     return ATTN_OK;
 }
 
+int get_wtab(int dev, int S, int D, double base, double k, short2** out) {
+    for (auto& e : g_win)
+        if (e.dev == dev && e.S == S && e.D == D && e.base == base && e.k == k) {
+            *out = e.table;
+            return ATTN_OK;
+        }
+    const std::vector<int16_t> host = attn_host::window_tile_table(S, D, base, k);
+    short2* d = nullptr;
+    cudaError_t e;
+    if ((e = cudaMalloc(&d, host.size() * sizeof(int16_t))) != cudaSuccess)
+        return cuda_fail("cudaMalloc(window table)", e, ATTN_ERR_OOM);
+    if ((e = cudaMemcpy(d, host.data(), host.size() * sizeof(int16_t), cudaMemcpyHostToDevice)) != cudaSuccess) {
+        cudaFree(d);
+        return cuda_fail("cudaMemcpy(window table)", e);
+    }
+    g_win.push_back({dev, S, D, base, k, d});
+    *out = d;
+    return ATTN_OK;
+}
+
 int get_schedule(int dev, int B, int Hq, int Hkv, int S, int causal, int sms, const SchedEntry** out) {
     for (auto& e : g_sched)
         if (e.dev == dev && e.B == B && e.Hq == Hq && e.Hkv == Hkv && e.S == S && e.causal == causal) {
@@ -159,14 +186,13 @@ int get_schedule(int dev, int B, int Hq, int Hkv, int S, int causal, int sms, co
     return ATTN_OK;
 }
 
-template <int D, bool CAUSAL, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE, bool WINDOW = false>
 int launch(const FwdParams& prm, int grid, cudaStream_t stream, DevInfo& di) {
-    constexpr unsigned bit = 1u << ((D == 128 ? 4 : 0) | (CAUSAL ? 2 : 0) | (ROPE ? 1 : 0));
-    auto kern = attn::attn_fwd_kernel<D, CAUSAL, ROPE>;
+    constexpr unsigned bit = 1u << ((WINDOW ? 8 : 0) | (D == 128 ? 4 : 0) | (CAUSAL ? 2 : 0) | (ROPE ? 1 : 0));
+    auto kern = attn::attn_fwd_kernel<D, CAUSAL, ROPE, WINDOW>;
     // At least 120 KB so that only one CTA fits on an SM: each CTA takes all 512 TMEM columns.
-    constexpr int smem = static_cast<int>(attn::SmemLayout<D>::kAlloc) > 120 * 1024
-                             ? static_cast<int>(attn::SmemLayout<D>::kAlloc)
-                             : 120 * 1024;
+    using Layout = attn::SmemLayout<D, attn::k_stages<WINDOW>()>;
+    constexpr int smem = static_cast<int>(Layout::kAlloc) > 120 * 1024 ? static_cast<int>(Layout::kAlloc) : 120 * 1024;
     cudaError_t e;
     if (!(di.configured & bit)) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
@@ -196,7 +222,6 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     if (rope_base > 0.0 && !std::isfinite(rope_base)) return ATTN_ERR_UNSUPPORTED;
     const bool window = window_k > 0.0 && !std::isinf(window_k);
     if (window && !(rope && causal)) return ATTN_ERR_UNSUPPORTED;
-    if (window) return ATTN_ERR_UNSUPPORTED;  // the windowed kernel variant is not built yet
     if (std::isnan(window_k) || std::isnan(rope_base)) return ATTN_ERR_UNSUPPORTED;
 
     int dev = 0;
@@ -206,19 +231,27 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     FwdParams prm;
     SchedEntry sched;  // copied under the lock: the cache vector may grow later
     float2* rope_tab = nullptr;
+    short2* wtab = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         int rc = probe_device(dev);
         if (rc != ATTN_OK) return rc;
         if (rope && (rc = get_rope(dev, S, D, rope_base, &rope_tab)) != ATTN_OK) return rc;
+        if (window && (rc = get_wtab(dev, S, D, rope_base, window_k, &wtab)) != ATTN_OK) return rc;
         const SchedEntry* se = nullptr;
         if ((rc = get_schedule(dev, B, Hq, Hkv, S, causal, g_dev[dev].sms, &se)) != ATTN_OK) return rc;
         sched = *se;
         prm.status = g_dev[dev].status;
     }
     if (!encode_bshd(&prm.tm_q, q, B, S, Hq, D) || !encode_bshd(&prm.tm_k, k, B, S, Hkv, D) ||
-        !encode_bshd(&prm.tm_v, v, B, S, Hkv, D))
+        !encode_bshd(&prm.tm_v, v, B, S, Hkv, D) ||
+        (window && !encode_bshd(&prm.tm_k16, k, B, S, Hkv, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)))
         return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    {
+        const std::vector<int32_t> w = attn_host::window_widths(D, rope ? rope_base : 10000.0, window ? window_k : 0.0);
+        for (int r = 0; r < 64; ++r) prm.win[r] = r < D / 2 ? w[r] : INT32_MAX;
+    }
+    prm.wtab = wtab;
     prm.o = static_cast<__nv_bfloat16*>(o);
     prm.lse = lse;
     prm.rope = rope_tab;
@@ -234,6 +267,8 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     DevInfo& di = g_dev[dev];
     const int grid = sched.ctas;
+    if (window)  // RoPE and causal masking are implied (checked above)
+        return D == 128 ? launch<128, true, true, true>(prm, grid, st, di) : launch<64, true, true, true>(prm, grid, st, di);
     if (D == 128) {
         if (causal) return rope ? launch<128, true, true>(prm, grid, st, di) : launch<128, true, false>(prm, grid, st, di);
         return rope ? launch<128, false, true>(prm, grid, st, di) : launch<128, false, false>(prm, grid, st, di);
@@ -340,6 +375,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     prm.o = static_cast<__nv_bfloat16*>(o);
     prm.lse = lse;
     prm.rope = rope ? reinterpret_cast<const float2*>(na.scratch) : nullptr;
+    prm.wtab = nullptr;
     prm.tasks = reinterpret_cast<const uint2*>(na.scratch + na.off_tasks);
     prm.task_off = reinterpret_cast<const int*>(na.scratch + na.off_offsets);
     prm.status = g_dev[dev].status;
@@ -424,7 +460,12 @@ extern "C" void attn_release_cache(void) {
         cudaFree(e.tasks);
         cudaFree(e.offsets);
     }
+    for (auto& e : g_win) {
+        cudaSetDevice(e.dev);
+        cudaFree(e.table);
+    }
     g_rope.clear();
     g_sched.clear();
+    g_win.clear();
     if (have) cudaSetDevice(cur);
 }

@@ -52,7 +52,11 @@ namespace attn {
 
 constexpr int kBlockM = 128;  // query rows per stage
 constexpr int kBlockN = 128;  // keys per KV tile
-constexpr int kKStages = 2;
+constexpr int kMaxKStages = 3;
+// K ring depth: the windowed variant holds each K tile until its PV is issued
+// (the softmax reads boundary pairs from it), so it keeps one more tile in flight.
+template <bool WINDOW>
+__host__ __device__ constexpr int k_stages() { return WINDOW ? 3 : 2; }
 constexpr int kVStages = 2;
 constexpr int kNumThreads = 512;  // four warpgroups; launched at 128 registers per thread
 constexpr int kWarpRope = 8;
@@ -73,6 +77,7 @@ struct FwdParams {
     CUtensorMap tm_q;  // [B][S][Hq][D] bf16, box {64, 1, 128, 1}, 128B swizzle
     CUtensorMap tm_k;  // [B][S][Hkv][D]
     CUtensorMap tm_v;
+    CUtensorMap tm_k16; // K again, box {16, 1, 128, 1}, 32-byte swizzle (windowed variant: one 16-channel group per load)
     __nv_bfloat16* o;   // [B][S][Hq][D]
     float* lse;         // [B][Hq][S] or null
     const float2* rope; // RoPE factor tables (see RopeGeom), null when RoPE is off
@@ -82,6 +87,9 @@ struct FwdParams {
     int B, Hq, Hkv, S;
     float scale_log2;   // log2(e) / sqrt(D)
     unsigned long long wait_limit_ns;
+    int win[64];        // W_r = floor(k * 2*pi / theta_r), ascending in r (windowed variant)
+    const short2* wtab; // windowed variant, per tile distance: (first pair kept at the tile's smallest distance,
+                        // first pair kept at its largest), see window_tile
 };
 
 // barrier slots
@@ -90,9 +98,9 @@ enum : int {
     BAR_Q_ROT = 2,    // [2] Q_s rotated (RoPE)
     BAR_Q_EMPTY = 4,  // [2] last QK^T of the unit read Q_s
     BAR_K_FULL = 6,   // [kKStages]
-    BAR_K_ROT = BAR_K_FULL + kKStages,
-    BAR_K_EMPTY = BAR_K_ROT + kKStages,
-    BAR_V_FULL = BAR_K_EMPTY + kKStages,  // [kVStages]
+    BAR_K_ROT = BAR_K_FULL + kMaxKStages,
+    BAR_K_EMPTY = BAR_K_ROT + kMaxKStages,
+    BAR_V_FULL = BAR_K_EMPTY + kMaxKStages,  // [kVStages]
     BAR_V_EMPTY = BAR_V_FULL + kVStages,
     BAR_S_FULL = BAR_V_EMPTY + kVStages,  // [2] S_s(n) in TMEM (and PV_s(n+1) done)
     BAR_P_FULL = BAR_S_FULL + 2,          // [2] P_s(n) in TMEM, O_s rescaled
@@ -102,12 +110,12 @@ enum : int {
     NUM_BARS = BAR_DRAIN + 1
 };
 
-template <int D>
+template <int D, int KS>
 struct SmemLayout {
     static constexpr uint32_t kTileBytes = 128u * D * 2u;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kK = kQ + 2 * kTileBytes;
-    static constexpr uint32_t kV = kK + kKStages * kTileBytes;
+    static constexpr uint32_t kV = kK + KS * kTileBytes;
     static constexpr uint32_t kBars = kV + kVStages * kTileBytes;
     static constexpr uint32_t kMisc = kBars + 8 * NUM_BARS;
     static constexpr uint32_t kBytes = kMisc + 16;
@@ -143,11 +151,44 @@ __device__ __forceinline__ Unit decode_unit(uint2 w, const FwdParams& p, bool ca
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int i) { return bar0 + 8u * static_cast<uint32_t>(i); }
 
-// ------------------------------------------------------------------ producer
+// ------------------------------------------------------------------ window geometry
+// Per-RoPE-pair window ("ATFlash", The idea): pair r of cell (i, j) is kept
+// iff the distance i - j <= W_r.  W_r grows with r, so the pairs a cell drops
+// are a prefix.  Query tile qt against key tile n covers distances
+// 128*(qt-n) - 127 .. 128*(qt-n) + 127, so the bounds depend on the tile
+// distance qt - n only; the host tabulates, per tile distance,
+//   .x = first pair kept at the tile's smallest distance (pairs below are
+//        dropped for every cell),
+//   .y = first pair kept at its largest distance (pairs from here on are kept
+//        for every cell); pairs in [.x, .y) are the tile's boundary pairs.
+//
+// Pairs below z are dropped for every cell of the KV tile against every query
+// tile of the unit.  K is held as D/16 groups of 16 channels (one K=16 MMA
+// step each); the 16-pair blocks below m0 = z / 16 are never loaded nor
+// multiplied (for block m: channel groups m and m + D/32), and the pairs of
+// block m0 below z are zeroed in shared memory.
+struct WinTile {
+    int z, m0;
+};
 template <int D>
+__device__ __forceinline__ WinTile window_tile(const FwdParams& p, const Unit& u, int n) {
+    // only the stages that visit key tile n count (n <= nhi, so the tile distance is >= 0)
+    int z = D / 2;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+        if (u.valid[s] && n <= u.nhi[s]) z = min(z, static_cast<int>(p.wtab[u.row0[s] / kBlockM - n].x));
+    WinTile w;
+    w.z = z;
+    w.m0 = min(z / 16, D / 32 - 1);
+    return w;
+}
+
+// ------------------------------------------------------------------ producer
+template <int D, bool WINDOW>
 __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, int t_begin, int t_end,
                               const WaitCtl& ctl) {
-    using L = SmemLayout<D>;
+    constexpr int kKStages = k_stages<WINDOW>();
+    using L = SmemLayout<D, kKStages>;
     int kit = 0, vit = 0;
     int qit[2] = {0, 0};
     for (int ti = t_begin; ti < t_end; ++ti) {
@@ -165,12 +206,25 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
         }
         for (int n = u.nmax; n >= 0; --n) {
             const int ks = kit % kKStages;
+            const WinTile w = WINDOW ? window_tile<D>(p, u, n) : WinTile{0, 0};  // before the wait: load in flight
             if (!mbar_wait(bar_at(bar0, BAR_K_EMPTY + ks), ((kit / kKStages) & 1) ^ 1, ctl, kStatusProducer)) return;
             const uint32_t kb = bar_at(bar0, BAR_K_FULL + ks);
-            mbar_arrive_expect_tx(kb, L::kTileBytes);
-            for (int sub = 0; sub < D / 64; ++sub)
-                tma_load_4d(sm + L::kK + ks * L::kTileBytes + sub * kSubTileBytes, &p.tm_k, kb, sub * 64, u.kvh,
-                            n * kBlockN, u.b);
+            if (WINDOW) {
+                // only the 16-pair blocks with a kept pair: 16 channels x 128 rows = 4 KB per group, two per block
+                constexpr int kBlocks = D / 32;
+                mbar_arrive_expect_tx(kb, static_cast<uint32_t>(2 * (kBlocks - w.m0)) * 4096u);
+                for (int m = w.m0; m < kBlocks; ++m) {
+                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + m * 4096u, &p.tm_k16, kb, 16 * m, u.kvh,
+                                n * kBlockN, u.b);
+                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + (m + kBlocks) * 4096u, &p.tm_k16, kb,
+                                D / 2 + 16 * m, u.kvh, n * kBlockN, u.b);
+                }
+            } else {
+                mbar_arrive_expect_tx(kb, L::kTileBytes);
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + sub * kSubTileBytes, &p.tm_k, kb, sub * 64, u.kvh,
+                                n * kBlockN, u.b);
+            }
             ++kit;
             const int vs = vit % kVStages;
             if (!mbar_wait(bar_at(bar0, BAR_V_EMPTY + vs), ((vit / kVStages) & 1) ^ 1, ctl, kStatusProducer)) return;
@@ -185,15 +239,19 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
 }
 
 // ------------------------------------------------------------------ RoPE
-// Rotation of one 128-row tile in place.  The tile is stored as D/64 column
-// blocks of [128 rows][128 B] with the 128-byte swizzle (16-byte chunk c of
-// row r sits at chunk c ^ (r & 7)).  Pair (r, r + D/2) has both members at the
-// same swizzled offset in column blocks 0 and 1 for D = 128, and in chunks c
-// and c + 4 of the single block for D = 64, so each thread rotates whole pairs
-// from two 16-byte loads.  Input bf16, math fp32, output fp16.
+// Rotation of one 128-row tile in place.  Q and K tiles are stored as D/64
+// column blocks of [128 rows][128 B] with the 128-byte swizzle (16-byte chunk
+// c of row r sits at chunk c ^ (r & 7)).  Pair (r, r + D/2) has both members
+// at the same swizzled offset in column blocks 0 and 1 for D = 128, and in
+// chunks c and c + 4 of the single block for D = 64, so each thread rotates
+// whole pairs from two 16-byte loads.  The windowed variant stores K as D/16
+// channel groups of [128 rows][32 B] with the 32-byte swizzle (group g at
+// g * 4 KB; the 16-byte half h of row r sits at half h ^ ((r >> 2) & 1)), so
+// that dropped groups are never loaded.  Input bf16, math fp32, output fp16.
 //
-// Thread t owns chunk c = t % kChunks (pairs 8c..8c+7) of rows rr + kRows*i,
-// rr = t / kChunks.  Angles come from the angle-addition rule, as complex
+// Thread t owns chunk c = t / kRows (pairs 8c..8c+7) of rows rr + kRows*i,
+// rr = t % kRows: eight consecutive threads touch eight rows of one chunk,
+// which is free of bank conflicts in both layouts.  Angles come from the angle-addition rule, as complex
 // numbers: the angle of row pos0 + rr is base(pos0) * rowfac(rr), with
 // base(pos0) = (cos, sin)(pos0 theta) read once per tile, and each pass
 // advances it by step = (cos, sin)(kRows theta).  The host computes every
@@ -230,7 +288,7 @@ template <int D>
 __device__ __forceinline__ void rope_load_consts(const FwdParams& p, int t, RopeConsts& k) {
     using G = RopeGeom<D>;
     const int ntiles = (p.S + kBlockM - 1) / kBlockM;
-    const int c = t % G::kChunks, rr = t / G::kChunks;
+    const int c = t / G::kRows, rr = t % G::kRows;
     load8_packed(p.rope + (static_cast<size_t>(ntiles) + rr) * G::kHalf + 8 * c, k.cr, k.sr);
     load8_packed(p.rope + (static_cast<size_t>(ntiles) + G::kRows) * G::kHalf + 8 * c, k.cs, k.ss);
 }
@@ -239,7 +297,7 @@ template <int D>
 __device__ __forceinline__ void rope_load_base(const FwdParams& p, int tile, int t, uint64_t (&cb)[4],
                                                uint64_t (&sb)[4]) {
     using G = RopeGeom<D>;
-    load8_packed(p.rope + static_cast<size_t>(tile) * G::kHalf + 8 * (t % G::kChunks), cb, sb);
+    load8_packed(p.rope + static_cast<size_t>(tile) * G::kHalf + 8 * (t / G::kRows), cb, sb);
 }
 
 // (c, s) <- (c, s) * (fc, fs) as complex numbers, two pairs per operand.
@@ -249,11 +307,12 @@ __device__ __forceinline__ void cmul2(uint64_t& c, uint64_t& s, uint64_t fc, uin
     c = nc;
 }
 
-template <int D>
+// LAYOUT_GROUPS: the windowed K layout; pairs below `zero_below` come out as 0.
+template <int D, bool LAYOUT_GROUPS>
 __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts& k, uint64_t (&cb)[4],
-                                                 uint64_t (&sb)[4], int t) {
+                                                 uint64_t (&sb)[4], int t, int zero_below = 0) {
     using G = RopeGeom<D>;
-    const int c = t % G::kChunks, rr = t / G::kChunks;
+    const int c = t / G::kRows, rr = t % G::kRows;
     // angle of this thread's first row
 #pragma unroll
     for (int q = 0; q < 4; ++q) cmul2(cb[q], sb[q], k.cr[q], k.sr[q]);
@@ -261,7 +320,11 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
     for (int i = 0; i < G::kIters; ++i) {
         const int row = rr + G::kRows * i;
         uint32_t lo_off, hi_off;
-        if (D == 128) {
+        if (LAYOUT_GROUPS) {
+            const uint32_t half = static_cast<uint32_t>(((c & 1) ^ ((row >> 2) & 1)) << 4);
+            lo_off = static_cast<uint32_t>((c >> 1) * 4096 + row * 32) + half;
+            hi_off = lo_off + static_cast<uint32_t>(G::kChunks / 2 * 4096);
+        } else if (D == 128) {
             lo_off = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
             hi_off = lo_off + kSubTileBytes;
         } else {
@@ -282,6 +345,12 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
             f2_unpack(f2_fma(y, cb[q], f2_mul(x, sb[q])), b0, b1);           // y cos + x sin
             lo_out[q] = pack_f16x2(a0, a1);
             hi_out[q] = pack_f16x2(b0, b1);
+            if (LAYOUT_GROUPS) {  // pairs 8c+2q, 8c+2q+1 below zero_below are dropped
+                const int pr = 8 * c + 2 * q;
+                const uint32_t keep = (pr >= zero_below ? 0x0000FFFFu : 0u) | (pr + 1 >= zero_below ? 0xFFFF0000u : 0u);
+                lo_out[q] &= keep;
+                hi_out[q] &= keep;
+            }
         }
         *reinterpret_cast<uint4*>(tile + lo_off) = make_uint4(lo_out[0], lo_out[1], lo_out[2], lo_out[3]);
         *reinterpret_cast<uint4*>(tile + hi_off) = make_uint4(hi_out[0], hi_out[1], hi_out[2], hi_out[3]);
@@ -290,10 +359,11 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
     }
 }
 
-template <int D>
+template <int D, bool WINDOW>
 __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_t bar0, int t_begin, int t_end,
                           const WaitCtl& ctl, int t) {
-    using L = SmemLayout<D>;
+    constexpr int kKStages = k_stages<WINDOW>();
+    using L = SmemLayout<D, kKStages>;
     RopeConsts k;
     rope_load_consts<D>(p, t, k);
     int kit = 0;
@@ -307,7 +377,7 @@ __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_
             rope_load_base<D>(p, u.row0[s] / kBlockM, t, cb, sb);
             if (!__all_sync(0xffffffffu, mbar_wait(bar_at(bar0, BAR_Q_FULL + s), qit[s] & 1, ctl, kStatusRope)))
                 return;
-            rope_rotate_tile<D>(smg + L::kQ + s * L::kTileBytes, k, cb, sb, t);
+            rope_rotate_tile<D, false>(smg + L::kQ + s * L::kTileBytes, k, cb, sb, t);
             fence_proxy_async_smem();
             mbar_arrive(bar_at(bar0, BAR_Q_ROT + s));
             ++qit[s];
@@ -315,10 +385,18 @@ __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_
         for (int n = u.nmax; n >= 0; --n) {
             const int ks = kit % kKStages;
             rope_load_base<D>(p, n, t, cb, sb);
+            const WinTile w = WINDOW ? window_tile<D>(p, u, n) : WinTile{0, 0};  // before the wait: load in flight
             if (!__all_sync(0xffffffffu,
                             mbar_wait(bar_at(bar0, BAR_K_FULL + ks), (kit / kKStages) & 1, ctl, kStatusRope)))
                 return;
-            rope_rotate_tile<D>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t);
+            if (WINDOW) {
+                using G = RopeGeom<D>;
+                const int c = t / G::kRows;
+                // chunk c is in block c / 2; blocks below m0 were not loaded and are not multiplied
+                if (c / 2 >= w.m0) rope_rotate_tile<D, true>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t, w.z);
+            } else {
+                rope_rotate_tile<D, false>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t);
+            }
             fence_proxy_async_smem();
             mbar_arrive(bar_at(bar0, BAR_K_ROT + ks));
             ++kit;
@@ -327,10 +405,11 @@ __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool WINDOW>
 __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, uint32_t tmem, int t_begin,
                          int t_end, const WaitCtl& ctl) {
-    using L = SmemLayout<D>;
+    constexpr int kKStages = k_stages<WINDOW>();
+    using L = SmemLayout<D, kKStages>;
     // QK^T: A = Q tile, B = K tile, both K-major; fp16 after rotation, bf16 otherwise.
     constexpr uint32_t kIdescQK = umma_idesc_f16(ROPE ? 0u : 1u, 0u, kBlockM, kBlockN);
     // PV: A = P (bf16, TMEM), B = V tile [keys][D] with D contiguous: MN-major.
@@ -338,15 +417,15 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
     const int kbar_ready = ROPE ? BAR_K_ROT : BAR_K_FULL;
     const int qbar_ready = ROPE ? BAR_Q_ROT : BAR_Q_FULL;
 
-    static_assert(kKStages == 2 && kVStages == 2, "descriptor selects below assume two stages");
+    static_assert(kVStages == 2, "descriptor selects below assume two V stages");
     // operand descriptors, built once; each MMA step only advances the start address
     const uint64_t qdesc0 = sw128_desc(sm + L::kQ, 16u, 1024u);
     const uint64_t qdesc1 = sw128_desc(sm + L::kQ + L::kTileBytes, 16u, 1024u);
-    const uint64_t kdesc0 = sw128_desc(sm + L::kK, 16u, 1024u);
-    const uint64_t kdesc1 = sw128_desc(sm + L::kK + L::kTileBytes, 16u, 1024u);
+    // windowed K: one 16-channel group of [128 rows][32 B] per K=16 step, 32-byte swizzle, 8-row atoms 256 B apart
+    const uint64_t kdesc0 = WINDOW ? sw32_desc(sm + L::kK, 256u) : sw128_desc(sm + L::kK, 16u, 1024u);
     const uint64_t vdesc0 = sw128_desc(sm + L::kV, kSubTileBytes, 1024u);
     const uint64_t vdesc1 = sw128_desc(sm + L::kV + L::kTileBytes, kSubTileBytes, 1024u);
-    int kit = 0, vit = 0;
+    int kit = 0, vit = 0, krel = 0;
     int qit[2] = {0, 0}, pit[2] = {0, 0}, oit[2] = {0, 0};
     bool ok = true;
     for (int ti = t_begin; ti < t_end && ok; ++ti) {
@@ -386,6 +465,11 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                     for (int kk = 1; kk < kBlockN / 16; ++kk)
                         umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, 1u);
                     first_pv[s] = false;
+                    if (WINDOW && n + 1 == 0) {
+                        // windowed: the softmax reads Q_s until it hands over the unit's last P
+                        tc_commit(bar_at(bar0, BAR_Q_EMPTY + s));
+                        ++qit[s];
+                    }
                 }
                 if (do_s && n <= u.nhi[s]) {
                     if (!k_ready) {
@@ -400,16 +484,29 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                         tc_fence_after();
                     }
                     const uint64_t qdesc = s ? qdesc1 : qdesc0;
-                    const uint64_t kdesc = ks ? kdesc1 : kdesc0;
-                    // 16 channels per step: 32 bytes inside a 128-byte row, next column block every 4 steps
-                    umma_ss(tS, qdesc, kdesc, kIdescQK, 0u);
+                    const uint64_t kdesc = desc_advance(kdesc0, static_cast<uint32_t>(ks) * (L::kTileBytes >> 4));
+                    if (WINDOW) {
+                        // k-step kk covers pairs of block kk % (D/32); blocks below m0 hold only dropped pairs
+                        const int m0 = window_tile<D>(p, u, n).m0;
+                        uint32_t acc = 0u;
 #pragma unroll
-                    for (int kk = 1; kk < D / 16; ++kk) {
-                        const uint32_t units = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
-                        umma_ss(tS, desc_advance(qdesc, units), desc_advance(kdesc, units), kIdescQK, 1u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            if (kk % (D / 32) < m0) continue;
+                            const uint32_t qunits = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
+                            umma_ss(tS, desc_advance(qdesc, qunits), desc_advance(kdesc, kk * 256u), kIdescQK, acc);
+                            acc = 1u;
+                        }
+                    } else {
+                        // 16 channels per step: 32 bytes inside a 128-byte row, next column block every 4 steps
+                        umma_ss(tS, qdesc, kdesc, kIdescQK, 0u);
+#pragma unroll
+                        for (int kk = 1; kk < D / 16; ++kk) {
+                            const uint32_t units = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
+                            umma_ss(tS, desc_advance(qdesc, units), desc_advance(kdesc, units), kIdescQK, 1u);
+                        }
                     }
                     tc_commit(bar_at(bar0, BAR_S_FULL + s));
-                    if (n == 0) {
+                    if (!WINDOW && n == 0) {
                         tc_commit(bar_at(bar0, BAR_Q_EMPTY + s));
                         ++qit[s];
                     }
@@ -417,8 +514,13 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
             }
             if (!ok) break;
             if (do_s) {
-                tc_commit(bar_at(bar0, BAR_K_EMPTY + ks));
+                if (!WINDOW) tc_commit(bar_at(bar0, BAR_K_EMPTY + ks));
                 ++kit;
+            }
+            if (WINDOW && do_pv) {
+                // windowed: the softmax reads K(n+1) until it hands over P(n+1), which the PVs above waited for
+                tc_commit(bar_at(bar0, BAR_K_EMPTY + krel % kKStages));
+                ++krel;
             }
             if (do_pv) {
                 tc_commit(bar_at(bar0, BAR_V_EMPTY + vs));
@@ -513,12 +615,66 @@ __device__ __forceinline__ float tile_exp_to_p(uint32_t taddr, int limit, float 
     return s0 + s1;
 }
 
+// Windowed variant, boundary pairs: pairs in [r_begin, r_end) are kept by the
+// QK^T product for this tile but dropped for some of its cells (distance
+// i - j > W_r).  Their exact terms q'_r k'_r + q'_{r+D/2} k'_{r+D/2} are
+// subtracted from those cells of this thread's row, from the same fp16
+// operands the tensor cores multiplied (the products are exact in fp32, so
+// only the summation order differs).  rel = row - first key of the tile.
+// Called by the whole warp; most tiles have no boundary pair.
+template <int D>
+__device__ __noinline__ void window_correct(uint32_t tS, const uint8_t* qtile, const uint8_t* ktile,
+                                            const FwdParams& p, int r_begin, int r_end, int rel, int t) {
+    constexpr int kHalf = D / 2;
+    const int lane = t & 31;
+#pragma unroll 1
+    for (int cc = 0; cc < kBlockN; cc += 32) {
+        uint32_t r[32];
+        tmem_load_32(tS + cc, r);
+#pragma unroll 1
+        for (int pr = r_begin; pr < r_end; ++pr) {
+            const int lim = rel - p.win[pr];  // keys j < lim of this tile are beyond the window for this row
+            // rows of a warp are consecutive, so lim grows by one per lane: decide per warp
+            if (!__any_sync(0xffffffffu, lim > cc)) continue;
+            const bool full = __all_sync(0xffffffffu, lim >= cc + 32);
+            const int dx = pr, dy = pr + kHalf;  // channels of the pair
+            const float qx = f16_at(qtile + (dx / 64) * kSubTileBytes + t * 128 + ((((dx % 64) / 8) ^ (t & 7)) << 4) +
+                                    (dx % 8) * 2);
+            const float qy = f16_at(qtile + (dy / 64) * kSubTileBytes + t * 128 + ((((dy % 64) / 8) ^ (t & 7)) << 4) +
+                                    (dy % 8) * 2);
+            // K in 16-channel groups with the 32-byte swizzle: channel d of key row j at
+            // (d/16)*4096 + j*32 + ((((d%16)/8) ^ ((j>>2)&1)) << 4) + (d%8)*2; cc is a multiple of 8,
+            // so the swizzle bit of key cc + j is (j >> 2) & 1
+            const uint8_t* kx = ktile + (dx / 16) * 4096 + (dx % 8) * 2 + cc * 32;
+            const uint8_t* ky = ktile + (dy / 16) * 4096 + (dy % 8) * 2 + cc * 32;
+            const int hx0 = ((dx % 16) / 8) << 4, hx1 = hx0 ^ 16;
+            const int hy0 = ((dy % 16) / 8) << 4, hy1 = hy0 ^ 16;
+            const int jmax = full ? 32 : lim - cc;  // this row's dropped keys in the chunk
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (full || j < jmax) {
+                    const bool sw = (j >> 2) & 1;
+                    const float term = fmaf(qx, f16_at(kx + j * 32 + (sw ? hx1 : hx0)),
+                                            qy * f16_at(ky + j * 32 + (sw ? hy1 : hy0)));
+                    r[j] = __float_as_uint(__uint_as_float(r[j]) - term);
+                }
+            }
+        }
+        tmem_store_32(tS + cc, r);
+    }
+    (void)lane;
+    tmem_store_wait();
+}
+
 // One body serves both stages (stage is a runtime value: a second copy of this
 // code measurably costs instruction-cache capacity).  Per-stage fields of the
 // unit are picked with selects so nothing is indexed at run time.
-template <int D, bool CAUSAL>
-__device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint32_t tmem, int t_begin, int t_end,
-                             const WaitCtl& ctl, int t) {
+template <int D, bool CAUSAL, bool WINDOW>
+__device__ void softmax_role(const FwdParams& p, int stage, uint8_t* smg, uint32_t bar0, uint32_t tmem, int t_begin,
+                             int t_end, const WaitCtl& ctl, int t) {
+    constexpr int kKStages = k_stages<WINDOW>();
+    using L = SmemLayout<D, kKStages>;
+    int kit = 0;  // K tiles seen by the unit loop (which K stage holds tile n), windowed variant
     const uint32_t lane_base = static_cast<uint32_t>(t & ~31);  // this warp's TMEM lane quarter
     const uint32_t trow = tmem + (lane_base << 16);
     const uint32_t tS = trow + static_cast<uint32_t>(stage * 128);
@@ -529,6 +685,8 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
     int sit = 0, oit = 0;
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, CAUSAL);
+        const int kit_unit = kit;  // K tiles of earlier units (tile n of this unit is the (nmax-n)-th after them)
+        kit += u.nmax + 1;
         const bool valid = stage ? u.valid[1] : u.valid[0];
         if (!valid) continue;
         const int nhi = stage ? u.nhi[1] : u.nhi[0];
@@ -542,6 +700,16 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
                 return;
             ++sit;
             tc_fence_after();
+            if (WINDOW) {
+                // boundary pairs: kept for the tile by the MMA, dropped beyond W_r for some of its cells
+                const int z = window_tile<D>(p, u, n).z;
+                const int rel0 = (stage ? u.row0[1] : u.row0[0]) - n * kBlockN;  // first row - first key
+                const int r_end = p.wtab[rel0 / kBlockM].y;                       // kept everywhere from here on
+                if (z < r_end)
+                    window_correct<D>(tS, smg + L::kQ + stage * L::kTileBytes,
+                                      smg + L::kK + ((kit_unit + u.nmax - n) % kKStages) * L::kTileBytes, p, z, r_end,
+                                      rel0 + t, t);
+            }
             // keys [0, limit) of this tile are visible to this row; only the
             // diagonal tile (causal) and the ragged last tile have a limit < 128
             const bool diag = CAUSAL && n == nhi;
@@ -622,9 +790,11 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint32_t bar0, uint3
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE, bool WINDOW>
 __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
-    using L = SmemLayout<D>;
+    static_assert(!WINDOW || (CAUSAL && ROPE), "the window is defined with RoPE and causal masking");
+    constexpr int kKStages = k_stages<WINDOW>();
+    using L = SmemLayout<D, kKStages>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sm = smem_addr(smg);
@@ -678,17 +848,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_c
 
     if (warp < 8) {
         regs_increase<kRegsSoftmax>();
-        softmax_role<D, CAUSAL>(p, warp / 4, bar0, tmem, t_begin, t_end, ctl, threadIdx.x % 128);
+        softmax_role<D, CAUSAL, WINDOW>(p, warp / 4, smg, bar0, tmem, t_begin, t_end, ctl, threadIdx.x % 128);
     } else if (warp < kWarpTma) {
         regs_decrease<kRegsRope>();
-        if (ROPE) rope_role<D>(p, CAUSAL, smg, bar0, t_begin, t_end, ctl, threadIdx.x - kWarpRope * 32);
+        if (ROPE) rope_role<D, WINDOW>(p, CAUSAL, smg, bar0, t_begin, t_end, ctl, threadIdx.x - kWarpRope * 32);
     } else {
         regs_decrease<kRegsOther>();
         if (warp == kWarpTma) {
-            if (lane == 0) producer_role<D>(p, CAUSAL, sm, bar0, t_begin, t_end, ctl);
+            if (lane == 0) producer_role<D, WINDOW>(p, CAUSAL, sm, bar0, t_begin, t_end, ctl);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            if (lane == 0) mma_role<D, ROPE>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);
+            if (lane == 0) mma_role<D, ROPE, WINDOW>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);
             __syncwarp();
         }
     }

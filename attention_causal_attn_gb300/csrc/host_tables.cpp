@@ -74,6 +74,22 @@ std::vector<int32_t> window_widths(int D, double base, double k) {
     return w;
 }
 
+std::vector<int16_t> window_tile_table(int S, int D, double base, double k) {
+    const std::vector<int32_t> w = window_widths(D, base, k);
+    const int ntiles = (S + kTile - 1) / kTile;
+    auto first = [&](long long d) {
+        int r = 0;
+        while (r < D / 2 && static_cast<long long>(w[r]) < d) ++r;
+        return static_cast<int16_t>(r);
+    };
+    std::vector<int16_t> t(static_cast<size_t>(ntiles) * 2);
+    for (int i = 0; i < ntiles; ++i) {
+        t[2 * i] = first(std::max<long long>(0, static_cast<long long>(kTile) * i - (kTile - 1)));
+        t[2 * i + 1] = first(static_cast<long long>(kTile) * i + (kTile - 1));
+    }
+    return t;
+}
+
 long long schedule_units(int B, int Hq, int Hkv, int S) {
     const long long nqt = (S + kTile - 1) / kTile;
     const long long G = Hq / Hkv;

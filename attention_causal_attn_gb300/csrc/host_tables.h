@@ -34,6 +34,12 @@ size_t rope_factor_table_floats(int S, int D);
 // the window is off (k <= 0 or infinite).  ("ATFlash", The idea.)
 std::vector<int32_t> window_widths(int D, double base, double k);
 
+// Window bounds per tile distance t = 0..ceil(S/128)-1 (query tile minus key
+// tile), as int16 pairs: [2t] = first pair r with W_r >= max(0, 128t - 127)
+// (the tile's smallest distance), [2t+1] = first pair with W_r >= 128t + 127
+// (its largest).  D/2 when no pair qualifies.
+std::vector<int16_t> window_tile_table(int S, int D, double base, double k);
+
 // One work unit = two 128-row query tiles sharing a KV head, encoded as the
 // kernel reads it: x = qtile0 | qtile1 << 16 (0xFFFF: no second tile),
 // y = h0 | h1 << 8 | b << 16.

@@ -80,16 +80,23 @@ def test_no_lse_and_side_stream_and_determinism():
     _check(o1.float().cpu().numpy(), l1.cpu().numpy(), o_ref, lse_ref)
 
 
-def _sampled(B, Hq, Hkv, S, D, causal, base, outliers=0.0, nrows=256, nheads=8, seed=si.MASTER_SEED):
-    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, outliers=outliers, seed=seed)
-    o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=causal, rope_base=base)
+_INPUT_CACHE = {}
+
+
+def _sampled(B, Hq, Hkv, S, D, causal, base, outliers=0.0, nrows=256, nheads=8, seed=si.MASTER_SEED, window_k=None):
+    key = (B, Hq, Hkv, S, D, outliers, seed)
+    if key not in _INPUT_CACHE:  # the long-context workload is generated once for its three window settings
+        _INPUT_CACHE.clear()
+        _INPUT_CACHE[key] = si.make_qkv(B, Hq, Hkv, S, D, outliers=outliers, seed=seed)
+    q, k, v = _INPUT_CACHE[key]
+    o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=causal, rope_base=base, window_k=window_k)
     attn.attn_check()
     rows = si.sample_rows(seed, S, nrows)
     heads = si.sample_heads(seed, B, Hq, Hkv, nheads)
     rb = np.repeat([b for b, _ in heads], len(rows))
     rh = np.repeat([h for _, h in heads], len(rows))
     ri = np.tile(rows, len(heads))
-    o_ref, lse_ref = oracle.attn_rows(q, k, v, rb, rh, ri, causal=causal, rope_base=base)
+    o_ref, lse_ref = oracle.attn_rows(q, k, v, rb, rh, ri, causal=causal, rope_base=base, window_k=window_k)
     idx_b = torch.from_numpy(rb).long().cuda()
     idx_h = torch.from_numpy(rh).long().cuda()
     idx_i = torch.from_numpy(ri).long().cuda()
@@ -128,3 +135,36 @@ def test_late_large_score_rescales_running_max(base):
     attn.attn_check()
     o_ref, lse_ref = oracle.attn_full(q, k, v, causal=True, rope_base=base)
     _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "late large score")
+
+
+WINDOW_SMALL = [
+    # B, Hq, Hkv, S, D, rope_base, k
+    (1, 2, 2, 640, 128, 10000.0, 0.05),   # heavy pruning: whole channel groups skipped, many boundary pairs
+    (1, 4, 2, 700, 128, 100.0, 0.3),      # GQA pairs, small base: every tile has boundary pairs
+    (1, 2, 1, 300, 64, 500.0, 1.0),       # D = 64, ragged
+    (2, 4, 4, 1024, 128, 10000.0, 1.0),   # MHA pairs of query tiles (the two stages drop different pairs)
+    (1, 2, 2, 400, 128, 10000.0, 1e-9),   # W_r = 0: only the diagonal keeps its terms (all groups dropped)
+    (1, 2, 2, 256, 128, 500000.0, 4.0),   # window barely bites
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,base,k", WINDOW_SMALL)
+def test_window_small_all_rows(B, Hq, Hkv, S, D, base, k):
+    q, k_, v = si.make_qkv(B, Hq, Hkv, S, D, seed=202 + S)
+    o, lse = attn.attn_fwd(_dev(q), _dev(k_), _dev(v), causal=True, rope_base=base, window_k=k)
+    attn.attn_check()
+    o_ref, lse_ref = oracle.attn_full(q, k_, v, causal=True, rope_base=base, window_k=k)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"window k={k} S={S} D={D}")
+    # the window must change the result where it prunes (not silently ignored)
+    o_off, _ = oracle.attn_full(q, k_, v, causal=True, rope_base=base)
+    if k < 1.0:
+        assert np.abs(o_off - o_ref).max() > 5e-2
+
+
+def _sampled_window(k):
+    return _sampled(1, 32, 8, 131072, 128, True, 500000.0, nrows=128, window_k=k)
+
+
+@pytest.mark.parametrize("k", [1.0, 4.0, None])
+def test_window_s131072_sampled(k):
+    _sampled_window(k)

@@ -61,16 +61,20 @@ def workload_config(name, w):
 
 # --------------------------------------------------------------------- CPU oracle timing
 def time_oracle(q, k, v, w, budget_s, seed=si.MASTER_SEED):
-    """Time the float64 oracle on a bounded sample of query rows; returns (TFLOP/s, seconds, sample, threads)."""
+    """Time the float64 oracle on a bounded sample of query rows; returns (TFLOP/s, seconds, sample, threads).
+
+    Samples grow (more seeded rows, then further seeded sets of 8 heads) until
+    about budget_s seconds of oracle time have been spent.
+    """
     import oracle
     B, Hq, Hkv, S = w["B"], w["Hq"], w["Hkv"], w["S"]
-    heads = si.sample_heads(seed, B, Hq, Hkv, 8)
     nrows = 4
-    spent = 0.0
     total_flops = 0.0
     total_time = 0.0
     rows_done = 0
-    while True:
+    head_sets = 0
+    while total_time < budget_s:
+        heads = si.sample_heads(seed + 97 * head_sets, B, Hq, Hkv, 8)
         rows = si.sample_rows(seed + nrows, S, nrows)
         rb = np.repeat([b for b, _ in heads], len(rows))
         rh = np.repeat([h for _, h in heads], len(rows))
@@ -83,11 +87,11 @@ def time_oracle(q, k, v, w, budget_s, seed=si.MASTER_SEED):
         total_flops += float(np.sum(4.0 * w["D"] * keys))
         total_time += dt
         rows_done += len(ri)
-        spent += dt
-        if spent >= budget_s or nrows >= S:
-            break
-        nrows = min(S, max(nrows * 2, int(nrows * min(8.0, 0.5 * budget_s / max(dt, 1e-3)))))
-    sample = (f"{rows_done} query rows of {len(heads)} seeded (batch, head) pairs, useful work "
+        if nrows >= S:
+            head_sets += 1  # every row of these heads done: continue with other heads
+        else:
+            nrows = min(S, max(nrows * 2, int(nrows * min(8.0, 0.5 * budget_s / max(dt, 1e-3)))))
+    sample = (f"{rows_done} query rows over {head_sets + 1} seeded sets of 8 (batch, head) pairs, useful work "
               f"4*D*(keys) per row, {total_time:.1f} s")
     return total_flops / total_time / 1e12, total_time, sample, oracle.threads()
 

@@ -86,18 +86,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // {64, 1, 128, 1} = 128 rows of one head and 64 channels, 128-byte swizzle.
 // Rows past S read as zero.
 bool encode_bshd(CUtensorMap* m, const void* base, int B, int S, int H, int D, int box_inner = 64,
-                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B, int box_rows = 128) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
                                    static_cast<cuuint64_t>(S) * H * D * 2};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, 128, 1};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t elem[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, elem,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Q, K, V loads (128-row boxes) and the O store (32-row boxes: one warp's rows).
+bool encode_operands(FwdParams* prm, const void* q, const void* k, const void* v, void* o, int B, int S, int Hq,
+                     int Hkv, int D) {
+    return encode_bshd(&prm->tm_q, q, B, S, Hq, D) && encode_bshd(&prm->tm_k, k, B, S, Hkv, D) &&
+           encode_bshd(&prm->tm_v, v, B, S, Hkv, D) &&
+           encode_bshd(&prm->tm_o, o, B, S, Hq, D, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32);
 }
 
 int probe_device(int dev) {
@@ -191,7 +199,7 @@ int launch(const FwdParams& prm, int grid, cudaStream_t stream, DevInfo& di) {
     constexpr unsigned bit = 1u << ((WINDOW ? 8 : 0) | (D == 128 ? 4 : 0) | (CAUSAL ? 2 : 0) | (ROPE ? 1 : 0));
     auto kern = attn::attn_fwd_kernel<D, CAUSAL, ROPE, WINDOW>;
     // At least 120 KB so that only one CTA fits on an SM: each CTA takes all 512 TMEM columns.
-    using Layout = attn::SmemLayout<D, attn::k_stages<WINDOW>()>;
+    using Layout = attn::SmemLayout<D, WINDOW>;
     constexpr int smem = static_cast<int>(Layout::kAlloc) > 120 * 1024 ? static_cast<int>(Layout::kAlloc) : 120 * 1024;
     cudaError_t e;
     if (!(di.configured & bit)) {
@@ -243,8 +251,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
         sched = *se;
         prm.status = g_dev[dev].status;
     }
-    if (!encode_bshd(&prm.tm_q, q, B, S, Hq, D) || !encode_bshd(&prm.tm_k, k, B, S, Hkv, D) ||
-        !encode_bshd(&prm.tm_v, v, B, S, Hkv, D) ||
+    if (!encode_operands(&prm, q, k, v, o, B, S, Hq, Hkv, D) ||
         (window && !encode_bshd(&prm.tm_k16, k, B, S, Hkv, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)))
         return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
     {
@@ -369,8 +376,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     }
 
     FwdParams prm;
-    if (!encode_bshd(&prm.tm_q, q, B, S, Hq, D) || !encode_bshd(&prm.tm_k, k, B, S, Hkv, D) ||
-        !encode_bshd(&prm.tm_v, v, B, S, Hkv, D))
+    if (!encode_operands(&prm, q, k, v, o, B, S, Hq, Hkv, D))
         return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
     prm.o = static_cast<__nv_bfloat16*>(o);
     prm.lse = lse;

@@ -78,6 +78,7 @@ struct FwdParams {
     CUtensorMap tm_k;  // [B][S][Hkv][D]
     CUtensorMap tm_v;
     CUtensorMap tm_k16; // K again, box {16, 1, 128, 1}, 32-byte swizzle (windowed variant: one 16-channel group per load)
+    CUtensorMap tm_o;   // O [B][S][Hq][D] bf16, box {64, 1, 32, 1}, 128B swizzle: one warp's rows of one 64-channel block
     __nv_bfloat16* o;   // [B][S][Hq][D]
     float* lse;         // [B][Hq][S] or null
     const float2* rope; // RoPE factor tables (see RopeGeom), null when RoPE is off
@@ -110,13 +111,24 @@ enum : int {
     NUM_BARS = BAR_DRAIN + 1
 };
 
-template <int D, int KS>
+// Output staging for the TMA-store epilogue: per stage, one [32 rows][128 B]
+// block (64 channels, 128-byte swizzle) per warp of the softmax warpgroup.
+// The windowed variant's third K stage leaves no room for it; it stores O
+// with plain per-row stores.
+template <bool WINDOW>
+__host__ __device__ constexpr bool epi_tma() { return !WINDOW; }
+constexpr uint32_t kEpiWarpBytes = 32u * 128u;
+constexpr uint32_t kEpiStageBytes = 4u * kEpiWarpBytes;
+
+template <int D, bool WINDOW>
 struct SmemLayout {
+    static constexpr int KS = k_stages<WINDOW>();
     static constexpr uint32_t kTileBytes = 128u * D * 2u;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kK = kQ + 2 * kTileBytes;
     static constexpr uint32_t kV = kK + KS * kTileBytes;
-    static constexpr uint32_t kBars = kV + kVStages * kTileBytes;
+    static constexpr uint32_t kO = kV + kVStages * kTileBytes;  // 1024-byte aligned (tiles are multiples of 16 KB)
+    static constexpr uint32_t kBars = kO + (epi_tma<WINDOW>() ? 2 * kEpiStageBytes : 0u);
     static constexpr uint32_t kMisc = kBars + 8 * NUM_BARS;
     static constexpr uint32_t kBytes = kMisc + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -188,7 +200,7 @@ template <int D, bool WINDOW>
 __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, int t_begin, int t_end,
                               const WaitCtl& ctl) {
     constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, kKStages>;
+    using L = SmemLayout<D, WINDOW>;
     int kit = 0, vit = 0;
     int qit[2] = {0, 0};
     for (int ti = t_begin; ti < t_end; ++ti) {
@@ -363,7 +375,7 @@ template <int D, bool WINDOW>
 __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_t bar0, int t_begin, int t_end,
                           const WaitCtl& ctl, int t) {
     constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, kKStages>;
+    using L = SmemLayout<D, WINDOW>;
     RopeConsts k;
     rope_load_consts<D>(p, t, k);
     int kit = 0;
@@ -409,7 +421,7 @@ template <int D, bool ROPE, bool WINDOW>
 __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, uint32_t tmem, int t_begin,
                          int t_end, const WaitCtl& ctl) {
     constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, kKStages>;
+    using L = SmemLayout<D, WINDOW>;
     // QK^T: A = Q tile, B = K tile, both K-major; fp16 after rotation, bf16 otherwise.
     constexpr uint32_t kIdescQK = umma_idesc_f16(ROPE ? 0u : 1u, 0u, kBlockM, kBlockN);
     // PV: A = P (bf16, TMEM), B = V tile [keys][D] with D contiguous: MN-major.
@@ -506,24 +518,21 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                         }
                     }
                     tc_commit(bar_at(bar0, BAR_S_FULL + s));
-                    if (!WINDOW && n == 0) {
-                        tc_commit(bar_at(bar0, BAR_Q_EMPTY + s));
-                        ++qit[s];
-                    }
+                    if (!WINDOW && n == 0) ++qit[s];  // Q_s is released by its softmax once S_s(0) has landed
                 }
             }
             if (!ok) break;
-            if (do_s) {
-                if (!WINDOW) tc_commit(bar_at(bar0, BAR_K_EMPTY + ks));
-                ++kit;
-            }
+            // Without the window the K/V slots are released by the softmax (see
+            // softmax_loop): each commit here would take a slot of the tensor
+            // core's short instruction queue between two groups of MMAs.
+            if (do_s) ++kit;
             if (WINDOW && do_pv) {
                 // windowed: the softmax reads K(n+1) until it hands over P(n+1), which the PVs above waited for
                 tc_commit(bar_at(bar0, BAR_K_EMPTY + krel % kKStages));
                 ++krel;
             }
             if (do_pv) {
-                tc_commit(bar_at(bar0, BAR_V_EMPTY + vs));
+                if (WINDOW) tc_commit(bar_at(bar0, BAR_V_EMPTY + vs));
                 ++vit;
             }
         }
@@ -548,12 +557,31 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-// Masked row maximum of 64 raw scores: keys at or past `limit` are ignored.
+// Streams the 128 columns of this thread's row of a tile from TMEM in
+// 32-column chunks: the load of chunk k + 1 is in flight while f(chunk k, its
+// first column) runs.
+template <typename F>
+__device__ __forceinline__ void tmem_stream_128(uint32_t taddr, F&& f) {
+    uint32_t a[32], b[32];
+    tmem_load_32(taddr, a);
+    tmem_load_32_async(taddr + 32, b);
+    f(a, 0);
+    tmem_wait_ld_32(b);
+    tmem_load_32_async(taddr + 64, a);
+    f(b, 32);
+    tmem_wait_ld_32(a);
+    tmem_load_32_async(taddr + 96, b);
+    f(a, 64);
+    tmem_wait_ld_32(b);
+    f(b, 96);
+}
+
+// Masked row maximum of 32 raw scores: keys at or past `limit` are ignored.
 template <bool MASKED>
-__device__ __forceinline__ float row_max64(const uint32_t (&r)[64], int col0, int limit, float mx) {
+__device__ __forceinline__ float row_max32(const uint32_t (&r)[32], int col0, int limit, float mx) {
     float m0 = mx, m1 = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) {
+    for (int j = 0; j < 32; j += 4) {
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -588,13 +616,9 @@ __device__ __forceinline__ void exp_pack32(const uint32_t (&r)[32], int col0, in
 
 template <bool MASKED>
 __device__ __forceinline__ float tile_row_max(uint32_t taddr, int limit) {
+    static_assert(kBlockN == 128, "the TMEM stream covers 128 columns");
     float mx = -INFINITY;
-#pragma unroll
-    for (int cc = 0; cc < kBlockN; cc += 64) {
-        uint32_t r[64];
-        tmem_load_64(taddr + cc, r);
-        mx = row_max64<MASKED>(r, cc, limit, mx);
-    }
+    tmem_stream_128(taddr, [&](const uint32_t (&r)[32], int cc) { mx = row_max32<MASKED>(r, cc, limit, mx); });
     return mx;
 }
 
@@ -602,14 +626,12 @@ template <bool MASKED>
 __device__ __forceinline__ float tile_exp_to_p(uint32_t taddr, int limit, float c, float mc) {
     const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
     uint64_t sum2 = f2_pack(0.f, 0.f);
-#pragma unroll
-    for (int cc = 0; cc < kBlockN; cc += 32) {
-        uint32_t r[32];
-        tmem_load_32(taddr + cc, r);
+    // P of keys cc.. goes to columns cc/2..: never a column whose S is still to be read
+    tmem_stream_128(taddr, [&](const uint32_t (&r)[32], int cc) {
         uint32_t pk[16];
         exp_pack32<MASKED>(r, cc, limit, c2, nmc2, sum2, pk);
         tmem_store_16(taddr + cc / 2, pk);
-    }
+    });
     float s0, s1;
     f2_unpack(sum2, s0, s1);
     return s0 + s1;
@@ -670,10 +692,10 @@ __device__ __noinline__ void window_correct(uint32_t tS, const uint8_t* qtile, c
 // code measurably costs instruction-cache capacity).  Per-stage fields of the
 // unit are picked with selects so nothing is indexed at run time.
 template <int D, bool CAUSAL, bool WINDOW>
-__device__ void softmax_role(const FwdParams& p, int stage, uint8_t* smg, uint32_t bar0, uint32_t tmem, int t_begin,
+__device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32_t bar0, uint32_t tmem, int t_begin,
                              int t_end, const WaitCtl& ctl, int t) {
     constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, kKStages>;
+    using L = SmemLayout<D, WINDOW>;
     int kit = 0;  // K tiles seen by the unit loop (which K stage holds tile n), windowed variant
     const uint32_t lane_base = static_cast<uint32_t>(t & ~31);  // this warp's TMEM lane quarter
     const uint32_t trow = tmem + (lane_base << 16);
@@ -689,6 +711,10 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint8_t* smg, uint32
         kit += u.nmax + 1;
         const bool valid = stage ? u.valid[1] : u.valid[0];
         if (!valid) continue;
+        // The stage that visits every K/V tile of the unit releases the K/V
+        // slots: stage 1 when present (its first tile is the unit's first, and
+        // its products are issued after stage 0's), else stage 0.
+        const bool releaser = stage == 1 || !u.valid[1];
         const int nhi = stage ? u.nhi[1] : u.nhi[0];
         const int head = stage ? u.h[1] : u.h[0];
         const int row = (stage ? u.row0[1] : u.row0[0]) + t;
@@ -700,6 +726,15 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint8_t* smg, uint32
                 return;
             ++sit;
             tc_fence_after();
+            if (!WINDOW && n == 0 && t == 0)  // the unit's last product reading Q_s has landed
+                mbar_arrive(bar_at(bar0, BAR_Q_EMPTY + stage));
+            if (!WINDOW && releaser && t == 0) {
+                // S_s(n) landed, and the issue order puts it after every other
+                // product that reads K(n) or V(n+1): both slots are free again
+                const int it = kit_unit + u.nmax - n;
+                mbar_arrive(bar_at(bar0, BAR_K_EMPTY + it % kKStages));
+                if (n + 1 <= u.nmax) mbar_arrive(bar_at(bar0, BAR_V_EMPTY + (it - 1) % kVStages));
+            }
             if (WINDOW) {
                 // boundary pairs: kept for the tile by the MMA, dropped beyond W_r for some of its cells
                 const int z = window_tile<D>(p, u, n).z;
@@ -759,34 +794,88 @@ __device__ void softmax_role(const FwdParams& p, int stage, uint8_t* smg, uint32
             return;
         ++oit;
         tc_fence_after();
+        if (!WINDOW && releaser && t == 0)  // the unit's last products (PV of tile 0) are done: V(0) is free
+            mbar_arrive(bar_at(bar0, BAR_V_EMPTY + (kit_unit + u.nmax) % kVStages));
         const float inv_l = 1.0f / l;
         const uint64_t il2 = f2_pack(inv_l, inv_l);
         const bool row_ok = row < p.S;
-        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.S + row) * p.Hq + head) * D;
-#pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-            uint32_t r[32];
-            tmem_load_32(tO + cc, r);
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float x0, x1;
-                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il2), x0, x1);
-                pk[j] = pack_bf16x2(x0, x1);
-            }
-            if (row_ok) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + cc);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-            }
-        }
         if (row_ok && p.lse != nullptr)
             p.lse[(static_cast<size_t>(u.b) * p.Hq + head) * p.S + row] =
                 (m_used * c + log2f(l)) * 0.69314718055994531f;
-        tc_fence_before();
-        mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
+        if constexpr (epi_tma<WINDOW>()) {
+            // Each warp stages its 32 rows one 64-channel block at a time (128-byte
+            // swizzle: chunk c of row r at chunk c ^ (r & 7)) and stores the block
+            // with one TMA copy; rows past S are clipped by the copy.  O_s is
+            // handed back as soon as its last columns are in registers.
+            const int lane = t & 31, wq = t >> 5;
+            uint8_t* blk = smg + L::kO + static_cast<uint32_t>(stage) * kEpiStageBytes + static_cast<uint32_t>(wq) * kEpiWarpBytes;
+            const int row0 = (stage ? u.row0[1] : u.row0[0]) + 32 * wq;
+#pragma unroll
+            for (int sub = 0; sub < D / 64; ++sub) {
+                if (lane == 0) bulk_wait_group_read<0>();  // the previous copy has read the block
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // 32 channels (four 16-byte chunks) at a time
+                    uint32_t r[32];
+                    tmem_load_32(tO + 64 * sub + 32 * h, r);
+                    if (sub == D / 64 - 1 && h == 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float x0, x1;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il2), x0, x1);
+                        pk[j] = pack_bf16x2(x0, x1);
+                    }
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int c8 = 4 * h + c4;
+                        *reinterpret_cast<uint4*>(blk + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&p.tm_o, smem_addr(blk), 64 * sub, head, row0, u.b);
+                    bulk_commit_group();
+                }
+            }
+        } else {
+            __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.S + row) * p.Hq + head) * D;
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t r[32];
+                tmem_load_32(tO + cc, r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float x0, x1;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il2), x0, x1);
+                    pk[j] = pack_bf16x2(x0, x1);
+                }
+                if (row_ok) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
+        }
     }
+}
+
+// The softmax warpgroup's role; before the warps leave, each warp's output
+// copies must have finished (their source is this CTA's shared memory).
+template <int D, bool CAUSAL, bool WINDOW>
+__device__ void softmax_role(const FwdParams& p, int stage, uint8_t* smg, uint32_t bar0, uint32_t tmem, int t_begin,
+                             int t_end, const WaitCtl& ctl, int t) {
+    softmax_loop<D, CAUSAL, WINDOW>(p, stage, smg, bar0, tmem, t_begin, t_end, ctl, t);
+    if (epi_tma<WINDOW>() && (t & 31) == 0) bulk_wait_group<0>();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -794,7 +883,7 @@ template <int D, bool CAUSAL, bool ROPE, bool WINDOW>
 __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     static_assert(!WINDOW || (CAUSAL && ROPE), "the window is defined with RoPE and causal masking");
     constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, kKStages>;
+    using L = SmemLayout<D, WINDOW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sm = smem_addr(smg);

@@ -643,22 +643,24 @@ __device__ __forceinline__ float tile_exp_to_p(uint32_t taddr, int limit, float 
 // subtracted from those cells of this thread's row, from the same fp16
 // operands the tensor cores multiplied (the products are exact in fp32, so
 // only the summation order differs).  rel = row - first key of the tile.
-// Called by the whole warp; most tiles have no boundary pair.
+// Per 32-key chunk and pair, the K values of the chunk's keys are read first
+// (broadcast loads: every row needs the same ones), then applied with selects.
+// W_r ascends in r and the dropped keys of a row are those with j < rel - W_r,
+// so once no row of the warp drops a key, later pairs and later chunks drop
+// none either.  Called by the whole warp; most tiles have no boundary pair.
 template <int D>
 __device__ __noinline__ void window_correct(uint32_t tS, const uint8_t* qtile, const uint8_t* ktile,
                                             const FwdParams& p, int r_begin, int r_end, int rel, int t) {
     constexpr int kHalf = D / 2;
-    const int lane = t & 31;
 #pragma unroll 1
     for (int cc = 0; cc < kBlockN; cc += 32) {
+        if (!__any_sync(0xffffffffu, rel - p.win[r_begin] - cc > 0)) break;
         uint32_t r[32];
         tmem_load_32(tS + cc, r);
 #pragma unroll 1
         for (int pr = r_begin; pr < r_end; ++pr) {
-            const int lim = rel - p.win[pr];  // keys j < lim of this tile are beyond the window for this row
-            // rows of a warp are consecutive, so lim grows by one per lane: decide per warp
-            if (!__any_sync(0xffffffffu, lim > cc)) continue;
-            const bool full = __all_sync(0xffffffffu, lim >= cc + 32);
+            const int lim = rel - p.win[pr] - cc;  // this row drops the pair for keys cc + j, j < lim
+            if (!__any_sync(0xffffffffu, lim > 0)) break;
             const int dx = pr, dy = pr + kHalf;  // channels of the pair
             const float qx = f16_at(qtile + (dx / 64) * kSubTileBytes + t * 128 + ((((dx % 64) / 8) ^ (t & 7)) << 4) +
                                     (dx % 8) * 2);
@@ -669,22 +671,23 @@ __device__ __noinline__ void window_correct(uint32_t tS, const uint8_t* qtile, c
             // so the swizzle bit of key cc + j is (j >> 2) & 1
             const uint8_t* kx = ktile + (dx / 16) * 4096 + (dx % 8) * 2 + cc * 32;
             const uint8_t* ky = ktile + (dy / 16) * 4096 + (dy % 8) * 2 + cc * 32;
-            const int hx0 = ((dx % 16) / 8) << 4, hx1 = hx0 ^ 16;
-            const int hy0 = ((dy % 16) / 8) << 4, hy1 = hy0 ^ 16;
-            const int jmax = full ? 32 : lim - cc;  // this row's dropped keys in the chunk
+            const int hx = ((dx % 16) / 8) << 4, hy = ((dy % 16) / 8) << 4;
+            float kxv[32], kyv[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                if (full || j < jmax) {
-                    const bool sw = (j >> 2) & 1;
-                    const float term = fmaf(qx, f16_at(kx + j * 32 + (sw ? hx1 : hx0)),
-                                            qy * f16_at(ky + j * 32 + (sw ? hy1 : hy0)));
-                    r[j] = __float_as_uint(__uint_as_float(r[j]) - term);
-                }
+                const int sw = ((j >> 2) & 1) << 4;
+                kxv[j] = f16_at(kx + j * 32 + (hx ^ sw));
+                kyv[j] = f16_at(ky + j * 32 + (hy ^ sw));
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float v = __uint_as_float(r[j]);
+                const float term = fmaf(qx, kxv[j], qy * kyv[j]);
+                r[j] = __float_as_uint(j < lim ? v - term : v);
             }
         }
         tmem_store_32(tS + cc, r);
     }
-    (void)lane;
     tmem_store_wait();
 }
 

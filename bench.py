@@ -91,7 +91,7 @@ def time_oracle(q, k, v, w, budget_s, seed=si.MASTER_SEED):
             head_sets += 1  # every row of these heads done: continue with other heads
         else:
             nrows = min(S, max(nrows * 2, int(nrows * min(8.0, 0.5 * budget_s / max(dt, 1e-3)))))
-    sample = (f"{rows_done} query rows over {head_sets + 1} seeded sets of 8 (batch, head) pairs, useful work "
+    sample = (f"{rows_done} query rows over {head_sets + 1} seeded sets of {len(heads)} (batch, head) pairs, useful work "
               f"4*D*(keys) per row, {total_time:.1f} s")
     return total_flops / total_time / 1e12, total_time, sample, oracle.threads()
 
@@ -240,6 +240,15 @@ def run_ours(args, w, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         tf, secs, sample, threads = time_oracle(q_h, k_h, v_h, w, args.cpu_budget)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+        # the same oracle on one host core, a shorter sample
+        import oracle
+        oracle.set_threads(1)
+        try:
+            tf1, _, sample1, _ = time_oracle(q_h, k_h, v_h, w, max(1.0, args.cpu_budget / 4))
+        finally:
+            oracle.set_threads(threads)
+        cpu["value_1core"] = tf1
+        cpu["sample_1core"] = sample1
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

@@ -151,6 +151,28 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# --------------------------------------------------------------------- replicas (N > 1)
+# Every (batch, head) of the forward is independent: with N ranks each rank
+# runs the whole workload on its own seeded batch (weak scaling, no
+# collective on the data path); only the timings meet, as a max over ranks.
+def replica_seed(rank):
+    return si.MASTER_SEED + rank
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of a list of floats over all ranks (identity without a process group)."""
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(world, flops_per_rank, ms):
+    """Units all ranks processed / the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------- our arm
 def run_ours(args, w, rank, world, local_rank):
     import torch
@@ -165,7 +187,7 @@ def run_ours(args, w, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     B, Hq, Hkv, S, D = w["B"], w["Hq"], w["Hkv"], w["S"], w["D"]
-    seed = si.MASTER_SEED + rank  # every rank its own independent batch
+    seed = replica_seed(rank)  # every rank its own independent batch
     q_h, k_h, v_h = si.make_qkv(B, Hq, Hkv, S, D, outliers=w["outliers"], seed=seed)
     to_pinned = lambda a: torch.from_numpy(a).view(torch.bfloat16).pin_memory()
     q_p, k_p, v_p = to_pinned(q_h), to_pinned(k_h), to_pinned(v_h)
@@ -231,10 +253,7 @@ def run_ours(args, w, rank, world, local_rank):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    times = torch.tensor([elapsed_ms, e2e_ms, float(np.mean(launch_ms))], device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms, launch_avg_ms = times.tolist()
+    elapsed_ms, e2e_ms, launch_avg_ms = max_over_ranks([elapsed_ms, e2e_ms, float(np.mean(launch_ms))], dist, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -257,7 +276,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     flops = useful_flops(w)
     ms_per_step = elapsed_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms_per_step)
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (launch_avg_ms * 1e-3) / 1e12
@@ -289,7 +308,7 @@ def run_ours(args, w, rank, world, local_rank):
                      "kernel": "attn_fwd_kernel", "peak_source": f"bf16_tflops ({peak_kind}, burst)",
                      "algorithmic": "2*B*Hq*S^2*D useful causal FLOPs per launch"},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": args.steps,

@@ -45,7 +45,7 @@ def _rank_main(rank, world, port, out):
 @pytest.mark.timeout(180)
 def test_two_gloo_ranks_max_timing_and_independent_batches():
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
         res = dict(out)

@@ -47,6 +47,8 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert _call(lib, Hq=6, Hkv=4) == E["ATTN_ERR_SHAPE"]
     assert _call(lib, Hq=2, Hkv=4) == E["ATTN_ERR_SHAPE"]
     assert _call(lib, Hq=256, Hkv=1) == E["ATTN_ERR_SHAPE"]
+    assert _call(lib, B=65536) == E["ATTN_ERR_SHAPE"]  # the batch index is 16 bits of a work unit
+    assert _call(lib, S=(1 << 22) + 1) == E["ATTN_ERR_SHAPE"]
     assert _call(lib, q=24) == E["ATTN_ERR_ALIGN"]
     assert _call(lib, lse=18) == E["ATTN_ERR_ALIGN"]
     assert _call(lib, causal=2) == E["ATTN_ERR_UNSUPPORTED"]

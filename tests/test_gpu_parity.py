@@ -56,6 +56,24 @@ SMALL = [
 ]
 
 
+EDGE = [
+    # B, Hq, Hkv, S, D, causal, rope_base
+    (1, 255, 5, 130, 64, True, 10000.0),   # query heads at the API limit, GQA groups of 51
+    (1, 16, 1, 257, 128, True, 500000.0),  # every query head on one KV head
+    (300, 1, 1, 129, 64, True, None),      # many more work units than CTAs
+    (65535, 1, 1, 1, 64, True, 10000.0),   # batch at the API limit, one key per row
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base", EDGE)
+def test_limits_all_rows(B, Hq, Hkv, S, D, causal, base):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=303 + S)
+    o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=causal, rope_base=base)
+    attn.attn_check()
+    o_ref, lse_ref = oracle.attn_full(q, k, v, causal=causal, rope_base=base)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"B={B} Hq={Hq} S={S}")
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base", SMALL)
 def test_small_all_rows(B, Hq, Hkv, S, D, causal, base):
     q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=101 + S)

@@ -16,7 +16,7 @@ import numpy as np
 
 from ._build import INCLUDE, LIB, build
 
-__all__ = ["attn_fwd", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -50,6 +50,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
         lib.attn_fwd_noalloc.restype = i
         lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
+        lib.attn_fwd_host.restype = i
+        lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i
@@ -120,6 +122,41 @@ def attn_fwd(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=None, 
                           _stream_handle(stream, q.device))
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_host(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=None, window_k=None,
+                  return_lse: bool = True, device=None):
+    """The forward on BSHD bf16 CPU tensors (pinned for overlapped copies), on `device` (default: current).
+
+    Returns (o, lse) as CPU tensors; the call returns when both are filled.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (t.device.type == "cpu" and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CPU tensor (BSHD)")
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, S, Hkv, D] with q's B, S and D")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, pin_memory=q.is_pinned())
+    for name, t, shape, dt in (("o", o, (B, S, Hq, D), torch.bfloat16), ("lse", lse, (B, Hq, S), torch.float32)):
+        if t is not None and not (t.device.type == "cpu" and t.dtype == dt and t.is_contiguous()
+                                  and tuple(t.shape) == shape):
+            raise ValueError(f"{name} must be a contiguous CPU tensor {shape} of {dt}")
+    lib = load_library()
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr() if lse is not None else None,
+                               B, Hq, Hkv, S, D, int(bool(causal)),
+                               float(rope_base) if rope_base else 0.0,
+                               float(window_k) if window_k else 0.0)
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_host")
     return o, lse
 
 

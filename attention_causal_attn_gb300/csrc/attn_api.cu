@@ -216,21 +216,33 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                        int S, int D, int causal, double rope_base, double window_k, void* stream) {
+namespace {
+// Argument checks shared by the entry points (pointer alignment aside).
+int check_args(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int S, int D,
+               int causal, double rope_base, double window_k) {
     if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_NULL;
     if (B < 1 || B > 65535 || S < 1 || S > kMaxS || Hq < 1 || Hq > 255 || Hkv < 1 || Hkv > Hq || Hq % Hkv != 0)
         return ATTN_ERR_SHAPE;
     if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
-        return ATTN_ERR_ALIGN;
     if (causal != 0 && causal != 1) return ATTN_ERR_UNSUPPORTED;
     const bool rope = rope_base > 0.0 && std::isfinite(rope_base);
     if (rope_base > 0.0 && !std::isfinite(rope_base)) return ATTN_ERR_UNSUPPORTED;
     const bool window = window_k > 0.0 && !std::isinf(window_k);
     if (window && !(rope && causal)) return ATTN_ERR_UNSUPPORTED;
     if (std::isnan(window_k) || std::isnan(rope_base)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int S, int D, int causal, double rope_base, double window_k, void* stream) {
+    int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, window_k);
+    if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+                           (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+        arc = ATTN_ERR_ALIGN;
+    if (arc != ATTN_OK) return arc;
+    const bool rope = rope_base > 0.0 && std::isfinite(rope_base);
+    const bool window = window_k > 0.0 && !std::isinf(window_k);
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_NO_DEVICE;
@@ -313,17 +325,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                                 int Hkv, int S, int D, int causal, double rope_base, double window_k, void* stream) {
-    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_NULL;
-    if (B < 1 || B > 65535 || S < 1 || S > kMaxS || Hq < 1 || Hq > 255 || Hkv < 1 || Hkv > Hq || Hq % Hkv != 0)
-        return ATTN_ERR_SHAPE;
-    if (D != 64 && D != 128) return ATTN_ERR_SHAPE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
-        return ATTN_ERR_ALIGN;
-    if (causal != 0 && causal != 1) return ATTN_ERR_UNSUPPORTED;
-    if (std::isnan(window_k) || std::isnan(rope_base)) return ATTN_ERR_UNSUPPORTED;
-    if (rope_base > 0.0 && !std::isfinite(rope_base)) return ATTN_ERR_UNSUPPORTED;
-    const bool rope = rope_base > 0.0;
+    int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, window_k);
+    if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+                           (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+        arc = ATTN_ERR_ALIGN;
+    if (arc != ATTN_OK) return arc;
+    const bool rope = rope_base > 0.0 && std::isfinite(rope_base);
     const bool window = window_k > 0.0 && !std::isinf(window_k);
     if (window) return ATTN_ERR_UNSUPPORTED;
 
@@ -401,6 +408,154 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     return rope ? launch<64, false, true>(prm, grid, st, di) : launch<64, false, false>(prm, grid, st, di);
 }
 
+// ---------------------------------------------------------------------------
+// Host-buffer forward: chunks of (batch, KV heads) go host -> device, through
+// attn_fwd and back while the neighbouring chunks move, on three streams.
+namespace {
+struct HostPipe {
+    size_t slot_bytes = 0;   // one staging slot: q, k, v, o, lse of the largest chunk
+    uint8_t* buf = nullptr;  // two slots
+    cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+    bool ready = false;
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+// `rows` rows of `width` bytes, `pitch` bytes apart in host memory, to or from a
+// packed device buffer (one plain copy when the rows are contiguous).
+cudaError_t copy_rows(void* dst_packed, const void* src, size_t width, size_t pitch, int rows, cudaMemcpyKind kind,
+                      cudaStream_t st) {
+    if (width == pitch) return cudaMemcpyAsync(dst_packed, src, width * rows, kind, st);
+    return cudaMemcpy2DAsync(dst_packed, width, src, pitch, width, rows, kind, st);
+}
+cudaError_t copy_rows_out(void* dst, size_t pitch, const void* src_packed, size_t width, int rows, cudaStream_t st) {
+    if (width == pitch) return cudaMemcpyAsync(dst, src_packed, width * rows, cudaMemcpyDeviceToHost, st);
+    return cudaMemcpy2DAsync(dst, pitch, src_packed, width, width, rows, cudaMemcpyDeviceToHost, st);
+}
+
+int pipe_setup(HostPipe& hp, size_t slot_bytes) {
+    cudaError_t e;
+    if (!hp.ready) {
+        if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.s_comp, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail("cudaStreamCreate(host pipeline)", e);
+        for (int i = 0; i < 2; ++i)
+            if ((e = cudaEventCreateWithFlags(&hp.ev_in[i], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.ev_comp[i], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.ev_out[i], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail("cudaEventCreate(host pipeline)", e);
+        hp.ready = true;
+    }
+    if (hp.slot_bytes < slot_bytes) {
+        if (hp.buf != nullptr) {
+            cudaFree(hp.buf);
+            hp.buf = nullptr;
+            hp.slot_bytes = 0;
+        }
+        if ((e = cudaMalloc(&hp.buf, 2 * slot_bytes)) != cudaSuccess)
+            return cuda_fail("cudaMalloc(host pipeline staging)", e, ATTN_ERR_OOM);
+        hp.slot_bytes = slot_bytes;
+    }
+    return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                             int Hkv, int S, int D, int causal, double rope_base, double window_k) {
+    const int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, window_k);
+    if (arc != ATTN_OK) return arc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_NO_DEVICE;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);  // released before the pipeline's lock (lock order)
+        if (int rc0 = probe_device(dev); rc0 != ATTN_OK) return rc0;
+        sms = g_dev[dev].sms;
+    }
+    // Chunks: one batch element and a group of KV heads (with their query heads).
+    // Up to eight per call, so that the copies of the first chunk in and the last
+    // one out (which nothing overlaps) stay short, but each chunk keeps at least
+    // two work units per SM for the kernel's load balance.
+    const int G = Hq / Hkv;
+    const long long nqt = (S + 127) / 128;
+    auto units_for = [&](int hkv) {
+        return G >= 2 ? static_cast<long long>(hkv) * nqt * ((G + 1) / 2) : static_cast<long long>(hkv) * ((nqt + 1) / 2);
+    };
+    int groups = std::max(1, std::min(Hkv, (8 + B - 1) / B));
+    while (groups > 1 && units_for(Hkv / groups) < 2LL * sms) --groups;
+    const int gmax = (Hkv + groups - 1) / groups;
+    const size_t e2 = 2;  // bytes per bf16 element
+    const size_t q_bytes = align256(static_cast<size_t>(S) * gmax * G * D * e2);
+    const size_t kv_bytes = align256(static_cast<size_t>(S) * gmax * D * e2);
+    const size_t lse_bytes = align256(static_cast<size_t>(gmax) * G * S * sizeof(float));
+    const size_t slot_bytes = 2 * q_bytes + 2 * kv_bytes + lse_bytes;  // q, o, k, v, lse
+
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe& hp = g_pipe[dev];
+    int rc = pipe_setup(hp, slot_bytes);
+    if (rc != ATTN_OK) return rc;
+    const char* hq = static_cast<const char*>(q);
+    const char* hk = static_cast<const char*>(k);
+    const char* hv = static_cast<const char*>(v);
+    char* ho = static_cast<char*>(o);
+    cudaError_t e = cudaSuccess;
+    int c = 0;
+    for (int b = 0; b < B && rc == ATTN_OK; ++b) {
+        for (int gi = 0; gi < groups && rc == ATTN_OK; ++gi, ++c) {
+            const int g0 = Hkv * gi / groups, g1 = Hkv * (gi + 1) / groups;
+            if (g1 <= g0) continue;
+            const int hkv = g1 - g0, hq_n = hkv * G, h0 = g0 * G;
+            const int slot = c & 1;
+            uint8_t* base = hp.buf + slot * hp.slot_bytes;
+            uint8_t* dq = base;
+            uint8_t* dout = base + q_bytes;
+            uint8_t* dk = base + 2 * q_bytes;
+            uint8_t* dv = dk + kv_bytes;
+            float* dl = reinterpret_cast<float*>(dv + kv_bytes);
+            const size_t row_q = static_cast<size_t>(Hq) * D * e2, row_kv = static_cast<size_t>(Hkv) * D * e2;
+            const size_t w_q = static_cast<size_t>(hq_n) * D * e2, w_kv = static_cast<size_t>(hkv) * D * e2;
+            const size_t off_q = (static_cast<size_t>(b) * S * Hq + h0) * D * e2;
+            const size_t off_kv = (static_cast<size_t>(b) * S * Hkv + g0) * D * e2;
+            // in: the slot's previous chunk must have been read by its kernel
+            if (c >= 2 && (e = cudaStreamWaitEvent(hp.s_in, hp.ev_comp[slot], 0)) != cudaSuccess) break;
+            if ((e = copy_rows(dq, hq + off_q, w_q, row_q, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
+                (e = copy_rows(dk, hk + off_kv, w_kv, row_kv, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
+                (e = copy_rows(dv, hv + off_kv, w_kv, row_kv, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
+                (e = cudaEventRecord(hp.ev_in[slot], hp.s_in)) != cudaSuccess)
+                break;
+            // compute: after the inputs landed and the slot's previous outputs left
+            if ((e = cudaStreamWaitEvent(hp.s_comp, hp.ev_in[slot], 0)) != cudaSuccess) break;
+            if (c >= 2 && (e = cudaStreamWaitEvent(hp.s_comp, hp.ev_out[slot], 0)) != cudaSuccess) break;
+            rc = attn_fwd(dq, dk, dv, dout, lse != nullptr ? dl : nullptr, 1, hq_n, hkv, S, D, causal, rope_base,
+                          window_k, hp.s_comp);
+            if (rc != ATTN_OK) break;
+            if ((e = cudaEventRecord(hp.ev_comp[slot], hp.s_comp)) != cudaSuccess) break;
+            // out
+            if ((e = cudaStreamWaitEvent(hp.s_out, hp.ev_comp[slot], 0)) != cudaSuccess ||
+                (e = copy_rows_out(ho + off_q, row_q, dout, w_q, S, hp.s_out)) != cudaSuccess)
+                break;
+            if (lse != nullptr &&
+                (e = cudaMemcpyAsync(lse + (static_cast<size_t>(b) * Hq + h0) * S, dl,
+                                     static_cast<size_t>(hq_n) * S * sizeof(float), cudaMemcpyDeviceToHost,
+                                     hp.s_out)) != cudaSuccess)
+                break;
+            if ((e = cudaEventRecord(hp.ev_out[slot], hp.s_out)) != cudaSuccess) break;
+        }
+    }
+    // the call returns once every chunk is back in host memory
+    const cudaError_t e_sync = cudaStreamSynchronize(hp.s_out);
+    cudaStreamSynchronize(hp.s_comp);
+    cudaStreamSynchronize(hp.s_in);
+    if (rc != ATTN_OK) return rc;
+    if (e != cudaSuccess) return cuda_fail("host pipeline", e);
+    if (e_sync != cudaSuccess) return cuda_fail("cudaStreamSynchronize(host pipeline)", e_sync);
+    return attn_check(hp.s_comp);
+}
+
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
                                  float* cos_out, float* sin_out, int* win_out) {
     if (S < 1 || S > kMaxS || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
@@ -454,9 +609,28 @@ extern "C" const char* attn_error_string(int status) {
 }
 
 extern "C" void attn_release_cache(void) {
-    std::lock_guard<std::mutex> lock(g_mu);
     int cur = 0;
     const bool have = cudaGetDevice(&cur) == cudaSuccess;
+    // lock order: the host pipeline's lock before the table caches' (attn_fwd_host calls attn_fwd)
+    std::lock_guard<std::mutex> plock(g_pipe_mu);
+    {
+        for (int d = 0; d < kMaxDevices; ++d) {
+            HostPipe& hp = g_pipe[d];
+            if (!hp.ready) continue;
+            cudaSetDevice(d);
+            cudaFree(hp.buf);
+            for (int i = 0; i < 2; ++i) {
+                cudaEventDestroy(hp.ev_in[i]);
+                cudaEventDestroy(hp.ev_comp[i]);
+                cudaEventDestroy(hp.ev_out[i]);
+            }
+            cudaStreamDestroy(hp.s_in);
+            cudaStreamDestroy(hp.s_comp);
+            cudaStreamDestroy(hp.s_out);
+            hp = HostPipe();
+        }
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
     for (auto& e : g_rope) {
         cudaSetDevice(e.dev);
         cudaFree(e.table);

@@ -112,6 +112,36 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float
                      double rope_base, double window_k, void* stream);
 
 /*
+ * attn_fwd_host — attn_fwd with host buffers: copies in, computes, copies out.
+ *
+ * The source pages have no counterpart to this entry point.  It is for callers
+ * whose tensors live in host memory (a CPU-resident KV store, an offload
+ * path, an end-to-end measurement): it overlaps the host-device transfers
+ * with the compute instead of leaving them to run one after another.
+ *
+ *   q, k, v, o, lse  HOST pointers with the layouts of attn_fwd (lse may be
+ *                    NULL).  Page-locked memory (cudaHostAlloc / pinned torch
+ *                    tensors) lets the copies run asynchronously; pageable
+ *                    memory works, with the copies then staged by the driver.
+ *   other arguments  as attn_fwd; the device is the current one.
+ *
+ * The work is cut into chunks of one batch element and a group of KV heads
+ * (with their query heads): about four chunks per call.  Two device staging
+ * slots cycle through three library-owned streams: the next chunk's Q/K/V go
+ * host-to-device while the current chunk runs through attn_fwd and the
+ * previous chunk's O/LSE go device-to-host.  Each head's arithmetic is that
+ * of attn_fwd, so the results are bitwise those of attn_fwd on the same data.
+ *   - Synchronous: returns after every output is in host memory, with
+ *     ATTN_ERR_TIMEOUT if a bounded in-kernel wait ran out (as attn_check).
+ *   - The library keeps the staging slots (2 x the largest chunk's Q, K, V,
+ *     O and LSE) and the streams until attn_release_cache().
+ *   - One call at a time per device (calls are serialised by a lock).
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int Hq, int Hkv, int S, int D, int causal,
+                  double rope_base, double window_k);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

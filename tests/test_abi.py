@@ -18,8 +18,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
-    assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_build_tables", "attn_check", "attn_error_string",
-                          "attn_release_cache"}
+    assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_build_tables", "attn_check",
+                          "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for n in names:
@@ -55,6 +55,19 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert _call(lib, base=0.0, win=1.0) == E["ATTN_ERR_UNSUPPORTED"]  # window needs RoPE
     assert _call(lib, causal=0, win=1.0) == E["ATTN_ERR_UNSUPPORTED"]  # window needs causal
     assert _call(lib, base=math.inf) == E["ATTN_ERR_UNSUPPORTED"]
+
+
+def test_host_entry_checks_arguments_before_any_device_call(lib):
+    E = attn.ATTN_STATUS
+    call = lambda **kw: lib.attn_fwd_host(*(kw.get(n, 16) for n in ("q", "k", "v", "o")), None,
+                                           kw.get("B", 1), kw.get("Hq", 2), kw.get("Hkv", 2), kw.get("S", 128),
+                                           kw.get("D", 64), kw.get("causal", 1), kw.get("base", 1e4), kw.get("win", 0.0))
+    assert call(q=0) == E["ATTN_ERR_NULL"]
+    assert call(B=0) == E["ATTN_ERR_SHAPE"]
+    assert call(Hq=6, Hkv=4) == E["ATTN_ERR_SHAPE"]
+    assert call(D=80) == E["ATTN_ERR_SHAPE"]
+    assert call(causal=3) == E["ATTN_ERR_UNSUPPORTED"]
+    assert call(causal=0, win=2.0) == E["ATTN_ERR_UNSUPPORTED"]
 
 
 def test_rope_tables_are_float64_cos_sin_rounded(lib):

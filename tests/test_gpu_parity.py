@@ -186,3 +186,40 @@ def _sampled_window(k):
 @pytest.mark.parametrize("k", [1.0, 4.0, None])
 def test_window_s131072_sampled(k):
     _sampled_window(k)
+
+
+HOST = [
+    # B, Hq, Hkv, S, D, causal, rope_base, window_k
+    (4, 4, 4, 300, 128, True, 10000.0, None),    # one chunk per batch element
+    (2, 8, 4, 257, 64, True, None, None),        # two KV-head groups per batch element
+    (1, 8, 8, 1030, 128, True, 500000.0, None),  # four head groups, ragged
+    (1, 4, 2, 700, 128, True, 10000.0, 1.0),     # window
+    (3, 2, 1, 129, 64, False, None, None),       # full attention, one KV head
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base,wk", HOST)
+def test_host_entry_matches_device_entry_bitwise(B, Hq, Hkv, S, D, causal, base, wk):
+    """attn_fwd_host cuts the work into (batch, KV-head group) chunks; each head's
+    arithmetic is unchanged, so O and LSE equal attn_fwd's bit for bit."""
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=404 + S)
+    qp, kp, vp = (torch.from_numpy(x).view(torch.bfloat16).pin_memory() for x in (q, k, v))
+    o_h, l_h = attn.attn_fwd_host(qp, kp, vp, causal=causal, rope_base=base, window_k=wk)
+    o_d, l_d = attn.attn_fwd(qp.cuda(), kp.cuda(), vp.cuda(), causal=causal, rope_base=base, window_k=wk)
+    attn.attn_check()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())
+    if S <= 300:
+        o_ref, lse_ref = oracle.attn_full(q, k, v, causal=causal, rope_base=base, window_k=wk)
+        _check(o_h.float().numpy(), l_h.numpy(), o_ref, lse_ref, "host entry")
+
+
+def test_host_entry_pageable_memory_and_no_lse():
+    B, Hq, Hkv, S, D = 2, 4, 2, 333, 128
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=505)
+    qt, kt, vt = (torch.from_numpy(x).view(torch.bfloat16) for x in (q, k, v))  # not pinned
+    o_h, none = attn.attn_fwd_host(qt, kt, vt, causal=True, rope_base=10000.0, return_lse=False)
+    assert none is None
+    o_d, _ = attn.attn_fwd(qt.cuda(), kt.cuda(), vt.cuda(), causal=True, rope_base=10000.0)
+    attn.attn_check()
+    assert torch.equal(o_h, o_d.cpu())

@@ -48,6 +48,8 @@ def _load():
             lib.oracle_pruned_terms.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double]
             lib.oracle_window_widths.restype = None
             lib.oracle_window_widths.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, f64p]
+            lib.oracle_rope_rotate.restype = None
+            lib.oracle_rope_rotate.argtypes = [u16p] + [ctypes.c_int] * 4 + [ctypes.c_double, f64p]
             lib.oracle_threads.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -102,6 +104,15 @@ def attn_full(q, k, v, **kw):
     bb, hh, ii = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(S), indexing="ij")
     o, lse = attn_rows(q, k, v, bb.ravel(), hh.ravel(), ii.ravel(), **kw)
     return o.reshape(B, Hq, S, D).transpose(0, 2, 1, 3).copy(), lse.reshape(B, Hq, S)
+
+
+def rope_rotate(x, rope_base: float) -> np.ndarray:
+    """Every row of x (uint16 bf16 bits [B, S, H, D]) rotated at its position s, float64 [B, S, H, D]."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    B, S, H, D = x.shape
+    out = np.empty(x.shape, dtype=np.float64)
+    _load().oracle_rope_rotate(_ptr(x, ctypes.c_uint16), B, S, H, D, float(rope_base), _ptr(out, ctypes.c_double))
+    return out
 
 
 def pruned_terms(S: int, D: int, rope_base: float, window_k: float) -> int:

@@ -86,6 +86,19 @@ static void rope_rotate(const uint16_t* x, int D, const double* theta, double po
     }
 }
 
+/* Every row (b, s, h) of a BSHD bf16 tensor rotated at its position s, in
+   float64 ("AttnFuse", sec. 4.1: pair r with r + D/2, theta_r = base^(-2r/D)). */
+void oracle_rope_rotate(const uint16_t* x, int B, int S, int H, int D, double rope_base, double* out) {
+    double theta[512];
+    rope_thetas(D, rope_base, theta);
+    const long long rows = (long long)B * S * H;
+#pragma omp parallel for schedule(static)
+    for (long long i = 0; i < rows; ++i) {
+        const long long s = (i / H) % S;
+        rope_rotate(x + i * D, D, theta, (double)s, 1, out + i * D);
+    }
+}
+
 int oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

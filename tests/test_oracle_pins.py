@@ -86,6 +86,21 @@ def test_rope_equals_complex_rotation_then_sdpa(causal, base):
     np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-11)
 
 
+@pytest.mark.parametrize("base", [10000.0, 500000.0, 37.0])
+def test_standalone_rotation_equals_complex_rotation(base):
+    """The oracle's standalone rotation (used to check the pre-rotation kernel)
+    against multiplication by e^{i p theta_r}: a different formulation."""
+    x = si.bshd_bf16(7, 1, 2, 33, 3, 64)
+    got = oracle.rope_rotate(x, base)
+    np.testing.assert_allclose(got, _rope_complex(x, base), rtol=0, atol=1e-12)
+    # a rotation keeps each pair's length, and position 0 is the identity
+    xf = _f64(x)
+    h = 32
+    np.testing.assert_allclose(got[..., :h] ** 2 + got[..., h:] ** 2, xf[..., :h] ** 2 + xf[..., h:] ** 2,
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(got[:, 0], xf[:, 0])
+
+
 def _brute_relative(q, k, v, base, window_k):
     """Per-cell brute force from unrotated q, k and the relative angle only.
 

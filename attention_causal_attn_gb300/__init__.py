@@ -16,7 +16,7 @@ import numpy as np
 
 from ._build import INCLUDE, LIB, build
 
-__all__ = ["attn_fwd", "attn_fwd_host", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -52,6 +52,10 @@ def load_library(path: str | None = None):
         lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
         lib.attn_fwd_host.restype = i
         lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d]
+        lib.attn_rope_rotate.restype = i
+        lib.attn_rope_rotate.argtypes = [vp, vp, i, i, i, i, d, vp]
+        lib.attn_fwd_rotated.restype = i
+        lib.attn_fwd_rotated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i
@@ -122,6 +126,46 @@ def attn_fwd(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=None, 
                           _stream_handle(stream, q.device))
     if rc != 0:
         raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_rope_rotate(x, rope_base: float, out=None, stream=None):
+    """RoPE of a whole BSHD bf16 CUDA tensor in one pass; returns the rotated fp16 tensor."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 4 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous 4-D bf16 CUDA tensor (BSHD)")
+    B, S, H, D = x.shape
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    lib = load_library()
+    with torch.cuda.device(x.device):
+        rc = lib.attn_rope_rotate(x.data_ptr(), out.data_ptr(), B, S, H, D, float(rope_base),
+                                  _stream_handle(stream, x.device))
+    if rc != 0:
+        raise AttnError(rc, "attn_rope_rotate")
+    return out
+
+
+def attn_fwd_rotated(q_rot, k_rot, v, o=None, lse=None, *, causal: bool = True, return_lse: bool = True,
+                     stream=None):
+    """The forward on fp16 Q and K rotated by attn_rope_rotate (v bf16); returns (o, lse)."""
+    import torch
+    for name, t, dt in (("q_rot", q_rot, torch.float16), ("k_rot", k_rot, torch.float16), ("v", v, torch.bfloat16)):
+        if not (t.is_cuda and t.dtype == dt and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D {dt} CUDA tensor (BSHD)")
+    B, S, Hq, D = q_rot.shape
+    Hkv = k_rot.shape[2]
+    if o is None:
+        o = torch.empty(q_rot.shape, dtype=torch.bfloat16, device=q_rot.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q_rot.device)
+    lib = load_library()
+    with torch.cuda.device(q_rot.device):
+        rc = lib.attn_fwd_rotated(q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None, B, Hq, Hkv, S, D, int(bool(causal)),
+                                  _stream_handle(stream, q_rot.device))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_rotated")
     return o, lse
 
 

@@ -15,6 +15,7 @@
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "rope_rotate_kernel.cuh"
 #include "host_tables.h"
 
 // Raised (bitwise OR) by a CTA whose bounded wait ran out; read and cleared by attn_check().
@@ -234,8 +235,10 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
 }
 }  // namespace
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                        int S, int D, int causal, double rope_base, double window_k, void* stream) {
+namespace {
+// The forward; qk_f16: Q and K hold fp16 values (already rotated) rather than bf16.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S, int D,
+             int causal, double rope_base, double window_k, void* stream, bool qk_f16) {
     int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, window_k);
     if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
                            (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
@@ -282,6 +285,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     prm.S = S;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     prm.wait_limit_ns = kWaitLimitNs;
+    prm.qk_f16 = qk_f16 ? 1 : 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     DevInfo& di = g_dev[dev];
@@ -294,6 +298,79 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     }
     if (causal) return rope ? launch<64, true, true>(prm, grid, st, di) : launch<64, true, false>(prm, grid, st, di);
     return rope ? launch<64, false, true>(prm, grid, st, di) : launch<64, false, false>(prm, grid, st, di);
+}
+}  // namespace
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int S, int D, int causal, double rope_base, double window_k, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base, window_k, stream, false);
+}
+
+extern "C" int attn_fwd_rotated(const void* q_rot, const void* k_rot, const void* v, void* o, float* lse, int B,
+                                int Hq, int Hkv, int S, int D, int causal, void* stream) {
+    return fwd_impl(q_rot, k_rot, v, o, lse, B, Hq, Hkv, S, D, causal, 0.0, 0.0, stream, true);
+}
+
+// ---------------------------------------------------------------------------
+// Pre-rotation pass ("AttnFuse", sec. 5.3, The Rotation Calculus).
+namespace {
+struct SplitEntry {
+    int dev, S, D;
+    double base;
+    float2* table;
+};
+std::vector<SplitEntry> g_split;
+
+int get_split(int dev, int S, int D, double base, float2** out) {
+    for (auto& e : g_split)
+        if (e.dev == dev && e.S == S && e.D == D && e.base == base) {
+            *out = e.table;
+            return ATTN_OK;
+        }
+    const std::vector<float> host = attn_host::rope_split_tables(S, D, base);
+    float2* d = nullptr;
+    cudaError_t e;
+    if ((e = cudaMalloc(&d, host.size() * sizeof(float))) != cudaSuccess)
+        return cuda_fail("cudaMalloc(rotation tables)", e, ATTN_ERR_OOM);
+    if ((e = cudaMemcpy(d, host.data(), host.size() * sizeof(float), cudaMemcpyHostToDevice)) != cudaSuccess) {
+        cudaFree(d);
+        return cuda_fail("cudaMemcpy(rotation tables)", e);
+    }
+    g_split.push_back({dev, S, D, base, d});
+    *out = d;
+    return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_rope_rotate(const void* x, void* y, int B, int S, int H, int D, double rope_base, void* stream) {
+    if (x == nullptr || y == nullptr) return ATTN_ERR_NULL;
+    if (B < 1 || B > 65535 || S < 1 || S > kMaxS || H < 1 || H > 255 || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
+    if (!(rope_base > 0.0) || !std::isfinite(rope_base)) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y)) return ATTN_ERR_ALIGN;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+    float2* tab = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int rc = probe_device(dev);
+        if (rc != ATTN_OK) return rc;
+        if ((rc = get_split(dev, S, D, rope_base, &tab)) != ATTN_OK) return rc;
+    }
+    const long long rows = static_cast<long long>(B) * S * H;
+    const long long threads = rows * (D / 16);
+    const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+    const float2* base_tab = tab;
+    const float2* row_tab = tab + static_cast<size_t>((S + 127) / 128) * (D / 2);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (D == 128)
+        attn::rope_rotate_kernel<128><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), static_cast<uint4*>(y),
+                                                              base_tab, row_tab, rows, S, H);
+    else
+        attn::rope_rotate_kernel<64><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), static_cast<uint4*>(y),
+                                                             base_tab, row_tab, rows, S, H);
+    cudaError_t e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("rotation kernel launch", e);
+    return ATTN_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -397,6 +474,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     prm.Hkv = Hkv;
     prm.S = S;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    prm.qk_f16 = 0;
     prm.wait_limit_ns = kWaitLimitNs;
     DevInfo& di = g_dev[dev];
     const int grid = na.ctas;
@@ -644,6 +722,11 @@ extern "C" void attn_release_cache(void) {
         cudaSetDevice(e.dev);
         cudaFree(e.table);
     }
+    for (auto& e : g_split) {
+        cudaSetDevice(e.dev);
+        cudaFree(e.table);
+    }
+    g_split.clear();
     g_rope.clear();
     g_sched.clear();
     g_win.clear();

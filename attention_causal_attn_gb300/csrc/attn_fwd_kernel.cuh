@@ -89,6 +89,7 @@ struct FwdParams {
     float scale_log2;   // log2(e) / sqrt(D)
     unsigned long long wait_limit_ns;
     int win[64];        // W_r = floor(k * 2*pi / theta_r), ascending in r (windowed variant)
+    int qk_f16;         // without in-kernel RoPE: Q and K hold fp16 (already rotated) rather than bf16
     const short2* wtab; // windowed variant, per tile distance: (first pair kept at the tile's smallest distance,
                         // first pair kept at its largest), see window_tile
 };
@@ -423,7 +424,7 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
     constexpr int kKStages = k_stages<WINDOW>();
     using L = SmemLayout<D, WINDOW>;
     // QK^T: A = Q tile, B = K tile, both K-major; fp16 after rotation, bf16 otherwise.
-    constexpr uint32_t kIdescQK = umma_idesc_f16(ROPE ? 0u : 1u, 0u, kBlockM, kBlockN);
+    const uint32_t kIdescQK = umma_idesc_f16((ROPE || p.qk_f16) ? 0u : 1u, 0u, kBlockM, kBlockN);
     // PV: A = P (bf16, TMEM), B = V tile [keys][D] with D contiguous: MN-major.
     constexpr uint32_t kIdescPV = umma_idesc_f16(1u, 1u, kBlockM, D);
     const int kbar_ready = ROPE ? BAR_K_ROT : BAR_K_FULL;

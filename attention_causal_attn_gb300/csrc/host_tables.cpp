@@ -63,6 +63,23 @@ std::vector<float> rope_factor_table(int S, int D, double base) {
     return t;
 }
 
+std::vector<float> rope_split_tables(int S, int D, double base) {
+    const int half = D / 2;
+    const int ntiles = (S + kTile - 1) / kTile;
+    const std::vector<double> th = rope_thetas(D, base);
+    std::vector<float> t(static_cast<size_t>(ntiles + kTile) * half * 2);
+    size_t o = 0;
+    auto put = [&](double pos) {
+        for (int r = 0; r < half; ++r) {
+            t[o++] = static_cast<float>(std::cos(pos * th[r]));
+            t[o++] = static_cast<float>(std::sin(pos * th[r]));
+        }
+    };
+    for (int m = 0; m < ntiles; ++m) put(static_cast<double>(m) * kTile);
+    for (int rr = 0; rr < kTile; ++rr) put(static_cast<double>(rr));
+    return t;
+}
+
 std::vector<int32_t> window_widths(int D, double base, double k) {
     std::vector<int32_t> w(static_cast<size_t>(D / 2), INT32_MAX);
     if (!(k > 0.0) || std::isinf(k)) return w;

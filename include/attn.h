@@ -142,6 +142,40 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
                   double rope_base, double window_k);
 
 /*
+ * attn_rope_rotate — RoPE applied to a whole BSHD tensor in one pass.
+ *
+ * The pre-rotation side of "AttnFuse: A Composable DSL for Compiling
+ * Attentions to Fused GPU Kernels", sec. 5.3 The Rotation Calculus: rotate Q
+ * and K once, in a memory-bound sweep, then run the attention without in-loop
+ * rotation (attn_fwd_rotated), against attn_fwd's rotation of K tiles inside
+ * the loop each time a query tile visits them.  Same pairing, angles and
+ * positions (0..S-1) as attn_fwd.
+ *   x          bf16 device tensor [B][S][H][D], 16-byte aligned.
+ *   y          fp16 device output of the same shape (must not overlap x): the
+ *              rotation in fp32, rounded to fp16 as attn_fwd rounds its rotated
+ *              operands.  Angles are products of two factors computed in
+ *              float64 (tile base and row offset), accurate to a few fp32 ulps.
+ *   B, S, H, D as attn_fwd (H for the tensor's own heads); rope_base > 0.
+ *   stream     cudaStream_t (as void*); asynchronous.
+ * The first call for a (device, S, D, rope_base) builds and caches a factor
+ * table of (S/128 + 128) * D * 4 bytes.
+ */
+int attn_rope_rotate(const void* x, void* y, int B, int S, int H, int D, double rope_base, void* stream);
+
+/*
+ * attn_fwd_rotated — the forward on Q and K rotated beforehand.
+ *
+ *   q_rot, k_rot   fp16 device tensors, BSHD, as written by attn_rope_rotate.
+ *   v, o, lse, B, Hq, Hkv, S, D, causal, stream   as attn_fwd.
+ * Runs attn_fwd's kernel without in-loop rotation, with QK^T on the fp16
+ * operands (the window is not available here).  With attn_rope_rotate on Q
+ * and K first, the result equals attn_fwd's with RoPE up to the rounding of
+ * the angles (both paths round the rotated values to fp16).
+ */
+int attn_fwd_rotated(const void* q_rot, const void* k_rot, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int S, int D, int causal, void* stream);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

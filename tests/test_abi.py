@@ -18,8 +18,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
-    assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_build_tables", "attn_check",
-                          "attn_error_string", "attn_release_cache"}
+    assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated",
+                          "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for n in names:
@@ -68,6 +68,16 @@ def test_host_entry_checks_arguments_before_any_device_call(lib):
     assert call(D=80) == E["ATTN_ERR_SHAPE"]
     assert call(causal=3) == E["ATTN_ERR_UNSUPPORTED"]
     assert call(causal=0, win=2.0) == E["ATTN_ERR_UNSUPPORTED"]
+
+
+def test_rotation_entries_check_arguments_on_the_host(lib):
+    E = attn.ATTN_STATUS
+    assert lib.attn_rope_rotate(None, 16, 1, 128, 2, 128, 1e4, None) == E["ATTN_ERR_NULL"]
+    assert lib.attn_rope_rotate(16, 16, 1, 128, 2, 96, 1e4, None) == E["ATTN_ERR_SHAPE"]
+    assert lib.attn_rope_rotate(16, 16, 1, 128, 2, 128, 0.0, None) == E["ATTN_ERR_UNSUPPORTED"]
+    assert lib.attn_rope_rotate(24, 16, 1, 128, 2, 128, 1e4, None) == E["ATTN_ERR_ALIGN"]
+    assert lib.attn_fwd_rotated(16, 16, 16, 16, None, 1, 6, 4, 128, 128, 1, None) == E["ATTN_ERR_SHAPE"]
+    assert lib.attn_fwd_rotated(16, 16, 16, 16, None, 1, 2, 2, 128, 128, 2, None) == E["ATTN_ERR_UNSUPPORTED"]
 
 
 def test_rope_tables_are_float64_cos_sin_rounded(lib):

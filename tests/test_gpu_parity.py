@@ -223,3 +223,41 @@ def test_host_entry_pageable_memory_and_no_lse():
     o_d, _ = attn.attn_fwd(qt.cuda(), kt.cuda(), vt.cuda(), causal=True, rope_base=10000.0)
     attn.attn_check()
     assert torch.equal(o_h, o_d.cpu())
+
+
+@pytest.mark.parametrize("B,S,H,D,base", [(2, 1000, 3, 128, 10000.0), (1, 257, 4, 64, 500000.0),
+                                          (1, 131072, 1, 128, 500000.0)])
+def test_pre_rotation_matches_oracle_rotation(B, S, H, D, base):
+    """attn_rope_rotate (fp16 out) against the float64 rotation, within fp16 rounding
+    plus a few fp32 ulps of angle error; long rows check the angles at large positions."""
+    x = si.bshd_bf16(606, 1, B, S, H, D)
+    y = attn.attn_rope_rotate(_dev(x), base)
+    torch.cuda.synchronize()
+    ref = oracle.rope_rotate(x, base)
+    got = y.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    assert np.all(err <= 1e-3 * np.abs(ref) + 2e-4), f"max err {err.max():.3e}"
+
+
+PRE = [
+    # B, Hq, Hkv, S, D, causal, rope_base
+    (2, 4, 4, 384, 128, True, 10000.0),
+    (1, 4, 2, 300, 128, True, 500000.0),
+    (2, 3, 1, 257, 64, False, 10000.0),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base", PRE)
+def test_pre_rotated_forward_matches_oracle_and_fused(B, Hq, Hkv, S, D, causal, base):
+    """attn_rope_rotate on Q and K, then attn_fwd_rotated: the same attention as
+    the fused path ("AttnFuse", sec. 5.3: pre-rotation against fusion)."""
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=707 + S)
+    qd, kd, vd = _dev(q), _dev(k), _dev(v)
+    o, lse = attn.attn_fwd_rotated(attn.attn_rope_rotate(qd, base), attn.attn_rope_rotate(kd, base), vd,
+                                   causal=causal)
+    o_f, lse_f = attn.attn_fwd(qd, kd, vd, causal=causal, rope_base=base)
+    attn.attn_check()
+    o_ref, lse_ref = oracle.attn_full(q, k, v, causal=causal, rope_base=base)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "pre-rotated")
+    # both paths round the rotated operands to fp16; only the angles' last fp32 bits differ
+    assert (o.float() - o_f.float()).abs().max().item() <= 1e-2

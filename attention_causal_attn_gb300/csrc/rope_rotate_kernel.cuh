@@ -29,8 +29,9 @@ __global__ void __launch_bounds__(256) rope_rotate_kernel(const uint4* __restric
     const long long row = i / kChunks;
     const int c = static_cast<int>(i % kChunks);
     const int s = static_cast<int>((row / H) % S);
-    const float2* bf = base_tab + static_cast<size_t>(s / 128) * kHalf + 8 * c;
-    const float2* rf = row_tab + static_cast<size_t>(s % 128) * kHalf + 8 * c;
+    // (cos, sin) factors of pairs 8c..8c+7, two pairs per 16-byte load
+    const float4* bf = reinterpret_cast<const float4*>(base_tab + static_cast<size_t>(s / 128) * kHalf + 8 * c);
+    const float4* rf = reinterpret_cast<const float4*>(row_tab + static_cast<size_t>(s % 128) * kHalf + 8 * c);
     const uint4 lo = __ldg(x + row * (D / 8) + c);
     const uint4 hi = __ldg(x + row * (D / 8) + kChunks + c);
     const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
@@ -38,10 +39,12 @@ __global__ void __launch_bounds__(256) rope_rotate_kernel(const uint4* __restric
     uint32_t lo_out[4], hi_out[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+        const float4 f1v = __ldg(bf + q), f2v = __ldg(rf + q);
         float a[2], b[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const float2 f1 = __ldg(bf + 2 * q + e), f2 = __ldg(rf + 2 * q + e);
+            const float2 f1 = e ? make_float2(f1v.z, f1v.w) : make_float2(f1v.x, f1v.y);
+            const float2 f2 = e ? make_float2(f2v.z, f2v.w) : make_float2(f2v.x, f2v.y);
             const float cs = f1.x * f2.x - f1.y * f2.y;  // cos(A + B)
             const float sn = f1.y * f2.x + f1.x * f2.y;  // sin(A + B)
             const float xv = e ? bf16_hi(lw[q]) : bf16_lo(lw[q]);

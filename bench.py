@@ -198,9 +198,23 @@ def run_ours(args, w, rank, world, local_rank):
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     kw = dict(causal=w["causal"], rope_base=w["rope_base"], window_k=w["window_k"], stream=stream)
+    prerotate = args.rope_lowering == "prerotate"
+    launches_per_step = 3 if prerotate else 1
+    if prerotate:
+        # the other side of the Rotation Calculus: rotate Q and K in their own pass, then
+        # the attention without in-loop rotation (three launches per step)
+        if not w["rope_base"] or w["window_k"]:
+            raise SystemExit("--rope-lowering prerotate needs RoPE on and the window off")
+        q_rot = torch.empty(q.shape, dtype=torch.float16, device=dev)
+        k_rot = torch.empty(k.shape, dtype=torch.float16, device=dev)
 
-    def step():
-        attn.attn_fwd(q, k, v, o, lse, **kw)
+        def step():
+            attn.attn_rope_rotate(q, w["rope_base"], out=q_rot, stream=stream)
+            attn.attn_rope_rotate(k, w["rope_base"], out=k_rot, stream=stream)
+            attn.attn_fwd_rotated(q_rot, k_rot, v, o, lse, causal=w["causal"], stream=stream)
+    else:
+        def step():
+            attn.attn_fwd(q, k, v, o, lse, **kw)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -281,9 +295,12 @@ def run_ours(args, w, rank, world, local_rank):
     in_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
     out_bytes = o.numel() * 2 + lse.numel() * 4
     cfg = workload_config(args.workload, w)
+    cfg["rope_lowering"] = "pre-rotation pass + attention" if prerotate else "fused at load"
     cfg["l2"] = f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q/K/V per step vs 129 MB L2), no flush"
     cfg["timing"] = f"CUDA events on the launching stream, {args.steps} steps after {max(args.warmup, 3)} warm-up"
-    traffic = load_traffic(args.workload)
+    # the committed DRAM count belongs to the named workload at its own size, fused
+    same_shape = args.batch is None and args.seq is None and args.window_k is None and not prerotate
+    traffic = load_traffic(args.workload) if same_shape else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -303,13 +320,14 @@ def run_ours(args, w, rank, world, local_rank):
                         "peak_kind": peak_kind},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "attn_fwd_kernel", "peak_source": f"bf16_tflops ({peak_kind}, burst)",
+                     "kernel": ("step: 2 x rope_rotate_kernel + attn_fwd_kernel" if prerotate else "attn_fwd_kernel"),
+                     "peak_source": f"bf16_tflops ({peak_kind}, burst)",
                      "algorithmic": "2*B*Hq*S^2*D useful causal FLOPs per launch"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
-                "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": args.steps,
+                "ms_per_step": round(e2e_ms, 4), "entry": "attn_fwd_host (RoPE fused at load)"},
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
     }
     return line
@@ -382,6 +400,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
     ap.add_argument("--window-k", type=float, default=None, help="override the workload's window multiplier")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling captures)")
+    ap.add_argument("--seq", type=int, default=None, help="override the workload's sequence length")
+    ap.add_argument("--rope-lowering", default="fused", choices=["fused", "prerotate"],
+                    help="fused: RoPE at load (the specified path); prerotate: a rotation pass, then the attention")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle time for --impl reference")
@@ -394,6 +415,8 @@ def main():
         w["window_k"] = args.window_k if args.window_k > 0 else None
     if args.batch is not None:
         w["B"] = args.batch
+    if args.seq is not None:
+        w["S"] = args.seq
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

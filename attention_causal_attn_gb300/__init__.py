@@ -16,7 +16,7 @@ import numpy as np
 
 from ._build import INCLUDE, LIB, build
 
-__all__ = ["attn_fwd", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -56,6 +56,8 @@ def load_library(path: str | None = None):
         lib.attn_rope_rotate.argtypes = [vp, vp, i, i, i, i, d, vp]
         lib.attn_fwd_rotated.restype = i
         lib.attn_fwd_rotated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.attn_decode.restype = i
+        lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, d, d, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i
@@ -166,6 +168,32 @@ def attn_fwd_rotated(q_rot, k_rot, v, o=None, lse=None, *, causal: bool = True, 
                                   _stream_handle(stream, q_rot.device))
     if rc != 0:
         raise AttnError(rc, "attn_fwd_rotated")
+    return o, lse
+
+
+def attn_decode(q, k, v, o=None, lse=None, *, rope_base=None, window_k=None, return_lse: bool = True,
+                stream=None):
+    """One decode step: q [B, Hq, D] (position S-1) against caches k, v [B, S, Hkv, D]; returns (o, lse)."""
+    import torch
+    for name, t, nd in (("q", q, 3), ("k", k, 4), ("v", v, 4)):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == nd and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous {nd}-D bf16 CUDA tensor")
+    B, Hq, D = q.shape
+    S, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, S, Hkv, D] with q's B and D")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr() if lse is not None else None, B, Hq, Hkv, S, D,
+                             float(rope_base) if rope_base else 0.0, float(window_k) if window_k else 0.0,
+                             _stream_handle(stream, q.device))
+    if rc != 0:
+        raise AttnError(rc, "attn_decode")
     return o, lse
 
 

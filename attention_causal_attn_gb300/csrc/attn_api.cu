@@ -16,6 +16,7 @@
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
 #include "rope_rotate_kernel.cuh"
+#include "decode_kernel.cuh"
 #include "host_tables.h"
 
 // Raised (bitwise OR) by a CTA whose bounded wait ran out; read and cleared by attn_check().
@@ -315,19 +316,19 @@ extern "C" int attn_fwd_rotated(const void* q_rot, const void* k_rot, const void
 // Pre-rotation pass ("AttnFuse", sec. 5.3, The Rotation Calculus).
 namespace {
 struct SplitEntry {
-    int dev, S, D;
+    int dev, S, D, block;
     double base;
     float2* table;
 };
 std::vector<SplitEntry> g_split;
 
-int get_split(int dev, int S, int D, double base, float2** out) {
+int get_split(int dev, int S, int D, double base, int block, float2** out) {
     for (auto& e : g_split)
-        if (e.dev == dev && e.S == S && e.D == D && e.base == base) {
+        if (e.dev == dev && e.S == S && e.D == D && e.block == block && e.base == base) {
             *out = e.table;
             return ATTN_OK;
         }
-    const std::vector<float> host = attn_host::rope_split_tables(S, D, base);
+    const std::vector<float> host = attn_host::rope_split_tables(S, D, base, block);
     float2* d = nullptr;
     cudaError_t e;
     if ((e = cudaMalloc(&d, host.size() * sizeof(float))) != cudaSuccess)
@@ -336,7 +337,7 @@ int get_split(int dev, int S, int D, double base, float2** out) {
         cudaFree(d);
         return cuda_fail("cudaMemcpy(rotation tables)", e);
     }
-    g_split.push_back({dev, S, D, base, d});
+    g_split.push_back({dev, S, D, block, base, d});
     *out = d;
     return ATTN_OK;
 }
@@ -354,7 +355,7 @@ extern "C" int attn_rope_rotate(const void* x, void* y, int B, int S, int H, int
         std::lock_guard<std::mutex> lock(g_mu);
         int rc = probe_device(dev);
         if (rc != ATTN_OK) return rc;
-        if ((rc = get_split(dev, S, D, rope_base, &tab)) != ATTN_OK) return rc;
+        if ((rc = get_split(dev, S, D, rope_base, 128, &tab)) != ATTN_OK) return rc;
     }
     const long long rows = static_cast<long long>(B) * S * H;
     const long long threads = rows * (D / 16);
@@ -634,6 +635,143 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* 
     return attn_check(hp.s_comp);
 }
 
+// ---------------------------------------------------------------------------
+// Split-KV decode ("AttnFuse", sec. 4.2 Decode; "ATFlash", decode window).
+namespace {
+struct DecodeScratch {
+    size_t floats = 0;
+    float* buf = nullptr;
+};
+DecodeScratch g_dec[kMaxDevices];
+int g_dec_occ[kMaxDevices][2][3];  // resident split CTAs per SM, by [D == 128][variant], 0 = not yet queried
+
+using DecodeKernel = void (*)(attn::DecodeParams);
+
+template <int D>
+DecodeKernel decode_kernel(int variant) {  // 0: RoPE off, 1: RoPE, 2: RoPE + window
+    if (variant == 0) return attn::decode_split_kernel<D, false, false>;
+    if (variant == 1) return attn::decode_split_kernel<D, true, false>;
+    return attn::decode_split_kernel<D, true, true>;
+}
+
+// Opt the split kernel into its shared memory and read its residency (caller holds g_mu).
+int decode_occupancy(int dev, int D, int variant, int* occ) {
+    int& cached = g_dec_occ[dev][D == 128][variant];
+    if (cached == 0) {
+        const DecodeKernel kern = D == 128 ? decode_kernel<128>(variant) : decode_kernel<64>(variant);
+        const int smem = D == 128 ? attn::decode_smem_bytes<128>() : attn::decode_smem_bytes<64>();
+        cudaError_t e;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return cuda_fail("cudaFuncSetAttribute(decode)", e);
+        int n = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, attn::kDecThreads, smem)) != cudaSuccess)
+            return cuda_fail("cudaOccupancyMaxActiveBlocksPerMultiprocessor(decode)", e);
+        cached = std::max(1, n);
+    }
+    *occ = cached;
+    return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int S, int D, double rope_base, double window_k, void* stream) {
+    int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, 1, rope_base, window_k);
+    if (arc == ATTN_OK && Hq / Hkv > attn::kDecMaxGroup) arc = ATTN_ERR_UNSUPPORTED;
+    if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+                           (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+        arc = ATTN_ERR_ALIGN;
+    if (arc != ATTN_OK) return arc;
+    const bool rope = rope_base > 0.0 && std::isfinite(rope_base);
+    const bool window = window_k > 0.0 && !std::isinf(window_k);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+
+    // Splits are whole multiples of 128 keys (one 32-key tile per warp).  Among split counts up to
+    // about two waves of resident CTAs, take the one with the least estimated time, counted as
+    // waves x tiles per split.
+    const int tile = attn::kDecWarps * attn::kDecTile;
+    const int variant = !rope ? 0 : (window ? 2 : 1);
+    const int mtiles = (Hq / Hkv + attn::kDecHeads - 1) / attn::kDecHeads;
+    float2* tab = nullptr;
+    float* scratch = nullptr;
+    int nsplit = 1, split_len = S;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int rc = probe_device(dev);
+        if (rc != ATTN_OK) return rc;
+        if (rope && (rc = get_split(dev, S, D, rope_base, attn::kDecTile, &tab)) != ATTN_OK) return rc;
+        int occ = 1;
+        if ((rc = decode_occupancy(dev, D, variant, &occ)) != ATTN_OK) return rc;
+        const long long slots = static_cast<long long>(occ) * g_dev[dev].sms;
+        const long long units = static_cast<long long>(B) * Hkv * mtiles;
+        const int tiles = (S + tile - 1) / tile;
+        const long long cap = std::max(
+            1LL, std::min<long long>({static_cast<long long>(tiles), (2 * slots + units - 1) / units,
+                                      static_cast<long long>(attn::kDecMaxParts)}));
+        long long best = -1;
+        for (long long n = 1; n <= cap; ++n) {
+            const int per = static_cast<int>((tiles + n - 1) / n);  // tiles per split
+            const long long used = (tiles + per - 1) / per;         // splits actually made
+            const long long waves = (used * units + slots - 1) / slots;
+            const long long cost = waves * per;
+            if (best < 0 || cost < best) {
+                best = cost;
+                nsplit = static_cast<int>(used);
+                split_len = per * tile;
+            }
+        }
+        const size_t need = static_cast<size_t>(B) * Hq * nsplit * (D + 2);
+        DecodeScratch& ds = g_dec[dev];
+        if (ds.floats < need) {
+            if (ds.buf != nullptr) cudaFree(ds.buf);
+            ds.buf = nullptr;
+            ds.floats = 0;
+            cudaError_t e;
+            if ((e = cudaMalloc(&ds.buf, need * sizeof(float))) != cudaSuccess)
+                return cuda_fail("cudaMalloc(decode partials)", e, ATTN_ERR_OOM);
+            ds.floats = need;
+        }
+        scratch = ds.buf;
+    }
+    attn::DecodeParams dp;
+    dp.q = static_cast<const __nv_bfloat16*>(q);
+    dp.k = static_cast<const __nv_bfloat16*>(k);
+    dp.v = static_cast<const __nv_bfloat16*>(v);
+    dp.part_o = scratch;
+    dp.part_ml = scratch + static_cast<size_t>(B) * Hq * nsplit * D;
+    dp.rot_base = rope ? tab : nullptr;
+    dp.rot_row = rope ? tab + static_cast<size_t>((S + attn::kDecTile - 1) / attn::kDecTile) * (D / 2) : nullptr;
+    dp.B = B;
+    dp.Hq = Hq;
+    dp.Hkv = Hkv;
+    dp.S = S;
+    dp.nsplit = nsplit;
+    dp.split_len = split_len;
+    dp.mtiles = mtiles;
+    dp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    {
+        const std::vector<int32_t> w = attn_host::window_widths(D, rope ? rope_base : 10000.0, window ? window_k : 0.0);
+        for (int r = 0; r < 64; ++r) dp.win[r] = r < D / 2 ? w[r] : INT32_MAX;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const dim3 grid(static_cast<unsigned>(nsplit * mtiles), static_cast<unsigned>(B * Hkv));
+    if (D == 128)
+        decode_kernel<128>(variant)<<<grid, attn::kDecThreads, attn::decode_smem_bytes<128>(), st>>>(dp);
+    else
+        decode_kernel<64>(variant)<<<grid, attn::kDecThreads, attn::decode_smem_bytes<64>(), st>>>(dp);
+    cudaError_t e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("decode split kernel launch", e);
+    const unsigned rows = static_cast<unsigned>(B * Hq);
+    if (D == 128)
+        attn::decode_combine_kernel<128><<<rows, 128, 0, st>>>(dp.part_o, dp.part_ml, static_cast<__nv_bfloat16*>(o), lse,
+                                                             nsplit);
+    else
+        attn::decode_combine_kernel<64><<<rows, 128, 0, st>>>(dp.part_o, dp.part_ml, static_cast<__nv_bfloat16*>(o), lse,
+                                                            nsplit);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("decode combine kernel launch", e);
+    return ATTN_OK;
+}
+
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
                                  float* cos_out, float* sin_out, int* win_out) {
     if (S < 1 || S > kMaxS || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
@@ -725,6 +863,12 @@ extern "C" void attn_release_cache(void) {
     for (auto& e : g_split) {
         cudaSetDevice(e.dev);
         cudaFree(e.table);
+    }
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_dec[d].buf == nullptr) continue;
+        cudaSetDevice(d);
+        cudaFree(g_dec[d].buf);
+        g_dec[d] = DecodeScratch();
     }
     g_split.clear();
     g_rope.clear();

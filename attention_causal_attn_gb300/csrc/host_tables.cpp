@@ -63,11 +63,11 @@ std::vector<float> rope_factor_table(int S, int D, double base) {
     return t;
 }
 
-std::vector<float> rope_split_tables(int S, int D, double base) {
+std::vector<float> rope_split_tables(int S, int D, double base, int block) {
     const int half = D / 2;
-    const int ntiles = (S + kTile - 1) / kTile;
+    const int ntiles = (S + block - 1) / block;
     const std::vector<double> th = rope_thetas(D, base);
-    std::vector<float> t(static_cast<size_t>(ntiles + kTile) * half * 2);
+    std::vector<float> t(static_cast<size_t>(ntiles + block) * half * 2);
     size_t o = 0;
     auto put = [&](double pos) {
         for (int r = 0; r < half; ++r) {
@@ -75,8 +75,8 @@ std::vector<float> rope_split_tables(int S, int D, double base) {
             t[o++] = static_cast<float>(std::sin(pos * th[r]));
         }
     };
-    for (int m = 0; m < ntiles; ++m) put(static_cast<double>(m) * kTile);
-    for (int rr = 0; rr < kTile; ++rr) put(static_cast<double>(rr));
+    for (int m = 0; m < ntiles; ++m) put(static_cast<double>(m) * block);
+    for (int rr = 0; rr < block; ++rr) put(static_cast<double>(rr));
     return t;
 }
 

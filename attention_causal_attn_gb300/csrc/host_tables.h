@@ -30,10 +30,11 @@ constexpr int rope_rows_per_pass(int D) { return 2048 / D; }
 std::vector<float> rope_factor_table(int S, int D, double base);
 size_t rope_factor_table_floats(int S, int D);
 
-// Factor tables of the pre-rotation pass (float2 = (cos, sin), float32 from
-// float64): base[m][r] = angle 128*m*theta_r for m = 0..ceil(S/128)-1, then
-// row[rr][r] = angle rr*theta_r for rr = 0..127.
-std::vector<float> rope_split_tables(int S, int D, double base);
+// Factor tables of the pre-rotation pass (block = 128) and of decode
+// (block = 32), float2 = (cos, sin), float32 from float64:
+// base[m][r] = angle block*m*theta_r for m = 0..ceil(S/block)-1, then
+// row[rr][r] = angle rr*theta_r for rr = 0..block-1.
+std::vector<float> rope_split_tables(int S, int D, double base, int block);
 
 // W_r = floor(k * 2*pi / theta_r) clamped to [0, INT32_MAX]; INT32_MAX when
 // the window is off (k <= 0 or infinite).  ("ATFlash", The idea.)

@@ -355,6 +355,74 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
+# --------------------------------------------------------------------- decode
+def decode_bytes(w):
+    """K/V bytes a decode step must read: V whole, K without the 16-byte pair chunks the window skips."""
+    import attention_causal_attn_gb300 as attn
+    B, Hkv, S, D = w["B"], w["Hkv"], w["S"], w["D"]
+    v_bytes = B * S * Hkv * D * 2
+    if not w["window_k"]:
+        return 2 * v_bytes
+    _, _, win = attn.attn_build_tables(1, D, w["rope_base"], w["window_k"])
+    dist = np.arange(S - 1, -1, -1, dtype=np.int64)  # key j sits at distance S-1-j
+    cut = np.searchsorted(win.astype(np.int64), dist, side="left")  # pairs with W_r < dist
+    kept_chunks = (D // 2 - (cut // 8) * 8) * 2  # channels loaded per key (whole 8-pair chunks skipped)
+    return v_bytes + int(B * Hkv * 2 * kept_chunks.sum())
+
+
+def run_decode(args, w, rank, world, local_rank):
+    """One step = one attn_decode call (the newest token of each sequence against its cache)."""
+    import torch
+    import attention_causal_attn_gb300 as attn
+    attn.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B, Hq, Hkv, S, D = w["B"], w["Hq"], w["Hkv"], w["S"], w["D"]
+    q_full, k_h, v_h = si.make_qkv(B, 1, Hkv, S, D, seed=replica_seed(rank))
+    q_h = si.bshd_bf16(replica_seed(rank), 4, B, 1, Hq, D)[:, 0]
+    k, v = (torch.from_numpy(x).view(torch.bfloat16).to(dev) for x in (k_h, v_h))
+    q = torch.from_numpy(np.ascontiguousarray(q_h)).view(torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        attn.attn_decode(q, k, v, o, lse, rope_base=w["rope_base"], window_k=w["window_k"], stream=stream)
+    attn.attn_check(stream=stream, device=dev)
+    # caches larger than L2 are streamed from HBM on every step; smaller ones get an L2 flush between steps
+    kv_bytes = 2 * k.numel() * 2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if kv_bytes < (256 << 20) else None
+    times = []
+    with ClockSampler(local_rank) as clocks:
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.attn_decode(q, k, v, o, lse, rope_base=w["rope_base"], window_k=w["window_k"], stream=stream)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+    attn.attn_check(stream=stream, device=dev)
+    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    nbytes = decode_bytes(w)
+    peaks, peak_kind = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    cfg = workload_config(args.workload, w)
+    cfg["step"] = "decode: one query per sequence at position S-1 against the whole cache"
+    cfg["l2"] = "cache larger than L2, streamed every step" if flush is None else "L2 flushed between steps"
+    return {
+        "metric": "decode K/V read GB/s", "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                     "frac": round(gbs / float(peaks["hbm_gbs"]), 4), "traffic": None,
+                     "kernel": "decode_split_kernel + decode_combine_kernel",
+                     "algorithmic": "K/V bytes read per step (window-skipped K chunks excluded), median step time"},
+        "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
+    }
+
+
 # --------------------------------------------------------------------- reference arm
 def run_reference(args, w, rank):
     if rank != 0:
@@ -401,6 +469,8 @@ def main():
     ap.add_argument("--window-k", type=float, default=None, help="override the workload's window multiplier")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling captures)")
     ap.add_argument("--seq", type=int, default=None, help="override the workload's sequence length")
+    ap.add_argument("--decode", action="store_true",
+                    help="time one decode step (attn_decode) on the workload's cache shape instead of the prefill")
     ap.add_argument("--rope-lowering", default="fused", choices=["fused", "prerotate"],
                     help="fused: RoPE at load (the specified path); prerotate: a rotation pass, then the attention")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -422,6 +492,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         line = run_reference(args, w, rank)
+    elif args.decode:
+        line = run_decode(args, w, rank, world, local_rank)
     else:
         line = run_ours(args, w, rank, world, local_rank)
     if line is not None:

@@ -176,6 +176,35 @@ int attn_fwd_rotated(const void* q_rot, const void* k_rot, const void* v, void* 
                      int B, int Hq, int Hkv, int S, int D, int causal, void* stream);
 
 /*
+ * attn_decode — one decode step: each sequence's newest token against its KV cache.
+ *
+ * The query of each sequence sits at position S-1 and attends to keys
+ * 0..S-1 (its own K/V are the cache's last rows), with the conventions of
+ * attn_fwd: RoPE applied to q and to K as it is loaded, scale 1/sqrt(D),
+ * bf16 output, natural-log LSE.  The key range is split across CTAs and the
+ * partial results merge through their log-sum-exp ("AttnFuse: A Composable
+ * DSL for Compiling Attentions to Fused GPU Kernels", sec. 4.2 Decode).
+ * With window_k > 0 the per-RoPE-pair window of "ATFlash — Per-RoPE-Wavelength
+ * Attention Windows" (decode) applies: pair r of key j is dropped when
+ * S-1-j > W_r, and those K components are not loaded.
+ *   q       bf16 device [B][Hq][D].
+ *   k, v    bf16 device caches [B][S][Hkv][D] (K not rotated).
+ *   o       bf16 device output [B][Hq][D];  lse float32 [B][Hq] or NULL.
+ *   B, Hq, Hkv, S, D, rope_base, window_k   as attn_fwd; Hq / Hkv <= 32.
+ * Decode reads each K/V byte once: it is bound by HBM bandwidth.  Q K^T and
+ * P V run as warp-level mma.sync over 32-key tiles (rotated q and K rounded to
+ * fp16, P to bf16, fp32 accumulation, as in attn_fwd); the number of splits
+ * (multiples of 128 keys) is chosen for about one or two waves of resident
+ * CTAs.  Asynchronous on `stream`; the library keeps a partial-result scratch
+ * of B * Hq * splits * (D + 2) floats and a rotation-factor table of
+ * (ceil(S/32) + 32) * D/2 (cos, sin) pairs per (S, D, rope_base) until
+ * attn_release_cache().  Errors: as attn_fwd, and ATTN_ERR_UNSUPPORTED when
+ * Hq / Hkv > 32.
+ */
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int Hq, int Hkv, int S, int D, double rope_base, double window_k, void* stream);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

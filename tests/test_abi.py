@@ -19,7 +19,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
     assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated",
-                          "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
+                          "attn_decode", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for n in names:
@@ -78,6 +78,18 @@ def test_rotation_entries_check_arguments_on_the_host(lib):
     assert lib.attn_rope_rotate(24, 16, 1, 128, 2, 128, 1e4, None) == E["ATTN_ERR_ALIGN"]
     assert lib.attn_fwd_rotated(16, 16, 16, 16, None, 1, 6, 4, 128, 128, 1, None) == E["ATTN_ERR_SHAPE"]
     assert lib.attn_fwd_rotated(16, 16, 16, 16, None, 1, 2, 2, 128, 128, 2, None) == E["ATTN_ERR_UNSUPPORTED"]
+
+
+def test_decode_checks_arguments_on_the_host(lib):
+    E = attn.ATTN_STATUS
+    call = lambda **kw: lib.attn_decode(*(kw.get(n, 16) for n in ("q", "k", "v", "o")), None, kw.get("B", 1),
+                                         kw.get("Hq", 2), kw.get("Hkv", 2), kw.get("S", 128), kw.get("D", 128),
+                                         kw.get("base", 1e4), kw.get("win", 0.0), None)
+    assert call(q=0) == E["ATTN_ERR_NULL"]
+    assert call(S=0) == E["ATTN_ERR_SHAPE"]
+    assert call(Hq=66, Hkv=2) == E["ATTN_ERR_UNSUPPORTED"]  # more than 32 query heads per KV head
+    assert call(base=0.0, win=1.0) == E["ATTN_ERR_UNSUPPORTED"]  # window needs RoPE
+    assert call(k=24) == E["ATTN_ERR_ALIGN"]
 
 
 def test_rope_tables_are_float64_cos_sin_rounded(lib):

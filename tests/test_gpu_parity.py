@@ -261,3 +261,42 @@ def test_pre_rotated_forward_matches_oracle_and_fused(B, Hq, Hkv, S, D, causal, 
     _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "pre-rotated")
     # both paths round the rotated operands to fp16; only the angles' last fp32 bits differ
     assert (o.float() - o_f.float()).abs().max().item() <= 1e-2
+
+
+DECODE = [
+    # B, Hq, Hkv, S, D, rope_base, window_k
+    (2, 8, 2, 1000, 128, 10000.0, None),     # GQA groups of 4, several splits
+    (3, 4, 4, 257, 64, None, None),          # MHA, RoPE off, ragged split tail
+    (1, 32, 1, 700, 128, 10000.0, None),     # all 32 query heads on one KV head
+    (1, 16, 2, 1, 128, 10000.0, None),       # a cache of one key
+    (1, 32, 8, 5000, 128, 500000.0, 1.0),    # windowed decode
+    (1, 8, 8, 3000, 128, 100.0, 0.3),        # small base: the window drops most pairs of far keys
+    (2, 6, 2, 2500, 64, 10000.0, None),      # groups of 3, D = 64
+    (1, 40, 2, 1500, 128, 10000.0, 2.0),     # groups of 20: two 16-head tiles, the second partly empty
+    (2, 8, 4, 1800, 64, 500.0, 0.5),         # windowed, D = 64
+]
+
+
+def _decode_check(B, Hq, Hkv, S, D, base, wk, seed):
+    q_full, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=seed)
+    q_dec = np.ascontiguousarray(q_full[:, S - 1])  # the newest token of each sequence
+    o, lse = attn.attn_decode(_dev(q_dec), _dev(k), _dev(v), rope_base=base, window_k=wk)
+    attn.attn_check()
+    rb = np.repeat(np.arange(B), Hq)
+    rh = np.tile(np.arange(Hq), B)
+    ri = np.full(B * Hq, S - 1)
+    o_ref, lse_ref = oracle.attn_rows(q_full, k, v, rb, rh, ri, causal=True, rope_base=base, window_k=wk)
+    _check(o.float().cpu().numpy().reshape(B * Hq, D), lse.cpu().numpy().reshape(-1), o_ref, lse_ref,
+           f"decode S={S}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,base,wk", DECODE)
+def test_decode_matches_oracle_last_row(B, Hq, Hkv, S, D, base, wk):
+    """attn_decode: the query at position S-1 against the whole cache, i.e. the
+    last row of the causal prefill, split across CTAs and merged by LSE."""
+    _decode_check(B, Hq, Hkv, S, D, base, wk, seed=808 + S)
+
+
+@pytest.mark.parametrize("wk", [4.0, None])
+def test_decode_long_cache_s131072(wk):
+    _decode_check(1, 32, 8, 131072, 128, 500000.0, wk, seed=909)

@@ -225,8 +225,16 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const __gr
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
         const int lrow = (lane & 7);  // ldmatrix row this lane addresses
+        // with the window, k-step pairs (s, s + kPairSteps) whose 16 pairs every key of the tile
+        // drops are skipped: their loads, rotations and MMAs would only add zeros
+        // the next tile's cuts, ahead of the S arithmetic so that their lookups do not delay its K copy
+        const int rcut_next =
+            (WIN && t0 + kStride + lane < j1) ? window_cut<kHalf>(win_s, qpos - (t0 + kStride + lane)) : 0;
+        const int s_lo = WIN ? __reduce_min_sync(0xffffffffu, static_cast<unsigned>(t0 + lane < j1 ? rcut : kHalf)) / 16
+                             : 0;
 #pragma unroll
         for (int s = 0; s < kPairSteps; ++s) {
+            if (WIN && s < s_lo) continue;
             float4 fb[2];
             if (ROPE) {
 #pragma unroll
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_split_kernel(const __gr
         __syncwarp();  // every lane has read this tile's K
         // fetch the next tile's K behind the softmax and P V of this one
         if (more) {
-            if (WIN) rcut = t0 + kStride + lane < j1 ? window_cut<kHalf>(win_s, qpos - (t0 + kStride + lane)) : 0;
+            rcut = rcut_next;
             dec_stage<D, WIN>(kt, kbase, row_stride, t0 + kStride, j1, lane, rcut);
             stage_factors(t0 + kStride);
         }

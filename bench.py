@@ -333,9 +333,9 @@ def run_ours(args, w, rank, world, local_rank):
     return line
 
 
-def load_traffic(workload):
+def load_traffic(workload, kernel="attn_fwd_kernel"):
     """DRAM bytes per launch from the committed ncu summary of this kernel and workload, if present."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_kernel_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
@@ -405,6 +405,7 @@ def run_decode(args, w, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
     ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    same_shape = args.batch is None and args.seq is None and args.window_k is None
     nbytes = decode_bytes(w)
     peaks, peak_kind = load_peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
@@ -416,7 +417,8 @@ def run_decode(args, w, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                     "frac": round(gbs / float(peaks["hbm_gbs"]), 4), "traffic": None,
+                     "frac": round(gbs / float(peaks["hbm_gbs"]), 4),
+                     "traffic": load_traffic(args.workload, "decode_split_kernel") if same_shape else None,
                      "kernel": "decode_split_kernel + decode_combine_kernel",
                      "algorithmic": "K/V bytes read per step (window-skipped K chunks excluded), median step time"},
         "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),

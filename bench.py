@@ -370,6 +370,30 @@ def decode_bytes(w):
     return v_bytes + int(B * Hkv * 2 * kept_chunks.sum())
 
 
+def set_l2_fetch_granularity(nbytes):
+    """Set this process's CUDA context hint for the DRAM fetch size behind an L2 miss
+    (cudaLimitMaxL2FetchGranularity, 0..128 bytes).  It ends with the process; nothing on the
+    GPU outlives it.  Returns (before, after) in bytes."""
+    import ctypes
+    rt = None
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if rt is None:
+        raise RuntimeError("the CUDA runtime library was not found")
+    limit = 5  # cudaLimitMaxL2FetchGranularity
+    before, after = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    if rt.cudaDeviceGetLimit(ctypes.byref(before), limit) != 0:
+        raise RuntimeError("cudaDeviceGetLimit(cudaLimitMaxL2FetchGranularity) failed")
+    if rt.cudaDeviceSetLimit(limit, ctypes.c_size_t(nbytes)) != 0:
+        raise RuntimeError("cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity) failed")
+    rt.cudaDeviceGetLimit(ctypes.byref(after), limit)
+    return before.value, after.value
+
+
 def run_decode(args, w, rank, world, local_rank):
     """One step = one attn_decode call (the newest token of each sequence against its cache)."""
     import torch
@@ -382,6 +406,7 @@ def run_decode(args, w, rank, world, local_rank):
     q_h = si.bshd_bf16(replica_seed(rank), 4, B, 1, Hq, D)[:, 0]
     k, v = (torch.from_numpy(x).view(torch.bfloat16).to(dev) for x in (k_h, v_h))
     q = torch.from_numpy(np.ascontiguousarray(q_h)).view(torch.bfloat16).to(dev)
+    fetch = set_l2_fetch_granularity(args.l2_fetch_bytes) if args.l2_fetch_bytes is not None else None
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -405,13 +430,15 @@ def run_decode(args, w, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
     ms = float(np.median([a.elapsed_time(b) for a, b in times]))
-    same_shape = args.batch is None and args.seq is None and args.window_k is None
+    same_shape = args.batch is None and args.seq is None and args.window_k is None and args.l2_fetch_bytes is None
     nbytes = decode_bytes(w)
     peaks, peak_kind = load_peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
     cfg = workload_config(args.workload, w)
     cfg["step"] = "decode: one query per sequence at position S-1 against the whole cache"
     cfg["l2"] = "cache larger than L2, streamed every step" if flush is None else "L2 flushed between steps"
+    if fetch is not None:
+        cfg["l2_fetch_granularity_bytes"] = {"before": fetch[0], "during": fetch[1]}
     return {
         "metric": "decode K/V read GB/s", "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
@@ -473,6 +500,9 @@ def main():
     ap.add_argument("--seq", type=int, default=None, help="override the workload's sequence length")
     ap.add_argument("--decode", action="store_true",
                     help="time one decode step (attn_decode) on the workload's cache shape instead of the prefill")
+    ap.add_argument("--l2-fetch-bytes", type=int, default=None,
+                    help="decode only: set the context's L2 fetch granularity hint (32 lets the window's "
+                         "skipped 16-byte K chunks stay unread in DRAM)")
     ap.add_argument("--rope-lowering", default="fused", choices=["fused", "prerotate"],
                     help="fused: RoPE at load (the specified path); prerotate: a rotation pass, then the attention")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -50,6 +50,8 @@ def _load():
             lib.oracle_window_widths.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, f64p]
             lib.oracle_rope_rotate.restype = None
             lib.oracle_rope_rotate.argtypes = [u16p] + [ctypes.c_int] * 4 + [ctypes.c_double, f64p]
+            lib.oracle_attn_bwd.restype = ctypes.c_int
+            lib.oracle_attn_bwd.argtypes = [f64p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_double] + [f64p] * 3
             lib.oracle_threads.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -124,3 +126,31 @@ def window_widths(D: int, rope_base: float, window_k: float) -> np.ndarray:
     w = np.zeros(D // 2, dtype=np.float64)
     _load().oracle_window_widths(D, float(rope_base), float(window_k) if window_k else 0.0, _ptr(w, ctypes.c_double))
     return w
+
+
+def bf16_to_f64(x) -> np.ndarray:
+    """bf16 bits (uint16) widened exactly to float64."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def attn_bwd(q, k, v, dO, *, causal=True, rope_base=None):
+    """dQ [B,S,Hq,D], dK, dV [B,S,Hkv,D] (float64) of sum(O * dO) for the attention forward.
+
+    q, k, v, dO: uint16 bf16 bits (widened exactly) or float64 arrays, BSHD.
+    """
+    def f64(a):
+        return bf16_to_f64(a) if a.dtype == np.uint16 else np.ascontiguousarray(a, dtype=np.float64)
+    q, k, v, dO = (f64(a) for a in (q, k, v, dO))
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    rc = _load().oracle_attn_bwd(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
+                                 _ptr(dO, ctypes.c_double), B, Hq, Hkv, S, D, 1 if causal else 0,
+                                 float(rope_base) if rope_base else 0.0, _ptr(dq, ctypes.c_double),
+                                 _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dq, dk, dv

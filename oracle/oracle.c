@@ -235,3 +235,158 @@ long long oracle_pruned_terms(int S, int D, double rope_base, double window_k) {
         }
     return count;
 }
+
+/*
+ * Gradients of the attention above (RoPE, causal or full, GQA; window off)
+ * for a scalar loss whose gradient with respect to O is dO ("AttnFuse",
+ * sec. 4.4 Backward Pass: the backward re-derives the softmax probabilities
+ * from the forward's per-row L = m + log l).  Written from the chain rule on
+ * the definitions, one (batch, KV head) group at a time, with every
+ * probability row materialised:
+ *
+ *   p_ij   = exp(s_ij - LSE_i)                  (s as in the forward)
+ *   dV_j   = sum_i p_ij dO_i                    (summed over the group's heads)
+ *   dP_ij  = dO_i . V_j
+ *   Dlt_i  = sum_j p_ij dP_ij                   (= dO_i . O_i)
+ *   dS_ij  = p_ij (dP_ij - Dlt_i)               (softmax Jacobian)
+ *   dq'_i  = (1/sqrt(D)) sum_j dS_ij k'_j,  dk'_j = (1/sqrt(D)) sum_i dS_ij q'_i
+ *   dq_i   = R(p_i)^T dq'_i,  dk_j = R(p_j)^T dk'_j   (the transpose of the
+ *            rotation of pair r by angle a: (x, y) -> (x cos a + y sin a,
+ *            -x sin a + y cos a))
+ *
+ * Inputs are float64 (the bf16 bits widened by the caller, or any values for
+ * a finite-difference check): q, dO [B][S][Hq][D]; k, v [B][S][Hkv][D].
+ * Outputs dq [B][S][Hq][D], dk, dv [B][S][Hkv][D], float64.
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dO,
+                    int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                    double* dq, double* dk, double* dv) {
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 1024) return -1;
+    const int rope_on = rope_base > 0.0;
+    const int G = Hq / Hkv;
+    const int half = D / 2;
+    double theta[512];
+    if (rope_on) rope_thetas(D, rope_base, theta);
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bg = 0; bg < B * Hkv; ++bg) {
+        const int b = bg / Hkv, g = bg % Hkv;
+        double* kr = (double*)malloc(sizeof(double) * (size_t)S * D);   /* rotated keys */
+        double* dkr = (double*)calloc((size_t)S * D, sizeof(double));   /* gradient wrt rotated keys */
+        double* qr = (double*)malloc(sizeof(double) * (size_t)D);
+        double* dqr = (double*)malloc(sizeof(double) * (size_t)D);
+        double* p = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dvg = dv + ((size_t)b * S * Hkv + g) * D;  /* row j at dvg + j * Hkv * D */
+        for (int j = 0; j < S; ++j)
+            for (int d = 0; d < D; ++d) dvg[(size_t)j * Hkv * D + d] = 0.0;
+        /* rotated keys */
+        for (int j = 0; j < S; ++j) {
+            const double* kj = k + (((size_t)b * S + j) * Hkv + g) * D;
+            double* o = kr + (size_t)j * D;
+            for (int r = 0; r < half; ++r) {
+                const double x = kj[r], y = kj[r + half];
+                if (rope_on) {
+                    const double a = (double)j * theta[r], c = cos(a), s = sin(a);
+                    o[r] = x * c - y * s;
+                    o[r + half] = y * c + x * s;
+                } else {
+                    o[r] = x;
+                    o[r + half] = y;
+                }
+            }
+        }
+        for (int h = g * G; h < (g + 1) * G; ++h) {
+            for (int i = 0; i < S; ++i) {
+                const int last = causal ? i : S - 1;
+                const double* qi = q + (((size_t)b * S + i) * Hq + h) * D;
+                const double* doi = dO + (((size_t)b * S + i) * Hq + h) * D;
+                for (int r = 0; r < half; ++r) {
+                    const double x = qi[r], y = qi[r + half];
+                    if (rope_on) {
+                        const double a = (double)i * theta[r], c = cos(a), s = sin(a);
+                        qr[r] = x * c - y * s;
+                        qr[r + half] = y * c + x * s;
+                    } else {
+                        qr[r] = x;
+                        qr[r + half] = y;
+                    }
+                }
+                /* probabilities of row i */
+                double m = -INFINITY;
+                for (int j = 0; j <= last; ++j) {
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d) acc += qr[d] * kr[(size_t)j * D + d];
+                    p[j] = acc * inv_sqrt_d;
+                    if (p[j] > m) m = p[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j <= last; ++j) {
+                    p[j] = exp(p[j] - m);
+                    l += p[j];
+                }
+                for (int j = 0; j <= last; ++j) p[j] /= l;
+                /* dV, dP and the row's Dlt */
+                double dlt = 0.0;
+                for (int j = 0; j <= last; ++j) {
+                    const double* vj = v + (((size_t)b * S + j) * Hkv + g) * D;
+                    double* dvj = dvg + (size_t)j * Hkv * D;
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d) {
+                        dvj[d] += p[j] * doi[d];
+                        acc += doi[d] * vj[d];
+                    }
+                    dp[j] = acc;
+                    dlt += p[j] * acc;
+                }
+                /* dS, then the gradients wrt the rotated q and k */
+                for (int d = 0; d < D; ++d) dqr[d] = 0.0;
+                for (int j = 0; j <= last; ++j) {
+                    const double ds = p[j] * (dp[j] - dlt) * inv_sqrt_d;
+                    for (int d = 0; d < D; ++d) {
+                        dqr[d] += ds * kr[(size_t)j * D + d];
+                        dkr[(size_t)j * D + d] += ds * qr[d];
+                    }
+                }
+                /* back through the rotation of q */
+                double* dqi = dq + (((size_t)b * S + i) * Hq + h) * D;
+                for (int r = 0; r < half; ++r) {
+                    const double x = dqr[r], y = dqr[r + half];
+                    if (rope_on) {
+                        const double a = (double)i * theta[r], c = cos(a), s = sin(a);
+                        dqi[r] = x * c + y * s;
+                        dqi[r + half] = -x * s + y * c;
+                    } else {
+                        dqi[r] = x;
+                        dqi[r + half] = y;
+                    }
+                }
+            }
+        }
+        /* back through the rotation of k */
+        for (int j = 0; j < S; ++j) {
+            const double* x0 = dkr + (size_t)j * D;
+            double* dkj = dk + (((size_t)b * S + j) * Hkv + g) * D;
+            for (int r = 0; r < half; ++r) {
+                const double x = x0[r], y = x0[r + half];
+                if (rope_on) {
+                    const double a = (double)j * theta[r], c = cos(a), s = sin(a);
+                    dkj[r] = x * c + y * s;
+                    dkj[r + half] = -x * s + y * c;
+                } else {
+                    dkj[r] = x;
+                    dkj[r + half] = y;
+                }
+            }
+        }
+        free(kr);
+        free(dkr);
+        free(qr);
+        free(dqr);
+        free(p);
+        free(dp);
+    }
+    return 0;
+}

@@ -1,0 +1,158 @@
+"""Pins for the oracle's backward pass (gradients of sum(O * dO)).
+
+Each test ties it to something other than itself:
+- torch autograd through scaled_dot_product_attention in float64, with RoPE
+  written as complex multiplication (a library routine and a different
+  formulation of the rotation);
+- central finite differences of a forward written with explicit 2x2 rotation
+  matrices, on a tiny case (brute force);
+- invariants: the value gradients sum to the output gradients, a constant
+  added to every value row leaves dQ and dK unchanged, the gradients of a
+  fully masked-out key are zero, and GQA equals MHA with repeated K/V.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+
+
+def _inputs(B, Hq, Hkv, S, D, seed):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=seed)
+    dO = si.bshd_bf16(seed + 1000, 9, B, S, Hq, D)
+    return q, k, v, dO
+
+
+def _rope_torch(x, base):
+    """RoPE as complex multiplication on a float64 BSHD tensor: z_r * exp(i p theta_r)."""
+    B, S, H, D = x.shape
+    h = D // 2
+    theta = base ** (-2.0 * torch.arange(h, dtype=torch.float64) / D)
+    ang = torch.arange(S, dtype=torch.float64)[:, None] * theta[None, :]
+    rot = torch.polar(torch.ones_like(ang), ang)[None, :, None, :]
+    z = torch.complex(x[..., :h], x[..., h:]) * rot
+    return torch.cat([z.real, z.imag], dim=-1)
+
+
+def _autograd_ref(q, k, v, dO, causal, base):
+    G = q.shape[2] // k.shape[2]
+    qt, kt, vt = (torch.from_numpy(oracle.bf16_to_f64(a)).requires_grad_(True) for a in (q, k, v))
+    qr = _rope_torch(qt, base) if base else qt
+    kr = _rope_torch(kt, base) if base else kt
+    qh = qr.permute(0, 2, 1, 3)
+    kh = kr.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    vh = vt.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    o = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, is_causal=causal)
+    loss = (o.permute(0, 2, 1, 3) * torch.from_numpy(oracle.bf16_to_f64(dO))).sum()
+    loss.backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("Hq,Hkv,base", [(2, 2, None), (4, 2, 10000.0), (3, 1, 500000.0), (2, 1, 37.0)])
+def test_backward_equals_torch_autograd(causal, Hq, Hkv, base):
+    q, k, v, dO = _inputs(2, Hq, Hkv, 23, 16, seed=5)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dO, causal=causal, rope_base=base)
+    rq, rk, rv = _autograd_ref(q, k, v, dO, causal, base)
+    np.testing.assert_allclose(dq, rq, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, rk, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, rv, rtol=0, atol=1e-11)
+
+
+def _loss_explicit(q, k, v, dO, causal, base):
+    """sum(O * dO) with RoPE as an explicit 2x2 rotation matrix per (position, pair)."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    h = D // 2
+
+    def rot(x):
+        out = np.empty_like(x)
+        for s in range(S):
+            for r in range(h):
+                a = s * base ** (-2.0 * r / D) if base else 0.0
+                m = np.array([[math.cos(a), -math.sin(a)], [math.sin(a), math.cos(a)]])
+                pair = np.stack([x[:, s, :, r], x[:, s, :, r + h]], axis=-1)  # [B, H, 2]
+                res = pair @ m.T
+                out[:, s, :, r], out[:, s, :, r + h] = res[..., 0], res[..., 1]
+        return out
+
+    qr, kr = rot(q), rot(k)
+    total = 0.0
+    for b in range(B):
+        for hh in range(Hq):
+            g = hh // G
+            s = qr[b, :, hh, :] @ kr[b, :, g, :].T / math.sqrt(D)
+            if causal:
+                s = np.where(np.tril(np.ones((S, S), bool)), s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            total += float(np.sum((p @ v[b, :, g, :]) * dO[b, :, hh, :]))
+    return total
+
+
+@pytest.mark.parametrize("causal,base", [(True, 10000.0), (False, 10.0), (True, None)])
+def test_backward_matches_finite_differences(causal, base):
+    rng = np.random.default_rng(3)
+    B, Hq, Hkv, S, D = 1, 2, 1, 5, 4
+    q = rng.standard_normal((B, S, Hq, D))
+    k = rng.standard_normal((B, S, Hkv, D))
+    v = rng.standard_normal((B, S, Hkv, D))
+    dO = rng.standard_normal((B, S, Hq, D))
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dO, causal=causal, rope_base=base)
+    eps = 1e-6
+    for x, grad in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            up = _loss_explicit(q, k, v, dO, causal, base)
+            x[idx] = old - eps
+            dn = _loss_explicit(q, k, v, dO, causal, base)
+            x[idx] = old
+            num[idx] = (up - dn) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-8)
+
+
+def test_value_gradients_sum_to_output_gradients():
+    """Each probability row sums to one, so sum_j dV_j = sum_i dO_i over a KV group's heads."""
+    q, k, v, dO = _inputs(2, 4, 2, 31, 32, seed=8)
+    _, _, dv = oracle.attn_bwd(q, k, v, dO, causal=True, rope_base=10000.0)
+    dOf = oracle.bf16_to_f64(dO)
+    for g in range(2):
+        np.testing.assert_allclose(dv[:, :, g, :].sum(axis=1), dOf[:, :, 2 * g:2 * g + 2, :].sum(axis=(1, 2)),
+                                   rtol=0, atol=1e-11)
+
+
+def test_constant_value_shift_leaves_query_and_key_gradients():
+    """V_j + c for every j shifts O_i by c; dP and Dlt shift alike, so dS, dQ and dK do not change."""
+    q, k, v, dO = _inputs(1, 2, 2, 19, 16, seed=9)
+    vf = oracle.bf16_to_f64(v)
+    dq0, dk0, _ = oracle.attn_bwd(q, k, vf, dO, causal=True, rope_base=500000.0)
+    dq1, dk1, _ = oracle.attn_bwd(q, k, vf + np.linspace(-3, 3, 16), dO, causal=True, rope_base=500000.0)
+    np.testing.assert_allclose(dq1, dq0, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dk1, dk0, rtol=0, atol=1e-10)
+
+
+def test_last_key_gets_gradient_only_from_the_last_query():
+    """Under the causal mask key S-1 is seen by query S-1 alone; with that row's dO zero its dK, dV are zero."""
+    q, k, v, dO = _inputs(1, 2, 1, 13, 16, seed=10)
+    dOf = oracle.bf16_to_f64(dO)
+    dOf[:, -1] = 0.0
+    _, dk, dv = oracle.attn_bwd(q, k, v, dOf, causal=True, rope_base=10000.0)
+    assert np.all(dk[:, -1] == 0.0) and np.all(dv[:, -1] == 0.0)
+    assert np.abs(dk[:, :-1]).max() > 0 and np.abs(dv[:, :-1]).max() > 0
+
+
+def test_gqa_backward_equals_mha_with_repeated_kv():
+    """A KV head shared by G query heads gets the sum of the G heads' gradients."""
+    q, k, v, dO = _inputs(1, 4, 2, 17, 16, seed=12)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dO, causal=True, rope_base=10000.0)
+    k2, v2 = np.repeat(k, 2, axis=2), np.repeat(v, 2, axis=2)
+    dq2, dk2, dv2 = oracle.attn_bwd(q, k2, v2, dO, causal=True, rope_base=10000.0)
+    np.testing.assert_allclose(dq, dq2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, dk2.reshape(1, 17, 2, 2, 16).sum(axis=3), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, dv2.reshape(1, 17, 2, 2, 16).sum(axis=3), rtol=0, atol=1e-12)

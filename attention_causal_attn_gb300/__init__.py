@@ -16,7 +16,7 @@ import numpy as np
 
 from ._build import INCLUDE, LIB, build
 
-__all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -58,6 +58,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_rotated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.attn_decode.restype = i
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, d, d, vp]
+        lib.attn_bwd.restype = i
+        lib.attn_bwd.argtypes = [vp] * 9 + [i] * 6 + [d, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i
@@ -195,6 +197,33 @@ def attn_decode(q, k, v, o=None, lse=None, *, rope_base=None, window_k=None, ret
     if rc != 0:
         raise AttnError(rc, "attn_decode")
     return o, lse
+
+
+def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream=None):
+    """Gradients (dq, dk, dv) of the forward for upstream gradient dO; o and lse are the forward's outputs."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (BSHD)")
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, S, Hkv, D] with q's B, S and D")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dO.shape) != tuple(q.shape):
+        raise ValueError("o and dO must have q's shape")
+    if not (lse.is_cuda and lse.dtype == torch.float32 and tuple(lse.shape) == (B, Hq, S) and lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, Hq, S]")
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S, D, 1 if causal else 0,
+                          float(rope_base) if rope_base else 0.0, _stream_handle(stream, q.device))
+    if rc != 0:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_host(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=None, window_k=None,

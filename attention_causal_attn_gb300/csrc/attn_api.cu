@@ -17,6 +17,7 @@
 #include "attn_fwd_kernel.cuh"
 #include "rope_rotate_kernel.cuh"
 #include "decode_kernel.cuh"
+#include "bwd_kernel.cuh"
 #include "host_tables.h"
 
 // Raised (bitwise OR) by a CTA whose bounded wait ran out; read and cleared by attn_check().
@@ -772,6 +773,115 @@ extern "C" int attn_decode(const void* q, const void* k, const void* v, void* o,
     return ATTN_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Backward ("AttnFuse", sec. 4.4 Backward Pass: row reduction, dK/dV, dQ).
+namespace {
+DecodeScratch g_bwd[kMaxDevices];  // Dlt rows, [B][Hq][S] floats
+unsigned g_bwd_configured[kMaxDevices];
+
+template <int D, bool CAUSAL, bool ROPE>
+int launch_bwd(const attn::BwdParams& bp, int dev, int ntiles, cudaStream_t st) {
+    using L = attn::BwdLayout<D>;
+    // at least 120 KB so that one CTA fits on an SM: each CTA takes all 512 TMEM columns
+    constexpr int smem = static_cast<int>(L::kAlloc) > 120 * 1024 ? static_cast<int>(L::kAlloc) : 120 * 1024;
+    constexpr unsigned bit = 1u << ((D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0));
+    auto kv = attn::bwd_dkdv_kernel<D, CAUSAL, ROPE>;
+    auto kq = attn::bwd_dq_kernel<D, CAUSAL, ROPE>;
+    cudaError_t e;
+    if (!(g_bwd_configured[dev] & bit)) {
+        if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return cuda_fail("cudaFuncSetAttribute(backward)", e);
+        g_bwd_configured[dev] |= bit;
+    }
+    const int B = bp.f.B, Hq = bp.f.Hq, Hkv = bp.f.Hkv;
+    kv<<<dim3(static_cast<unsigned>(B * Hkv), static_cast<unsigned>(ntiles)), attn::kBwdThreads, smem, st>>>(bp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("dK/dV kernel launch", e);
+    kq<<<dim3(static_cast<unsigned>(B * Hq), static_cast<unsigned>(ntiles)), attn::kBwdThreads, smem, st>>>(bp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("dQ kernel launch", e);
+    return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
+                        double rope_base, void* stream) {
+    int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, 0.0);
+    if (arc == ATTN_OK && (dO == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr))
+        arc = ATTN_ERR_NULL;
+    if (arc == ATTN_OK && (static_cast<long long>(B) * Hq > INT_MAX / 2)) arc = ATTN_ERR_SHAPE;
+    if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+                           !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+                           (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+        arc = ATTN_ERR_ALIGN;
+    if (arc != ATTN_OK) return arc;
+    const bool rope = rope_base > 0.0 && std::isfinite(rope_base);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+
+    attn::BwdParams bp;
+    float2* rope_tab = nullptr;
+    float2* split_tab = nullptr;
+    float* dlt = nullptr;
+    const size_t rows = static_cast<size_t>(B) * Hq * S;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int rc = probe_device(dev);
+        if (rc != ATTN_OK) return rc;
+        if (rope && ((rc = get_rope(dev, S, D, rope_base, &rope_tab)) != ATTN_OK ||
+                     (rc = get_split(dev, S, D, rope_base, 32, &split_tab)) != ATTN_OK))
+            return rc;
+        DecodeScratch& ds = g_bwd[dev];
+        if (ds.floats < rows) {
+            if (ds.buf != nullptr) cudaFree(ds.buf);
+            ds.buf = nullptr;
+            ds.floats = 0;
+            cudaError_t e;
+            if ((e = cudaMalloc(&ds.buf, rows * sizeof(float))) != cudaSuccess)
+                return cuda_fail("cudaMalloc(backward rows)", e, ATTN_ERR_OOM);
+            ds.floats = rows;
+        }
+        dlt = ds.buf;
+        bp.f.status = g_dev[dev].status;
+    }
+    if (!encode_bshd(&bp.f.tm_q, q, B, S, Hq, D) || !encode_bshd(&bp.f.tm_k, k, B, S, Hkv, D) ||
+        !encode_bshd(&bp.f.tm_v, v, B, S, Hkv, D) || !encode_bshd(&bp.tm_do, dO, B, S, Hq, D))
+        return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    bp.f.rope = rope_tab;
+    bp.f.B = B;
+    bp.f.Hq = Hq;
+    bp.f.Hkv = Hkv;
+    bp.f.S = S;
+    bp.f.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    bp.f.wait_limit_ns = kWaitLimitNs;
+    bp.lse = lse;
+    bp.dlt = dlt;
+    bp.dq = static_cast<__nv_bfloat16*>(dq);
+    bp.dk = static_cast<__nv_bfloat16*>(dk);
+    bp.dv = static_cast<__nv_bfloat16*>(dv);
+    bp.rot_base = rope ? split_tab : nullptr;
+    bp.rot_row = rope ? split_tab + static_cast<size_t>((S + 31) / 32) * (D / 2) : nullptr;
+    bp.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const unsigned dot_blocks = static_cast<unsigned>((rows + 7) / 8);
+    if (D == 128)
+        attn::bwd_dot_kernel<128><<<dot_blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                static_cast<const __nv_bfloat16*>(dO), dlt, B, S, Hq);
+    else
+        attn::bwd_dot_kernel<64><<<dot_blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
+                                                               static_cast<const __nv_bfloat16*>(dO), dlt, B, S, Hq);
+    cudaError_t e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("backward row-reduction launch", e);
+    const int ntiles = (S + 127) / 128;
+    if (D == 128) {
+        if (causal) return rope ? launch_bwd<128, true, true>(bp, dev, ntiles, st) : launch_bwd<128, true, false>(bp, dev, ntiles, st);
+        return rope ? launch_bwd<128, false, true>(bp, dev, ntiles, st) : launch_bwd<128, false, false>(bp, dev, ntiles, st);
+    }
+    if (causal) return rope ? launch_bwd<64, true, true>(bp, dev, ntiles, st) : launch_bwd<64, true, false>(bp, dev, ntiles, st);
+    return rope ? launch_bwd<64, false, true>(bp, dev, ntiles, st) : launch_bwd<64, false, false>(bp, dev, ntiles, st);
+}
+
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
                                  float* cos_out, float* sin_out, int* win_out) {
     if (S < 1 || S > kMaxS || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
@@ -869,6 +979,12 @@ extern "C" void attn_release_cache(void) {
         cudaSetDevice(d);
         cudaFree(g_dec[d].buf);
         g_dec[d] = DecodeScratch();
+    }
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_bwd[d].buf == nullptr) continue;
+        cudaSetDevice(d);
+        cudaFree(g_bwd[d].buf);
+        g_bwd[d] = DecodeScratch();
     }
     g_split.clear();
     g_rope.clear();

@@ -1,0 +1,607 @@
+// Backward pass of the fused RoPE + causal attention forward ("AttnFuse",
+// sec. 4.4 Backward Pass: FlashAttention-2's split into a row-reduction
+// kernel, a dK/dV kernel and a dQ kernel, each writing its own output tiles,
+// with the softmax probabilities re-derived from the forward's per-row LSE).
+//
+// For a loss with gradient dO with respect to O:
+//   P_ij  = exp2(S_ij * log2(e)/sqrt(D) - LSE_i * log2(e)),  S = Q' K'^T on the
+//           rotated operands (rounded to fp16 as in the forward)
+//   Dlt_i = dO_i . O_i                            (bwd_dot_kernel)
+//   dS_ij = P_ij (dO_i . V_j - Dlt_i)
+//   dV_j  = sum_i P_ij dO_i,  dK'_j = sum_i dS_ij Q'_i / sqrt(D)   (bwd_dkdv_kernel)
+//   dQ'_i = sum_j dS_ij K'_j / sqrt(D)                              (bwd_dq_kernel)
+//   dQ_i  = R(i)^T dQ'_i,  dK_j = R(j)^T dK'_j  (the rotation run backwards)
+//
+// Both tile kernels follow the forward's GB300 structure: TMA loads into
+// 128-byte-swizzled shared memory, the RoPE warps rotate tiles in place, one
+// thread issues tcgen05 MMAs into TMEM, and one warpgroup (one thread per
+// TMEM lane) turns S and dP into P and dS in TMEM, which the next MMAs read
+// as their A operand.  Every wait is bounded.
+#pragma once
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+struct BwdParams {
+    FwdParams f;            // tm_q, tm_k, tm_v, the RoPE factor table, shape, scale, status, wait limit
+    CUtensorMap tm_do;      // dO [B][S][Hq][D] bf16, box {64, 1, 128, 1}, 128-byte swizzle
+    const float* lse;       // [B][Hq][S] natural log, from the forward
+    const float* dlt;       // [B][Hq][S] dO_i . O_i
+    __nv_bfloat16* dq;      // [B][S][Hq][D]
+    __nv_bfloat16* dk;      // [B][S][Hkv][D]
+    __nv_bfloat16* dv;      // [B][S][Hkv][D]
+    const float2* rot_base; // (cos, sin)(32*m*theta_r), [m][r] (RoPE only)
+    const float2* rot_row;  // (cos, sin)(rr*theta_r), [rr][r], rr < 32
+    float inv_sqrt_d;
+};
+
+// Dlt for every row: one warp per (b, s, h) row of O and dO; dlt is [B][H][S].
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dot_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dO, float* __restrict__ dlt,
+                                                      int B, int S, int H) {
+    const long long row = blockIdx.x * 8LL + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= static_cast<long long>(B) * S * H) return;
+    float acc = 0.f;
+    if constexpr (D == 128) {
+        const uint2 a = __ldg(reinterpret_cast<const uint2*>(o + row * D) + lane);
+        const uint2 b = __ldg(reinterpret_cast<const uint2*>(dO + row * D) + lane);
+        acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) + bf16_lo(a.y) * bf16_lo(b.y) +
+              bf16_hi(a.y) * bf16_hi(b.y);
+    } else {
+        const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(o + row * D) + lane);
+        const uint32_t b = __ldg(reinterpret_cast<const uint32_t*>(dO + row * D) + lane);
+        acc = bf16_lo(a) * bf16_lo(b) + bf16_hi(a) * bf16_hi(b);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+        const long long h = row % H, s = (row / H) % S, b = row / (static_cast<long long>(H) * S);
+        dlt[(b * H + h) * S + s] = acc;
+    }
+}
+
+// Warp roles of the two tile kernels (320 threads).
+constexpr int kBwdThreads = 320;
+constexpr int kBwdWarpRope = 4;   // warps 4-7
+constexpr int kBwdWarpTma = 8;
+constexpr int kBwdWarpMma = 9;
+
+// Shared memory of a tile kernel: two resident tiles, two stages of two streamed tiles, two
+// stages of 2 x 128 per-row floats, then barriers and the abort flag / TMEM slot.
+template <int D>
+struct BwdLayout {
+    static constexpr uint32_t kTile = 128u * D * 2u;
+    static constexpr uint32_t kRes0 = 0, kRes1 = kTile;
+    static constexpr uint32_t kStr0 = 2 * kTile;              // stage s: tiles at kStr0 + s * 2 * kTile (+ kTile)
+    static constexpr uint32_t kRows = 6 * kTile;              // stage s: 256 floats at kRows + s * 1024
+    static constexpr uint32_t kBars = kRows + 2048;
+    static constexpr uint32_t kMisc = kBars + 256;
+    static constexpr uint32_t kBytes = kMisc + 64;
+    static constexpr uint32_t kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
+};
+
+enum : int {
+    BB_RES_FULL = 0,  // resident tiles landed
+    BB_RES_ROT,       // resident RoPE tile rotated
+    BB_STR_FULL,      // [2] streamed tiles landed
+    BB_STR_ROT = BB_STR_FULL + 2,    // [2] streamed RoPE tile rotated
+    BB_STR_EMPTY = BB_STR_ROT + 2,   // [2] the MMAs reading the stage are done
+    BB_S_FULL = BB_STR_EMPTY + 2,    // S and dP of the iteration in TMEM
+    BB_P_FULL,        // P and dS written to TMEM
+    BB_ACC_FULL,      // last accumulation done
+    BB_DRAIN,
+    BB_NUM
+};
+static_assert(BB_NUM * 8 <= 256, "barrier block");
+
+// (cos, sin) of position pos for pairs r and r + 1 (r even), from the per-32-key factor tables.
+__device__ __forceinline__ void bwd_factor2(const BwdParams& p, int pos, int r, int half, float4& f) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p.rot_base + static_cast<size_t>(pos >> 5) * half + r));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p.rot_row + static_cast<size_t>(pos & 31) * half + r));
+    f = make_float4(a.x * b.x - a.y * b.y, a.y * b.x + a.x * b.y, a.z * b.z - a.w * b.w, a.w * b.z + a.z * b.w);
+}
+
+// Epilogue of one row held in TMEM columns [taddr, taddr + D): scale, rotate back by the row's
+// position (RoPE), round to bf16 and store D contiguous elements at dst.
+template <int D, bool ROPE>
+__device__ __forceinline__ void bwd_store_row(const BwdParams& p, uint32_t taddr, float scale, int pos, bool store,
+                                              __nv_bfloat16* dst) {
+    constexpr int kHalf = D / 2;
+#pragma unroll
+    for (int c0 = 0; c0 < kHalf; c0 += 32) {
+        uint32_t x[32], y[32];
+        tmem_load_32(taddr + c0, x);
+        tmem_load_32(taddr + kHalf + c0, y);
+        uint32_t px[16], py[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            float x0 = __uint_as_float(x[e]) * scale, x1 = __uint_as_float(x[e + 1]) * scale;
+            float y0 = __uint_as_float(y[e]) * scale, y1 = __uint_as_float(y[e + 1]) * scale;
+            if (ROPE && store) {  // rows past S have no table entry and are not stored
+                float4 f;
+                bwd_factor2(p, pos, c0 + e, kHalf, f);  // (cos, sin) of pairs c0+e, c0+e+1
+                const float a0 = x0 * f.x + y0 * f.y, b0 = -x0 * f.y + y0 * f.x;
+                const float a1 = x1 * f.z + y1 * f.w, b1 = -x1 * f.w + y1 * f.z;
+                x0 = a0;
+                y0 = b0;
+                x1 = a1;
+                y1 = b1;
+            }
+            px[e / 2] = pack_bf16x2(x0, x1);
+            py[e / 2] = pack_bf16x2(y0, y1);
+        }
+        if (store) {
+            uint4* dx = reinterpret_cast<uint4*>(dst + c0);
+            uint4* dy = reinterpret_cast<uint4*>(dst + kHalf + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dx[q] = make_uint4(px[4 * q], px[4 * q + 1], px[4 * q + 2], px[4 * q + 3]);
+                dy[q] = make_uint4(py[4 * q], py[4 * q + 1], py[4 * q + 2], py[4 * q + 3]);
+            }
+        }
+    }
+}
+
+// dK/dV kernel, one thread per key row: P^T = exp2(S^T c - LSE2_col) (0 where the query is
+// before the key) and dS^T = P^T (dP^T - Dlt_col), 32 columns at a time; P^T (bf16) overwrites
+// the S^T columns and dS^T (fp16 after RoPE, else bf16) the dP^T columns, two per column, never
+// a column still to be read.  Columns are queries q0 + c; c < lim is masked.
+template <bool ROPE, bool MASKED>
+__device__ __forceinline__ void bwd_ew_cols(uint32_t tS, uint32_t tdP, const float* ls, const float* dl, float c,
+                                            int lim) {
+#pragma unroll
+    for (int cc = 0; cc < 128; cc += 32) {
+        uint32_t rs[32], rd[32];
+        tmem_load_32(tS + cc, rs);
+        tmem_load_32(tdP + cc, rd);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const float2 l2 = *reinterpret_cast<const float2*>(ls + cc + e);
+            const float2 d2 = *reinterpret_cast<const float2*>(dl + cc + e);
+            float p0 = ex2_approx(__uint_as_float(rs[e]) * c - l2.x);
+            float p1 = ex2_approx(__uint_as_float(rs[e + 1]) * c - l2.y);
+            if (MASKED) {
+                if (cc + e < lim) p0 = 0.f;
+                if (cc + e + 1 < lim) p1 = 0.f;
+            }
+            const float s0 = p0 * (__uint_as_float(rd[e]) - d2.x);
+            const float s1 = p1 * (__uint_as_float(rd[e + 1]) - d2.y);
+            pp[e / 2] = pack_bf16x2(p0, p1);
+            pd[e / 2] = ROPE ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
+        }
+        tmem_store_16(tS + cc / 2, pp);
+        tmem_store_16(tdP + cc / 2, pd);
+    }
+}
+
+// dQ kernel, one thread per query row: dS = P (dP - Dlt_row) with P = exp2(S c - LSE2_row),
+// 0 for keys after the query (columns c > lim); dS overwrites the dP columns.
+template <bool ROPE, bool MASKED>
+__device__ __forceinline__ void bwd_ew_row(uint32_t tS, uint32_t tdP, float l2, float dl, float c, int lim) {
+#pragma unroll
+    for (int cc = 0; cc < 128; cc += 32) {
+        uint32_t rs[32], rd[32];
+        tmem_load_32(tS + cc, rs);
+        tmem_load_32(tdP + cc, rd);
+        uint32_t pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            float p0 = ex2_approx(__uint_as_float(rs[e]) * c - l2);
+            float p1 = ex2_approx(__uint_as_float(rs[e + 1]) * c - l2);
+            if (MASKED) {
+                if (cc + e > lim) p0 = 0.f;
+                if (cc + e + 1 > lim) p1 = 0.f;
+            }
+            const float s0 = p0 * (__uint_as_float(rd[e]) - dl);
+            const float s1 = p1 * (__uint_as_float(rd[e + 1]) - dl);
+            pd[e / 2] = ROPE ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
+        }
+        tmem_store_16(tdP + cc / 2, pd);
+    }
+}
+
+// One K-major 128 x D tile (D/64 column blocks of [128 rows][128 B]): the descriptor units of k-step kk.
+__device__ __forceinline__ uint32_t kmajor_units(int kk) {
+    return static_cast<uint32_t>((kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2);
+}
+
+__device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int code) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, code));
+}
+
+// Every issued MMA completes before TMEM is released (bounded).
+__device__ __forceinline__ void bwd_drain(uint32_t bar0, const WaitCtl& ctl) {
+    tc_commit(bar_at(bar0, BB_DRAIN));
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar_at(bar0, BB_DRAIN), 0)) {
+        if (global_timer_ns() - t0 > ctl.limit_ns) {
+            atomicOr(ctl.status, kStatusDrain);
+            break;
+        }
+    }
+}
+
+__device__ __forceinline__ void bwd_init_bars(uint32_t bar0) {
+    mbar_init(bar_at(bar0, BB_RES_FULL), 1);
+    mbar_init(bar_at(bar0, BB_RES_ROT), 128);
+    for (int s = 0; s < 2; ++s) {
+        mbar_init(bar_at(bar0, BB_STR_FULL + s), 1);
+        mbar_init(bar_at(bar0, BB_STR_ROT + s), 128);
+        mbar_init(bar_at(bar0, BB_STR_EMPTY + s), 1);
+    }
+    mbar_init(bar_at(bar0, BB_S_FULL), 1);
+    mbar_init(bar_at(bar0, BB_P_FULL), 128);
+    mbar_init(bar_at(bar0, BB_ACC_FULL), 1);
+    mbar_init(bar_at(bar0, BB_DRAIN), 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+}
+
+// dK and dV of one 128-key tile j of KV head g: CTA (b * Hkv + g, j) walks the query tiles
+// i >= j (all of them without the causal mask) of each of the group's query heads; the
+// heaviest tiles (small j) are launched first.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).
+template <int D, bool CAUSAL, bool ROPE>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sm = smem_addr(smg);
+    const uint32_t bar0 = sm + L::kBars;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smg + L::kMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smg + L::kMisc + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const FwdParams& f = p.f;
+    const int ntiles = (f.S + 127) / 128;
+    const int j = blockIdx.y;
+    const int b = blockIdx.x / f.Hkv, g = blockIdx.x % f.Hkv;
+    const int G = f.Hq / f.Hkv;
+    const int kv0 = j * 128;
+    const int i_lo = CAUSAL ? j : 0;
+    const int per_head = ntiles - i_lo;
+    const int iters = G * per_head;  // iteration it: head g*G + it / per_head, query tile i_lo + it % per_head
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        bwd_init_bars(bar0);
+    }
+    if (warp == kBwdWarpTma && lane == 0) {
+        tma_prefetch_desc(&f.tm_q);
+        tma_prefetch_desc(&f.tm_k);
+        tma_prefetch_desc(&f.tm_v);
+        tma_prefetch_desc(&p.tm_do);
+    }
+    if (warp == kBwdWarpMma) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, f.status, f.wait_limit_ns};
+
+    if (warp < 4) {
+        // ---- elementwise warpgroup: thread t owns key row kv0 + t (TMEM lane t)
+        const int t = threadIdx.x;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
+        const uint32_t tS = trow, tdP = trow + 128u, tdV = trow + 256u, tdK = trow + 256u + D;
+        const float c = f.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < iters && ok; ++it) {
+            const int s = it & 1;
+            const int q0 = (i_lo + it % per_head) * 128;
+            ok = bwd_wait(bar_at(bar0, BB_STR_FULL + s), (it >> 1) & 1, ctl, kStatusSoftmax);  // per-column values
+            if (!ok) break;
+            ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
+            if (!ok) break;
+            tc_fence_after();
+            const float* ls = reinterpret_cast<const float*>(smg + L::kRows + s * 1024);
+            const int lim = kv0 + t - q0;  // query columns c < lim precede the key
+            if (CAUSAL && __any_sync(0xffffffffu, lim > 0))
+                bwd_ew_cols<ROPE, true>(tS, tdP, ls, ls + 128, c, lim);
+            else
+                bwd_ew_cols<ROPE, false>(tS, tdP, ls, ls + 128, c, lim);
+            tmem_store_wait();
+            tc_fence_before();
+            mbar_arrive(bar_at(bar0, BB_P_FULL));
+        }
+        if (ok && bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax)) {
+            tc_fence_after();
+            const int key = kv0 + t;
+            const bool store = key < f.S;
+            const size_t off = ((static_cast<size_t>(b) * f.S + (store ? key : 0)) * f.Hkv + g) * D;
+            bwd_store_row<D, false>(p, tdV, 1.0f, key, store, p.dv + off);
+            bwd_store_row<D, ROPE>(p, tdK, p.inv_sqrt_d, key, store, p.dk + off);
+        }
+    } else if (warp < kBwdWarpTma) {
+        // ---- RoPE warps: the resident K tile once, then each streamed Q tile
+        if (ROPE) {
+            const int t = threadIdx.x - kBwdWarpRope * 32;
+            RopeConsts k;
+            rope_load_consts<D>(f, t, k);
+            uint64_t cb[4], sb[4];
+            rope_load_base<D>(f, j, t, cb, sb);
+            bool ok = bwd_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusRope);
+            if (ok) {
+                rope_rotate_tile<D, false>(smg + L::kRes0, k, cb, sb, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_at(bar0, BB_RES_ROT));
+            }
+            for (int it = 0; it < iters && ok; ++it) {
+                const int s = it & 1;
+                rope_load_base<D>(f, i_lo + it % per_head, t, cb, sb);
+                ok = bwd_wait(bar_at(bar0, BB_STR_FULL + s), (it >> 1) & 1, ctl, kStatusRope);
+                if (!ok) break;
+                rope_rotate_tile<D, false>(smg + L::kStr0 + s * 2 * L::kTile, k, cb, sb, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_at(bar0, BB_STR_ROT + s));
+            }
+        }
+    } else if (warp == kBwdWarpTma) {
+        // ---- producer: K and V once; per iteration Q and dO by TMA, LSE2 and Dlt by the lanes
+        if (lane == 0) {
+            const uint32_t rb = bar_at(bar0, BB_RES_FULL);
+            mbar_arrive_expect_tx(rb, 2 * L::kTile);
+#pragma unroll
+            for (int sub = 0; sub < D / 64; ++sub) {
+                tma_load_4d(sm + L::kRes0 + sub * kSubTileBytes, &f.tm_k, rb, sub * 64, g, kv0, b);
+                tma_load_4d(sm + L::kRes1 + sub * kSubTileBytes, &f.tm_v, rb, sub * 64, g, kv0, b);
+            }
+        }
+        for (int it = 0; it < iters; ++it) {
+            const int s = it & 1, n = it >> 1;
+            const int h = g * G + it / per_head;
+            const int q0 = (i_lo + it % per_head) * 128;
+            if (n >= 1 && !bwd_wait(bar_at(bar0, BB_STR_EMPTY + s), (n - 1) & 1, ctl, kStatusProducer)) break;
+            float* ls = reinterpret_cast<float*>(smg + L::kRows + s * 1024);
+            const float* lse_row = p.lse + (static_cast<size_t>(b) * f.Hq + h) * f.S;
+            const float* dlt_row = p.dlt + (static_cast<size_t>(b) * f.Hq + h) * f.S;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = q0 + lane + 32 * q;
+                const bool in = r < f.S;
+                ls[lane + 32 * q] = in ? lse_row[r] * 1.4426950408889634f : INFINITY;  // padded queries get P = 0
+                ls[128 + lane + 32 * q] = in ? dlt_row[r] : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t fb = bar_at(bar0, BB_STR_FULL + s);
+                mbar_arrive_expect_tx(fb, 2 * L::kTile);
+                const uint32_t dq = sm + L::kStr0 + s * 2 * L::kTile;
+#pragma unroll
+                for (int sub = 0; sub < D / 64; ++sub) {
+                    tma_load_4d(dq + sub * kSubTileBytes, &f.tm_q, fb, sub * 64, h, q0, b);
+                    tma_load_4d(dq + L::kTile + sub * kSubTileBytes, &p.tm_do, fb, sub * 64, h, q0, b);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == kBwdWarpMma && lane == 0) {
+        // ---- MMA issuer
+        // S^T = K Q^T (A = K tile, B = Q tile, both K-major; fp16 after RoPE) and dP^T = V dO^T (bf16)
+        const uint32_t kIdescS = umma_idesc_f16(ROPE ? 0u : 1u, 0u, 128, 128);
+        constexpr uint32_t kIdescDP = umma_idesc_f16(1u, 0u, 128, 128);
+        // dV += P^T dO and dK += dS^T Q: A from TMEM, B = the [queries][D] tile, MN-major
+        constexpr uint32_t kIdescDV = umma_idesc_f16(1u, 1u, 128, D);
+        const uint32_t kIdescDK = umma_idesc_f16(ROPE ? 0u : 1u, 1u, 128, D);
+        const uint32_t tS = tmem, tdP = tmem + 128u, tdV = tmem + 256u, tdK = tmem + 256u + D;
+        const uint64_t kdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
+        const uint64_t vdesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
+        bool ok = mbar_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
+        if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
+        for (int it = 0; it < iters && ok; ++it) {
+            const int s = it & 1, n = it >> 1;
+            ok = mbar_wait(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
+            if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t qa = sm + L::kStr0 + s * 2 * L::kTile, da = qa + L::kTile;
+            const uint64_t qdesc = sw128_desc(qa, 16u, 1024u), ddesc = sw128_desc(da, 16u, 1024u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tS, desc_advance(kdesc, kmajor_units(kk)), desc_advance(qdesc, kmajor_units(kk)), kIdescS,
+                        kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tdP, desc_advance(vdesc, kmajor_units(kk)), desc_advance(ddesc, kmajor_units(kk)), kIdescDP,
+                        kk > 0 ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_S_FULL));
+            ok = mbar_wait(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t dmn = sw128_desc(da, kSubTileBytes, 1024u), qmn = sw128_desc(qa, kSubTileBytes, 1024u);
+            // 16 queries per k-step: 2048 bytes of the tile, 8 TMEM columns of P^T / dS^T
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tdV, tS + kk * 8u, desc_advance(dmn, kk * 128u), kIdescDV, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tdK, tdP + kk * 8u, desc_advance(qmn, kk * 128u), kIdescDK, (it > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
+        }
+        if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));
+        bwd_drain(bar0, ctl);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// dQ of one 128-row query tile i of head h: CTA (b * Hq + h, y) walks the key tiles j <= i (all
+// of them without the causal mask); with the mask the heaviest tiles go first (i = ntiles-1-y).
+// TMEM: S [0,128), dP [128,256), dQ [256, 256+D).
+template <int D, bool CAUSAL, bool ROPE>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sm = smem_addr(smg);
+    const uint32_t bar0 = sm + L::kBars;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smg + L::kMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smg + L::kMisc + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const FwdParams& f = p.f;
+    const int ntiles = (f.S + 127) / 128;
+    const int i = CAUSAL ? ntiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
+    const int b = blockIdx.x / f.Hq, h = blockIdx.x % f.Hq;
+    const int g = h / (f.Hq / f.Hkv);
+    const int q0 = i * 128;
+    const int iters = CAUSAL ? i + 1 : ntiles;  // iteration it: key tile it
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        bwd_init_bars(bar0);
+    }
+    if (warp == kBwdWarpTma && lane == 0) {
+        tma_prefetch_desc(&f.tm_q);
+        tma_prefetch_desc(&f.tm_k);
+        tma_prefetch_desc(&f.tm_v);
+        tma_prefetch_desc(&p.tm_do);
+    }
+    if (warp == kBwdWarpMma) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, f.status, f.wait_limit_ns};
+
+    if (warp < 4) {
+        // ---- elementwise warpgroup: thread t owns query row q0 + t (TMEM lane t)
+        const int t = threadIdx.x;
+        const int row = q0 + t;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
+        const uint32_t tS = trow, tdP = trow + 128u, tdQ = trow + 256u;
+        const float c = f.scale_log2;
+        const size_t rix = (static_cast<size_t>(b) * f.Hq + h) * f.S + (row < f.S ? row : 0);
+        const float l2 = row < f.S ? p.lse[rix] * 1.4426950408889634f : INFINITY;  // padded rows get P = 0
+        const float dl = row < f.S ? p.dlt[rix] : 0.f;
+        bool ok = true;
+        for (int it = 0; it < iters && ok; ++it) {
+            ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
+            if (!ok) break;
+            tc_fence_after();
+            const int lim = q0 + t - it * 128;  // key columns c > lim follow the query
+            if (CAUSAL && __any_sync(0xffffffffu, lim < 127))
+                bwd_ew_row<ROPE, true>(tS, tdP, l2, dl, c, lim);
+            else
+                bwd_ew_row<ROPE, false>(tS, tdP, l2, dl, c, lim);
+            tmem_store_wait();
+            tc_fence_before();
+            mbar_arrive(bar_at(bar0, BB_P_FULL));
+        }
+        if (ok && bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax)) {
+            tc_fence_after();
+            const bool store = row < f.S;
+            const size_t off = ((static_cast<size_t>(b) * f.S + (store ? row : 0)) * f.Hq + h) * D;
+            bwd_store_row<D, ROPE>(p, tdQ, p.inv_sqrt_d, row, store, p.dq + off);
+        }
+    } else if (warp < kBwdWarpTma) {
+        // ---- RoPE warps: the resident Q tile once, then each streamed K tile
+        if (ROPE) {
+            const int t = threadIdx.x - kBwdWarpRope * 32;
+            RopeConsts k;
+            rope_load_consts<D>(f, t, k);
+            uint64_t cb[4], sb[4];
+            rope_load_base<D>(f, i, t, cb, sb);
+            bool ok = bwd_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusRope);
+            if (ok) {
+                rope_rotate_tile<D, false>(smg + L::kRes0, k, cb, sb, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_at(bar0, BB_RES_ROT));
+            }
+            for (int it = 0; it < iters && ok; ++it) {
+                const int s = it & 1;
+                rope_load_base<D>(f, it, t, cb, sb);
+                ok = bwd_wait(bar_at(bar0, BB_STR_FULL + s), (it >> 1) & 1, ctl, kStatusRope);
+                if (!ok) break;
+                rope_rotate_tile<D, false>(smg + L::kStr0 + s * 2 * L::kTile, k, cb, sb, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_at(bar0, BB_STR_ROT + s));
+            }
+        }
+    } else if (warp == kBwdWarpTma) {
+        // ---- producer: Q and dO once; per iteration K and V
+        if (lane == 0) {
+            const uint32_t rb = bar_at(bar0, BB_RES_FULL);
+            mbar_arrive_expect_tx(rb, 2 * L::kTile);
+#pragma unroll
+            for (int sub = 0; sub < D / 64; ++sub) {
+                tma_load_4d(sm + L::kRes0 + sub * kSubTileBytes, &f.tm_q, rb, sub * 64, h, q0, b);
+                tma_load_4d(sm + L::kRes1 + sub * kSubTileBytes, &p.tm_do, rb, sub * 64, h, q0, b);
+            }
+            for (int it = 0; it < iters; ++it) {
+                const int s = it & 1, n = it >> 1;
+                if (n >= 1 && !mbar_wait(bar_at(bar0, BB_STR_EMPTY + s), (n - 1) & 1, ctl, kStatusProducer)) break;
+                const uint32_t fb = bar_at(bar0, BB_STR_FULL + s);
+                mbar_arrive_expect_tx(fb, 2 * L::kTile);
+                const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile;
+#pragma unroll
+                for (int sub = 0; sub < D / 64; ++sub) {
+                    tma_load_4d(ka + sub * kSubTileBytes, &f.tm_k, fb, sub * 64, g, it * 128, b);
+                    tma_load_4d(ka + L::kTile + sub * kSubTileBytes, &f.tm_v, fb, sub * 64, g, it * 128, b);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kBwdWarpMma && lane == 0) {
+        // ---- MMA issuer: S = Q K^T, dP = dO V^T (K-major operands), then dQ += dS K (K tile MN-major)
+        const uint32_t kIdescS = umma_idesc_f16(ROPE ? 0u : 1u, 0u, 128, 128);
+        constexpr uint32_t kIdescDP = umma_idesc_f16(1u, 0u, 128, 128);
+        const uint32_t kIdescDQ = umma_idesc_f16(ROPE ? 0u : 1u, 1u, 128, D);
+        const uint32_t tS = tmem, tdP = tmem + 128u, tdQ = tmem + 256u;
+        const uint64_t qdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
+        const uint64_t ddesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
+        bool ok = mbar_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
+        if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
+        for (int it = 0; it < iters && ok; ++it) {
+            const int s = it & 1, n = it >> 1;
+            ok = mbar_wait(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
+            if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile, va = ka + L::kTile;
+            const uint64_t kdesc = sw128_desc(ka, 16u, 1024u), vdesc = sw128_desc(va, 16u, 1024u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
+                        kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tdP, desc_advance(ddesc, kmajor_units(kk)), desc_advance(vdesc, kmajor_units(kk)), kIdescDP,
+                        kk > 0 ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_S_FULL));
+            ok = mbar_wait(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t kmn = sw128_desc(ka, kSubTileBytes, 1024u);
+            // 16 keys per k-step: 2048 bytes of K, 8 TMEM columns of dS
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tdQ, tdP + kk * 8u, desc_advance(kmn, kk * 128u), kIdescDQ, (it > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
+        }
+        if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));
+        bwd_drain(bar0, ctl);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace attn

@@ -205,6 +205,30 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
                 int B, int Hq, int Hkv, int S, int D, double rope_base, double window_k, void* stream);
 
 /*
+ * attn_bwd — gradients of the attention forward: dQ, dK, dV for an upstream
+ * gradient dO ("AttnFuse: A Composable DSL for Compiling Attentions to Fused
+ * GPU Kernels", sec. 4.4 Backward Pass: a row-reduction kernel, a dK/dV
+ * kernel and a dQ kernel, each writing its own output tiles, with the
+ * probabilities re-derived from the forward's per-row LSE).
+ *   q, k, v  bf16 device, the forward's inputs (BSHD, K and V not rotated).
+ *   o, lse   the forward's outputs: o bf16 [B][S][Hq][D], lse float32
+ *            [B][Hq][S] (natural log), both required.
+ *   dO       bf16 device [B][S][Hq][D].
+ *   dq       bf16 device output [B][S][Hq][D]; dk, dv bf16 [B][S][Hkv][D]
+ *            (a KV head's gradients sum over its query heads).
+ *   B, Hq, Hkv, S, D, causal, rope_base   as attn_fwd; the window is not
+ *            supported here.
+ * dS = P (dP - dO.O) is rounded to fp16 for the products with the rotated
+ * fp16 Q and K (bf16 without RoPE), P to bf16 for dV; accumulation in fp32.
+ * Asynchronous on `stream`.  The library keeps a scratch of B*Hq*S floats
+ * (dO.O per row) and the rotation tables until attn_release_cache().
+ * Errors: as attn_fwd (ATTN_ERR_NULL also for dO, lse, dq, dk, dv).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+             void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+             void* stream);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

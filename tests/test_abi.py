@@ -19,7 +19,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
     assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated",
-                          "attn_decode", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
+                          "attn_decode", "attn_bwd", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for n in names:
@@ -90,6 +90,21 @@ def test_decode_checks_arguments_on_the_host(lib):
     assert call(Hq=66, Hkv=2) == E["ATTN_ERR_UNSUPPORTED"]  # more than 32 query heads per KV head
     assert call(base=0.0, win=1.0) == E["ATTN_ERR_UNSUPPORTED"]  # window needs RoPE
     assert call(k=24) == E["ATTN_ERR_ALIGN"]
+
+
+def test_backward_checks_arguments_on_the_host(lib):
+    E = attn.ATTN_STATUS
+    call = lambda **kw: lib.attn_bwd(*(kw.get(n, 16) for n in ("q", "k", "v", "o", "dO", "lse", "dq", "dk", "dv")),
+                                      kw.get("B", 1), kw.get("Hq", 2), kw.get("Hkv", 2), kw.get("S", 128),
+                                      kw.get("D", 128), kw.get("causal", 1), kw.get("base", 1e4), None)
+    assert call(dO=0) == E["ATTN_ERR_NULL"]
+    assert call(lse=0) == E["ATTN_ERR_NULL"]
+    assert call(dv=0) == E["ATTN_ERR_NULL"]
+    assert call(D=96) == E["ATTN_ERR_SHAPE"]
+    assert call(Hq=6, Hkv=4) == E["ATTN_ERR_SHAPE"]
+    assert call(causal=2) == E["ATTN_ERR_UNSUPPORTED"]
+    assert call(dq=24) == E["ATTN_ERR_ALIGN"]
+    assert call(lse=18) == E["ATTN_ERR_ALIGN"]
 
 
 def test_rope_tables_are_float64_cos_sin_rounded(lib):

@@ -300,3 +300,49 @@ def test_decode_matches_oracle_last_row(B, Hq, Hkv, S, D, base, wk):
 @pytest.mark.parametrize("wk", [4.0, None])
 def test_decode_long_cache_s131072(wk):
     _decode_check(1, 32, 8, 131072, 128, 500000.0, wk, seed=909)
+
+
+# ---------------------------------------------------------------- backward
+# Gradients are compared per tensor, relative to the reference's scale: the
+# bf16 outputs alone carry up to 2^-9 = 1.95e-3 of it, and P enters dV in bf16
+# and dS enters dQ/dK in fp16 (bf16 without RoPE).  Measured on GB300: at most
+# 4.1e-3 (max) and 2.4e-3 (mean) over the cases below; the gate keeps about a
+# factor 2.5.  A reference that is exactly zero (a cache of one key gives
+# dS = 0) is held to 1e-3 of an absolute unit scale.
+BWD_MAX, BWD_MEAN = 1e-2, 5e-3
+
+BWD = [
+    # B, Hq, Hkv, S, D, causal, rope_base
+    (1, 2, 2, 128, 64, True, 10000.0),
+    (2, 4, 2, 300, 128, True, 10000.0),    # GQA, ragged tail
+    (1, 2, 2, 256, 128, True, None),       # RoPE off: bf16 operands throughout
+    (1, 2, 1, 200, 64, False, 500000.0),   # full attention, group of 2
+    (2, 3, 1, 129, 128, True, 10000.0),    # group of 3, one key past a tile
+    (1, 2, 2, 1, 128, True, 10000.0),      # S = 1
+    (1, 4, 4, 1024, 128, True, 10000.0),   # eight tiles per head
+]
+
+
+def _check_grad(got, ref, tag):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.isfinite(got).all(), f"{tag}: non-finite gradient"
+    err = np.abs(got - ref)
+    scale_max, scale_mean = max(np.abs(ref).max(), 1e-3), max(np.abs(ref).mean(), 1e-3)
+    assert err.max() <= BWD_MAX * scale_max, f"{tag}: max err {err.max():.3e} vs scale {scale_max:.3e}"
+    assert err.mean() <= BWD_MEAN * scale_mean, f"{tag}: mean err {err.mean():.3e} vs scale {scale_mean:.3e}"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base", BWD)
+def test_backward_matches_oracle(B, Hq, Hkv, S, D, causal, base):
+    """attn_bwd on the GPU forward's own O and LSE against the float64 chain rule."""
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=600 + S)
+    dO = si.bshd_bf16(601 + S, 9, B, S, Hq, D)
+    qd, kd, vd, dOd = _dev(q), _dev(k), _dev(v), _dev(dO)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=causal, rope_base=base)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dOd, causal=causal, rope_base=base)
+    attn.attn_check()
+    rq, rk, rv = oracle.attn_bwd(q, k, v, dO, causal=causal, rope_base=base)
+    tag = f"B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal{causal} base{base}"
+    _check_grad(dv.float().cpu().numpy(), rv, tag + " dV")
+    _check_grad(dk.float().cpu().numpy(), rk, tag + " dK")
+    _check_grad(dq.float().cpu().numpy(), rq, tag + " dQ")

@@ -16,7 +16,9 @@
 // 128-byte-swizzled shared memory, the RoPE warps rotate tiles in place, one
 // thread issues tcgen05 MMAs into TMEM, and one warpgroup (one thread per
 // TMEM lane) turns S and dP into P and dS in TMEM, which the next MMAs read
-// as their A operand.  Every wait is bounded.
+// as their A operand.  Two warpgroups share that work, one per half of the
+// 128 columns, each writing its packed P / dS inside its own half.  Every
+// wait is bounded.
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -63,11 +65,13 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const __nv_bfloat16* __res
     }
 }
 
-// Warp roles of the two tile kernels (320 threads).
-constexpr int kBwdThreads = 320;
-constexpr int kBwdWarpRope = 4;   // warps 4-7
-constexpr int kBwdWarpTma = 8;
-constexpr int kBwdWarpMma = 9;
+// Warp roles of the two tile kernels (448 threads): warps 0-7 elementwise (two warpgroups, one per
+// half of the columns), 8-11 RoPE, 12 TMA, 13 MMA.
+constexpr int kBwdThreads = 448;
+constexpr int kBwdEw = 256;
+constexpr int kBwdWarpRope = 8;
+constexpr int kBwdWarpTma = 12;
+constexpr int kBwdWarpMma = 13;
 
 // Shared memory of a tile kernel: two resident tiles, two stages of two streamed tiles, two
 // stages of 2 x 128 per-row floats, then barriers and the abort flag / TMEM slot.
@@ -108,10 +112,11 @@ __device__ __forceinline__ void bwd_factor2(const BwdParams& p, int pos, int r, 
 // position (RoPE), round to bf16 and store D contiguous elements at dst.
 template <int D, bool ROPE>
 __device__ __forceinline__ void bwd_store_row(const BwdParams& p, uint32_t taddr, float scale, int pos, bool store,
-                                              __nv_bfloat16* dst) {
+                                              __nv_bfloat16* dst, int c_begin = 0, int c_end = D / 2) {
     constexpr int kHalf = D / 2;
 #pragma unroll
     for (int c0 = 0; c0 < kHalf; c0 += 32) {
+        if (c0 < c_begin || c0 >= c_end) continue;  // pairs [c_begin, c_end) of this thread's share
         uint32_t x[32], y[32];
         tmem_load_32(taddr + c0, x);
         tmem_load_32(taddr + kHalf + c0, y);
@@ -145,15 +150,16 @@ __device__ __forceinline__ void bwd_store_row(const BwdParams& p, uint32_t taddr
     }
 }
 
-// dK/dV kernel, one thread per key row: P^T = exp2(S^T c - LSE2_col) (0 where the query is
-// before the key) and dS^T = P^T (dP^T - Dlt_col), 32 columns at a time; P^T (bf16) overwrites
-// the S^T columns and dS^T (fp16 after RoPE, else bf16) the dP^T columns, two per column, never
-// a column still to be read.  Columns are queries q0 + c; c < lim is masked.
+// dK/dV kernel, one thread per key row and half of the columns (64 queries from tS, tdP): P^T =
+// exp2(S^T c - LSE2_col) (0 where the query is before the key) and dS^T = P^T (dP^T - Dlt_col),
+// 32 columns at a time; P^T (bf16) overwrites the half's S^T columns and dS^T (fp16 after RoPE,
+// else bf16) its dP^T columns, two per column, never a column still to be read.  Column c is
+// query q0 + c; c < lim is masked.
 template <bool ROPE, bool MASKED>
 __device__ __forceinline__ void bwd_ew_cols(uint32_t tS, uint32_t tdP, const float* ls, const float* dl, float c,
                                             int lim) {
 #pragma unroll
-    for (int cc = 0; cc < 128; cc += 32) {
+    for (int cc = 0; cc < 64; cc += 32) {
         uint32_t rs[32], rd[32];
         tmem_load_32(tS + cc, rs);
         tmem_load_32(tdP + cc, rd);
@@ -178,12 +184,13 @@ __device__ __forceinline__ void bwd_ew_cols(uint32_t tS, uint32_t tdP, const flo
     }
 }
 
-// dQ kernel, one thread per query row: dS = P (dP - Dlt_row) with P = exp2(S c - LSE2_row),
-// 0 for keys after the query (columns c > lim); dS overwrites the dP columns.
+// dQ kernel, one thread per query row and half of the columns (64 keys): dS = P (dP - Dlt_row)
+// with P = exp2(S c - LSE2_row), 0 for keys after the query (columns c > lim); dS overwrites the
+// half's dP columns.
 template <bool ROPE, bool MASKED>
 __device__ __forceinline__ void bwd_ew_row(uint32_t tS, uint32_t tdP, float l2, float dl, float c, int lim) {
 #pragma unroll
-    for (int cc = 0; cc < 128; cc += 32) {
+    for (int cc = 0; cc < 64; cc += 32) {
         uint32_t rs[32], rd[32];
         tmem_load_32(tS + cc, rs);
         tmem_load_32(tdP + cc, rd);
@@ -203,6 +210,10 @@ __device__ __forceinline__ void bwd_ew_row(uint32_t tS, uint32_t tdP, float l2, 
         tmem_store_16(tdP + cc / 2, pd);
     }
 }
+
+// TMEM column of k-step kk (16 rows of the streamed tile) of packed P / dS: each half of 64
+// columns keeps its packed values in its own first 32 columns.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint32_t>((kk / 4) * 64 + (kk % 4) * 8); }
 
 // One K-major 128 x D tile (D/64 column blocks of [128 rows][128 B]): the descriptor units of k-step kk.
 __device__ __forceinline__ uint32_t kmajor_units(int kk) {
@@ -234,7 +245,7 @@ __device__ __forceinline__ void bwd_init_bars(uint32_t bar0) {
         mbar_init(bar_at(bar0, BB_STR_EMPTY + s), 1);
     }
     mbar_init(bar_at(bar0, BB_S_FULL), 1);
-    mbar_init(bar_at(bar0, BB_P_FULL), 128);
+    mbar_init(bar_at(bar0, BB_P_FULL), kBwdEw);
     mbar_init(bar_at(bar0, BB_ACC_FULL), 1);
     mbar_init(bar_at(bar0, BB_DRAIN), 1);
     fence_barrier_init();
@@ -285,9 +296,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, f.status, f.wait_limit_ns};
 
-    if (warp < 4) {
-        // ---- elementwise warpgroup: thread t owns key row kv0 + t (TMEM lane t)
-        const int t = threadIdx.x;
+    if (warp < 8) {
+        // ---- elementwise warpgroups: thread t owns key row kv0 + t (TMEM lane t), columns 64 half ..
+        const int t = threadIdx.x % 128, half = threadIdx.x / 128;
         const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const uint32_t tS = trow, tdP = trow + 128u, tdV = trow + 256u, tdK = trow + 256u + D;
         const float c = f.scale_log2;
@@ -300,12 +311,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
             if (!ok) break;
             tc_fence_after();
-            const float* ls = reinterpret_cast<const float*>(smg + L::kRows + s * 1024);
-            const int lim = kv0 + t - q0;  // query columns c < lim precede the key
+            const float* ls = reinterpret_cast<const float*>(smg + L::kRows + s * 1024) + 64 * half;
+            const int lim = kv0 + t - (q0 + 64 * half);  // query columns c < lim precede the key
+            const uint32_t hS = tS + 64u * half, hdP = tdP + 64u * half;
             if (CAUSAL && __any_sync(0xffffffffu, lim > 0))
-                bwd_ew_cols<ROPE, true>(tS, tdP, ls, ls + 128, c, lim);
+                bwd_ew_cols<ROPE, true>(hS, hdP, ls, ls + 128, c, lim);
             else
-                bwd_ew_cols<ROPE, false>(tS, tdP, ls, ls + 128, c, lim);
+                bwd_ew_cols<ROPE, false>(hS, hdP, ls, ls + 128, c, lim);
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
@@ -315,8 +327,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             const int key = kv0 + t;
             const bool store = key < f.S;
             const size_t off = ((static_cast<size_t>(b) * f.S + (store ? key : 0)) * f.Hkv + g) * D;
-            bwd_store_row<D, false>(p, tdV, 1.0f, key, store, p.dv + off);
-            bwd_store_row<D, ROPE>(p, tdK, p.inv_sqrt_d, key, store, p.dk + off);
+            if (half == 0)
+                bwd_store_row<D, false>(p, tdV, 1.0f, key, store, p.dv + off);
+            else
+                bwd_store_row<D, ROPE>(p, tdK, p.inv_sqrt_d, key, store, p.dk + off);
         }
     } else if (warp < kBwdWarpTma) {
         // ---- RoPE warps: the resident K tile once, then each streamed Q tile
@@ -418,10 +432,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             // 16 queries per k-step: 2048 bytes of the tile, 8 TMEM columns of P^T / dS^T
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tdV, tS + kk * 8u, desc_advance(dmn, kk * 128u), kIdescDV, (it > 0 || kk > 0) ? 1u : 0u);
+                umma_ts(tdV, tS + packed_col(kk), desc_advance(dmn, kk * 128u), kIdescDV, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tdK, tdP + kk * 8u, desc_advance(qmn, kk * 128u), kIdescDK, (it > 0 || kk > 0) ? 1u : 0u);
+                umma_ts(tdK, tdP + packed_col(kk), desc_advance(qmn, kk * 128u), kIdescDK, (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
         }
         if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));
@@ -477,9 +491,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, f.status, f.wait_limit_ns};
 
-    if (warp < 4) {
-        // ---- elementwise warpgroup: thread t owns query row q0 + t (TMEM lane t)
-        const int t = threadIdx.x;
+    if (warp < 8) {
+        // ---- elementwise warpgroups: thread t owns query row q0 + t (TMEM lane t), columns 64 half ..
+        const int t = threadIdx.x % 128, half = threadIdx.x / 128;
         const int row = q0 + t;
         const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const uint32_t tS = trow, tdP = trow + 128u, tdQ = trow + 256u;
@@ -492,11 +506,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
             if (!ok) break;
             tc_fence_after();
-            const int lim = q0 + t - it * 128;  // key columns c > lim follow the query
-            if (CAUSAL && __any_sync(0xffffffffu, lim < 127))
-                bwd_ew_row<ROPE, true>(tS, tdP, l2, dl, c, lim);
+            const int lim = q0 + t - (it * 128 + 64 * half);  // key columns c > lim follow the query
+            const uint32_t hS = tS + 64u * half, hdP = tdP + 64u * half;
+            if (CAUSAL && __any_sync(0xffffffffu, lim < 63))
+                bwd_ew_row<ROPE, true>(hS, hdP, l2, dl, c, lim);
             else
-                bwd_ew_row<ROPE, false>(tS, tdP, l2, dl, c, lim);
+                bwd_ew_row<ROPE, false>(hS, hdP, l2, dl, c, lim);
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
@@ -505,7 +520,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             tc_fence_after();
             const bool store = row < f.S;
             const size_t off = ((static_cast<size_t>(b) * f.S + (store ? row : 0)) * f.Hq + h) * D;
-            bwd_store_row<D, ROPE>(p, tdQ, p.inv_sqrt_d, row, store, p.dq + off);
+            // each warpgroup stores its share of the row's pairs (all of them at D = 64: one share)
+            if (D == 128 || half == 0)
+                bwd_store_row<D, ROPE>(p, tdQ, p.inv_sqrt_d, row, store, p.dq + off, D == 128 ? 32 * half : 0,
+                                       D == 128 ? 32 * half + 32 : D / 2);
         }
     } else if (warp < kBwdWarpTma) {
         // ---- RoPE warps: the resident Q tile once, then each streamed K tile
@@ -589,7 +607,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             // 16 keys per k-step: 2048 bytes of K, 8 TMEM columns of dS
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tdQ, tdP + kk * 8u, desc_advance(kmn, kk * 128u), kIdescDQ, (it > 0 || kk > 0) ? 1u : 0u);
+                umma_ts(tdQ, tdP + packed_col(kk), desc_advance(kmn, kk * 128u), kIdescDQ, (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
         }
         if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));

@@ -452,6 +452,58 @@ def run_decode(args, w, rank, world, local_rank):
     }
 
 
+# --------------------------------------------------------------------- backward
+def run_backward(args, w, rank, world, local_rank):
+    """One step = one attn_bwd call (dO.O rows, dK/dV, dQ) on the forward's own O and LSE."""
+    import torch
+    import attention_causal_attn_gb300 as attn
+    attn.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if w["window_k"]:
+        raise SystemExit("the backward has no window: pass --window-k 0")
+    B, Hq, Hkv, S, D = w["B"], w["Hq"], w["Hkv"], w["S"], w["D"]
+    q_h, k_h, v_h = si.make_qkv(B, Hq, Hkv, S, D, outliers=w["outliers"], seed=replica_seed(rank))
+    do_h = si.bshd_bf16(replica_seed(rank), 9, B, S, Hq, D)
+    q, k, v, dO = (torch.from_numpy(x).view(torch.bfloat16).to(dev) for x in (q_h, k_h, v_h, do_h))
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(causal=w["causal"], rope_base=w["rope_base"], stream=stream)
+    o, lse = attn.attn_fwd(q, k, v, **kw)
+    for _ in range(max(args.warmup, 3)):
+        attn.attn_bwd(q, k, v, o, lse, dO, **kw)
+    attn.attn_check(stream=stream, device=dev)
+    times = []
+    with ClockSampler(local_rank) as clocks:
+        for _ in range(args.steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.attn_bwd(q, k, v, o, lse, dO, **kw)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+    attn.attn_check(stream=stream, device=dev)
+    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    # useful backward work: 2.5 x the forward's 2*B*Hq*S^2*D causal FLOPs (dV, dP, dQ, dK and the
+    # recomputed S); the kernels execute 7/5 of it, S and dP being formed in both tile kernels
+    flops = 2.5 * 2.0 * B * Hq * S * S * D * (1.0 if w["causal"] else 2.0)
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks, _ = load_peaks()
+    cfg = workload_config(args.workload, w)
+    cfg["step"] = "backward: dO.O rows, dK/dV kernel, dQ kernel on the forward's O and LSE"
+    cfg["l2"] = "inputs larger than L2" if 4 * q.numel() * 2 > (256 << 20) else "inputs may stay in L2 between steps"
+    return {
+        "metric": "attention backward TFLOP/s", "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": float(peaks["bf16_tflops"]),
+                     "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4), "traffic": None,
+                     "kernel": "bwd_dot_kernel + bwd_dkdv_kernel + bwd_dq_kernel",
+                     "algorithmic": "5*B*Hq*S^2*D useful causal FLOPs per step, median step time"},
+        "gpu_launches": 3 * args.steps, "clocks": clocks.summary(),
+    }
+
+
 # --------------------------------------------------------------------- reference arm
 def run_reference(args, w, rank):
     if rank != 0:
@@ -500,6 +552,8 @@ def main():
     ap.add_argument("--seq", type=int, default=None, help="override the workload's sequence length")
     ap.add_argument("--decode", action="store_true",
                     help="time one decode step (attn_decode) on the workload's cache shape instead of the prefill")
+    ap.add_argument("--backward", action="store_true",
+                    help="time one backward step (attn_bwd) on the workload instead of the forward")
     ap.add_argument("--l2-fetch-bytes", type=int, default=None,
                     help="decode only: set the context's L2 fetch granularity hint (32 lets the window's "
                          "skipped 16-byte K chunks stay unread in DRAM)")
@@ -526,6 +580,8 @@ def main():
         line = run_reference(args, w, rank)
     elif args.decode:
         line = run_decode(args, w, rank, world, local_rank)
+    elif args.backward:
+        line = run_backward(args, w, rank, world, local_rank)
     else:
         line = run_ours(args, w, rank, world, local_rank)
     if line is not None:

@@ -371,16 +371,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             const int s = it & 1, n = it >> 1;
             const int h = g * G + it / per_head;
             const int q0 = (i_lo + it % per_head) * 128;
-            if (n >= 1 && !bwd_wait(bar_at(bar0, BB_STR_EMPTY + s), (n - 1) & 1, ctl, kStatusProducer)) break;
-            float* ls = reinterpret_cast<float*>(smg + L::kRows + s * 1024);
+            // the tile's per-row values are read before the slot frees up, off the refill's path
             const float* lse_row = p.lse + (static_cast<size_t>(b) * f.Hq + h) * f.S;
             const float* dlt_row = p.dlt + (static_cast<size_t>(b) * f.Hq + h) * f.S;
+            float lv[4], dv4[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int r = q0 + lane + 32 * q;
                 const bool in = r < f.S;
-                ls[lane + 32 * q] = in ? lse_row[r] * 1.4426950408889634f : INFINITY;  // padded queries get P = 0
-                ls[128 + lane + 32 * q] = in ? dlt_row[r] : 0.f;
+                lv[q] = in ? __ldg(lse_row + r) * 1.4426950408889634f : INFINITY;  // padded queries get P = 0
+                dv4[q] = in ? __ldg(dlt_row + r) : 0.f;
+            }
+            if (n >= 1 && !bwd_wait(bar_at(bar0, BB_STR_EMPTY + s), (n - 1) & 1, ctl, kStatusProducer)) break;
+            float* ls = reinterpret_cast<float*>(smg + L::kRows + s * 1024);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ls[lane + 32 * q] = lv[q];
+                ls[128 + lane + 32 * q] = dv4[q];
             }
             __syncwarp();
             if (lane == 0) {
@@ -407,22 +414,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         const uint64_t kdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
         const uint64_t vdesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
         bool ok = mbar_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
-        if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
         for (int it = 0; it < iters && ok; ++it) {
             const int s = it & 1, n = it >> 1;
             ok = mbar_wait(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
-            if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
             if (!ok) break;
             tc_fence_after();
             const uint32_t qa = sm + L::kStr0 + s * 2 * L::kTile, da = qa + L::kTile;
             const uint64_t qdesc = sw128_desc(qa, 16u, 1024u), ddesc = sw128_desc(da, 16u, 1024u);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                umma_ss(tS, desc_advance(kdesc, kmajor_units(kk)), desc_advance(qdesc, kmajor_units(kk)), kIdescS,
-                        kk > 0 ? 1u : 0u);
+            // dP^T needs no rotated operand: it runs while the RoPE warps finish Q
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 umma_ss(tdP, desc_advance(vdesc, kmajor_units(kk)), desc_advance(ddesc, kmajor_units(kk)), kIdescDP,
+                        kk > 0 ? 1u : 0u);
+            if (ROPE) {
+                if (it == 0) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
+                if (ok) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
+                if (!ok) break;
+                tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tS, desc_advance(kdesc, kmajor_units(kk)), desc_advance(qdesc, kmajor_units(kk)), kIdescS,
                         kk > 0 ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_S_FULL));
             ok = mbar_wait(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
@@ -582,22 +594,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         const uint64_t qdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
         const uint64_t ddesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
         bool ok = mbar_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
-        if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
         for (int it = 0; it < iters && ok; ++it) {
             const int s = it & 1, n = it >> 1;
             ok = mbar_wait(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
-            if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
             if (!ok) break;
             tc_fence_after();
             const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile, va = ka + L::kTile;
             const uint64_t kdesc = sw128_desc(ka, 16u, 1024u), vdesc = sw128_desc(va, 16u, 1024u);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
-                        kk > 0 ? 1u : 0u);
+            // dP needs no rotated operand: it runs while the RoPE warps finish K
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 umma_ss(tdP, desc_advance(ddesc, kmajor_units(kk)), desc_advance(vdesc, kmajor_units(kk)), kIdescDP,
+                        kk > 0 ? 1u : 0u);
+            if (ROPE) {
+                if (it == 0) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
+                if (ok) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
+                if (!ok) break;
+                tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
                         kk > 0 ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_S_FULL));
             ok = mbar_wait(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);

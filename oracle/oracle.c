@@ -390,3 +390,84 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
     }
     return 0;
 }
+
+/*
+ * Block-sparse attention output ("AttnFuse", sec. 4.3 Block-Sparse Attention:
+ * a CSR BlockMask lists, per row of blocks, the active key blocks; only those
+ * blocks' scores enter the softmax).  Blocks are `block` x `block`; the mask
+ * is shared by every batch element and head: key j is visible to query i iff
+ * block (i / block, j / block) is listed (and j <= i when causal).  Each row's
+ * score vector is materialised over the visible keys only, then handled as in
+ * oracle_attn_rows (RoPE, scale, max, exponentials, weighted sum, LSE).
+ * A row that sees no key gets O = 0 and LSE = -inf.
+ *   row_ptr [ceil(S/block) + 1], col_idx [row_ptr[last]]: the CSR mask.
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_rows_bs(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                        int block, const int* row_ptr, const int* col_idx,
+                        int n_rows, const int* row_b, const int* row_h, const int* row_i,
+                        double* o_out, double* lse_out) {
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 1024 || block < 1)
+        return -1;
+    const int nb = (S + block - 1) / block;
+    for (int r = 0; r < nb; ++r) {
+        if (row_ptr[r + 1] < row_ptr[r]) return -1;
+        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e)
+            if (col_idx[e] < 0 || col_idx[e] >= nb) return -1;
+    }
+    for (int n = 0; n < n_rows; ++n)
+        if (row_b[n] < 0 || row_b[n] >= B || row_h[n] < 0 || row_h[n] >= Hq || row_i[n] < 0 || row_i[n] >= S)
+            return -1;
+    /* the active table, one byte per (query block, key block) */
+    char* active = (char*)calloc((size_t)nb * nb, 1);
+    for (int r = 0; r < nb; ++r)
+        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e) active[(size_t)r * nb + col_idx[e]] = 1;
+    const int rope_on = rope_base > 0.0;
+    const int G = Hq / Hkv;
+    double theta[512];
+    if (rope_on) rope_thetas(D, rope_base, theta);
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int n = 0; n < n_rows; ++n) {
+        const int b = row_b[n], h = row_h[n], i = row_i[n], g = h / G;
+        double qrot[1024], krot[1024];
+        rope_rotate(q + (((size_t)b * S + i) * Hq + h) * D, D, theta, (double)i, rope_on, qrot);
+        double* s = (double*)malloc(sizeof(double) * (size_t)S);
+        int* key = (int*)malloc(sizeof(int) * (size_t)S);
+        int cnt = 0;
+        for (int j = 0; j < S; ++j) {
+            if (!active[(size_t)(i / block) * nb + j / block]) continue;
+            if (causal && j > i) continue;
+            rope_rotate(k + (((size_t)b * S + j) * Hkv + g) * D, D, theta, (double)j, rope_on, krot);
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qrot[d] * krot[d];
+            s[cnt] = acc * inv_sqrt_d;
+            key[cnt++] = j;
+        }
+        double* o = o_out + (size_t)n * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (cnt == 0) {
+            lse_out[n] = -INFINITY;
+        } else {
+            double m = s[0];
+            for (int c = 1; c < cnt; ++c)
+                if (s[c] > m) m = s[c];
+            double l = 0.0;
+            for (int c = 0; c < cnt; ++c) {
+                s[c] = exp(s[c] - m);
+                l += s[c];
+            }
+            for (int c = 0; c < cnt; ++c) {
+                const uint16_t* vj = v + (((size_t)b * S + key[c]) * Hkv + g) * D;
+                for (int d = 0; d < D; ++d) o[d] += s[c] * bf16_to_f64(vj[d]);
+            }
+            for (int d = 0; d < D; ++d) o[d] /= l;
+            lse_out[n] = m + log(l);
+        }
+        free(s);
+        free(key);
+    }
+    free(active);
+    return 0;
+}

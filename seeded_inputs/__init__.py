@@ -24,6 +24,7 @@ MASTER_SEED = 42
 
 # tensor ids: each tensor of a workload draws from its own counter stream
 TENSOR_Q, TENSOR_K, TENSOR_V = 1, 2, 3
+TENSOR_BLOCK_MASK = 20  # stream id of the random blocks of a block mask
 _OUTLIER_STREAM = 1000
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -195,3 +196,38 @@ def sample_heads(seed: int, B: int, Hq: int, Hkv: int, n: int = 8):
         if (b, h) not in pairs:
             pairs.append((b, h))
     return pairs[:n]
+
+
+def bigbird_block_mask(S: int, block: int = 128, window: int = 1, n_global: int = 1, n_random: int = 1,
+                       seed: int = MASTER_SEED, causal: bool = False):
+    """A BigBird-style block mask as CSR (row_ptr, col_idx) over ceil(S/block) blocks per side.
+
+    Row r lists: the blocks within `window` of the diagonal, the first `n_global` blocks (global
+    columns), `n_random` further blocks drawn from the splitmix64 stream of (seed, block-mask
+    id) at counters 256 r ..; the first
+    `n_global` rows list every block (global rows).  With causal=True blocks above the diagonal
+    are dropped.  Columns are sorted and unique.  Structure only: no attention arithmetic.
+    """
+    nb = (S + block - 1) // block
+    rows = []
+    for r in range(nb):
+        cols = set(range(max(0, r - window), min(nb, r + window + 1)))
+        cols.update(range(min(n_global, nb)))
+        if r < n_global:
+            cols.update(range(nb))
+        words = uniform_words(seed, TENSOR_BLOCK_MASK, r * 256, 256)
+        drawn = 0
+        for word in words:
+            if drawn >= n_random or len(cols) >= nb:
+                break
+            c = int(word % np.uint64(nb))
+            if c not in cols:
+                cols.add(c)
+                drawn += 1
+        if causal:
+            cols = {c for c in cols if c <= r}
+        rows.append(sorted(cols))
+    row_ptr = np.zeros(nb + 1, dtype=np.int32)
+    row_ptr[1:] = np.cumsum([len(c) for c in rows])
+    col_idx = np.array([c for cs in rows for c in cs], dtype=np.int32)
+    return row_ptr, col_idx

@@ -16,7 +16,7 @@ import numpy as np
 
 from ._build import INCLUDE, LIB, build
 
-__all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -60,6 +60,8 @@ def load_library(path: str | None = None):
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, d, d, vp]
         lib.attn_bwd.restype = i
         lib.attn_bwd.argtypes = [vp] * 9 + [i] * 6 + [d, vp]
+        lib.attn_fwd_blocksparse.restype = i
+        lib.attn_fwd_blocksparse.argtypes = [vp] * 5 + [i] * 6 + [d, vp, vp, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i
@@ -224,6 +226,57 @@ def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream
     if rc != 0:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv
+
+
+def _check_bshd(q, k, v):
+    """Shape checks shared by the bindings: BSHD bf16 CUDA tensors; returns (B, S, Hq, D, Hkv)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (BSHD)")
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, S, Hkv, D] with q's B, S and D")
+    return B, S, Hq, D, Hkv
+
+
+def create_block_mask(predicate, S: int, *, block: int = 128):
+    """The CSR block mask (row_ptr, col_idx) of predicate(q_block, k_block) -> bool over ceil(S/block)
+    blocks per side, evaluated once per block pair (int32 numpy arrays)."""
+    import numpy as np
+    nb = (S + block - 1) // block
+    rows = [[kb for kb in range(nb) if predicate(qb, kb)] for qb in range(nb)]
+    row_ptr = np.zeros(nb + 1, dtype=np.int32)
+    row_ptr[1:] = np.cumsum([len(r) for r in rows])
+    col_idx = np.array([c for r in rows for c in r], dtype=np.int32)
+    return row_ptr, col_idx
+
+
+def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, o=None, lse=None, *, causal: bool = False, rope_base=None,
+                         return_lse: bool = True, stream=None):
+    """The forward over a CSR block mask of 128 x 128 blocks (see create_block_mask); returns (o, lse)."""
+    import numpy as np
+    import torch
+    B, S, Hq, D, Hkv = _check_bshd(q, k, v)
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    if rp.shape != ((S + 127) // 128 + 1,):
+        raise ValueError("row_ptr must have ceil(S/128) + 1 entries")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr() if lse is not None else None, B, Hq, Hkv, S, D,
+                                      1 if causal else 0, float(rope_base) if rope_base else 0.0,
+                                      rp.ctypes.data, ci.ctypes.data if ci.size else None,
+                                      _stream_handle(stream, q.device))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_blocksparse")
+    return o, lse
 
 
 def attn_fwd_host(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=None, window_k=None,

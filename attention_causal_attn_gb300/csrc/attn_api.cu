@@ -18,6 +18,7 @@
 #include "rope_rotate_kernel.cuh"
 #include "decode_kernel.cuh"
 #include "bwd_kernel.cuh"
+#include "bs_fwd_kernel.cuh"
 #include "host_tables.h"
 
 // Raised (bitwise OR) by a CTA whose bounded wait ran out; read and cleared by attn_check().
@@ -882,6 +883,120 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     return rope ? launch_bwd<64, false, true>(bp, dev, ntiles, st) : launch_bwd<64, false, false>(bp, dev, ntiles, st);
 }
 
+// ---------------------------------------------------------------------------
+// Block-sparse forward ("AttnFuse", sec. 4.3 Block-Sparse Attention).
+namespace {
+struct MaskEntry {
+    int dev;
+    std::vector<int> csr;  // row_ptr then col_idx, as given
+    int* d = nullptr;
+};
+std::vector<MaskEntry> g_masks;  // device copies of the block masks seen, by content
+
+int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out) {
+    const int nnz = row_ptr[nrows];
+    for (auto& e : g_masks) {
+        if (e.dev != dev || e.csr.size() != static_cast<size_t>(nrows + 1 + nnz)) continue;
+        if (std::equal(row_ptr, row_ptr + nrows + 1, e.csr.begin()) &&
+            std::equal(col_idx, col_idx + nnz, e.csr.begin() + nrows + 1)) {
+            *out = e.d;
+            return ATTN_OK;
+        }
+    }
+    MaskEntry me;
+    me.dev = dev;
+    me.csr.assign(row_ptr, row_ptr + nrows + 1);
+    me.csr.insert(me.csr.end(), col_idx, col_idx + nnz);
+    cudaError_t e;
+    if ((e = cudaMalloc(&me.d, me.csr.size() * sizeof(int))) != cudaSuccess)
+        return cuda_fail("cudaMalloc(block mask)", e, ATTN_ERR_OOM);
+    if ((e = cudaMemcpy(me.d, me.csr.data(), me.csr.size() * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) {
+        cudaFree(me.d);
+        return cuda_fail("cudaMemcpy(block mask)", e);
+    }
+    *out = me.d;
+    g_masks.push_back(std::move(me));
+    return ATTN_OK;
+}
+
+template <int D, bool CAUSAL, bool ROPE>
+int launch_bs(const attn::BsParams& bp, int dev, int nrows, cudaStream_t st) {
+    constexpr int kMin = 120 * 1024;  // one CTA per SM: each takes all 512 TMEM columns
+    constexpr int smem = static_cast<int>(attn::BsLayout<D>::kAlloc) > kMin ? static_cast<int>(attn::BsLayout<D>::kAlloc) : kMin;
+    constexpr unsigned bit = 1u << (8 | (D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0));
+    auto kern = attn::bs_fwd_kernel<D, CAUSAL, ROPE>;
+    cudaError_t e;
+    if (!(g_bwd_configured[dev] & bit)) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return cuda_fail("cudaFuncSetAttribute(block-sparse)", e);
+        g_bwd_configured[dev] |= bit;
+    }
+    kern<<<dim3(static_cast<unsigned>(bp.f.B * bp.f.Hq), static_cast<unsigned>(nrows)), attn::kBsThreads, smem, st>>>(bp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("block-sparse kernel launch", e);
+    return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                    int Hkv, int S, int D, int causal, double rope_base, const int* row_ptr,
+                                    const int* col_idx, void* stream) {
+    int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, 0.0);
+    if (arc == ATTN_OK && row_ptr == nullptr) arc = ATTN_ERR_NULL;
+    if (arc == ATTN_OK && (static_cast<long long>(B) * Hq > INT_MAX / 2)) arc = ATTN_ERR_SHAPE;
+    if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+                           (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+        arc = ATTN_ERR_ALIGN;
+    if (arc != ATTN_OK) return arc;
+    // the mask: row_ptr[0] = 0, non-decreasing; each row's columns ascending, distinct, in range,
+    // and at most the row with the causal mask (tiles above the diagonal hold no visible key)
+    const int nrows = (S + 127) / 128;
+    if (row_ptr[0] != 0) return ATTN_ERR_SHAPE;
+    for (int r = 0; r < nrows; ++r) {
+        if (row_ptr[r + 1] < row_ptr[r]) return ATTN_ERR_SHAPE;
+        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+            if (col_idx == nullptr) return ATTN_ERR_NULL;
+            const int cidx = col_idx[e];
+            if (cidx < 0 || cidx >= nrows || (causal && cidx > r) || (e > row_ptr[r] && cidx <= col_idx[e - 1]))
+                return ATTN_ERR_SHAPE;
+        }
+    }
+    const bool rope = rope_base > 0.0 && std::isfinite(rope_base);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+    attn::BsParams bp;
+    float2* rope_tab = nullptr;
+    int* dmask = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int rc = probe_device(dev);
+        if (rc != ATTN_OK) return rc;
+        if (rope && (rc = get_rope(dev, S, D, rope_base, &rope_tab)) != ATTN_OK) return rc;
+        if ((rc = get_mask(dev, row_ptr, col_idx, nrows, &dmask)) != ATTN_OK) return rc;
+        bp.f.status = g_dev[dev].status;
+    }
+    if (!encode_bshd(&bp.f.tm_q, q, B, S, Hq, D) || !encode_bshd(&bp.f.tm_k, k, B, S, Hkv, D) ||
+        !encode_bshd(&bp.f.tm_v, v, B, S, Hkv, D))
+        return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    bp.f.o = static_cast<__nv_bfloat16*>(o);
+    bp.f.lse = lse;
+    bp.f.rope = rope_tab;
+    bp.f.B = B;
+    bp.f.Hq = Hq;
+    bp.f.Hkv = Hkv;
+    bp.f.S = S;
+    bp.f.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    bp.f.wait_limit_ns = kWaitLimitNs;
+    bp.row_ptr = dmask;
+    bp.col_idx = dmask + nrows + 1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (D == 128) {
+        if (causal) return rope ? launch_bs<128, true, true>(bp, dev, nrows, st) : launch_bs<128, true, false>(bp, dev, nrows, st);
+        return rope ? launch_bs<128, false, true>(bp, dev, nrows, st) : launch_bs<128, false, false>(bp, dev, nrows, st);
+    }
+    if (causal) return rope ? launch_bs<64, true, true>(bp, dev, nrows, st) : launch_bs<64, true, false>(bp, dev, nrows, st);
+    return rope ? launch_bs<64, false, true>(bp, dev, nrows, st) : launch_bs<64, false, false>(bp, dev, nrows, st);
+}
+
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
                                  float* cos_out, float* sin_out, int* win_out) {
     if (S < 1 || S > kMaxS || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
@@ -980,6 +1095,11 @@ extern "C" void attn_release_cache(void) {
         cudaFree(g_dec[d].buf);
         g_dec[d] = DecodeScratch();
     }
+    for (auto& e : g_masks) {
+        cudaSetDevice(e.dev);
+        cudaFree(e.d);
+    }
+    g_masks.clear();
     for (int d = 0; d < kMaxDevices; ++d) {
         if (g_bwd[d].buf == nullptr) continue;
         cudaSetDevice(d);

@@ -1,0 +1,244 @@
+// Block-sparse attention forward ("AttnFuse", sec. 4.3 Block-Sparse Attention:
+// a CSR BlockMask lists the active key blocks of each row of blocks, and the
+// kernel visits only those, so its work is proportional to the active share).
+//
+// Blocks are the kernel's 128 x 128 tiles.  CTA (b * Hq + h, i) computes query
+// tile i of head h: Q is loaded and rotated once, then the listed key tiles
+// are streamed (two slots) in descending order, each through
+//   S = Q K^T (tcgen05, TMEM)  ->  online softmax, P in bf16 over S  ->  O += P V.
+// Roles as in the backward kernels: one elementwise warpgroup (one thread per
+// query row, the prefill's softmax arithmetic and lazy rescale), four RoPE
+// warps, a TMA warp and an MMA warp.  A row of blocks with nothing listed
+// writes O = 0 and LSE = -inf.  Every wait is bounded.
+#pragma once
+
+#include "bwd_kernel.cuh"
+
+namespace attn {
+
+struct BsParams {
+    FwdParams f;           // tm_q, tm_k, tm_v, o, lse, RoPE factor table, shape, scale, status, wait limit
+    const int* row_ptr;    // [ceil(S/128) + 1]
+    const int* col_idx;    // listed key tiles of each row of tiles, ascending
+};
+
+constexpr int kBsThreads = 320;  // warps 0-3 softmax, 4-7 RoPE, 8 TMA, 9 MMA
+constexpr int kBsWarpRope = 4, kBsWarpTma = 8, kBsWarpMma = 9;
+
+template <int D>
+struct BsLayout {
+    static constexpr uint32_t kTile = 128u * D * 2u;
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kStr0 = kTile;  // slot s: K at kStr0 + 2 s kTile, V after it
+    static constexpr uint32_t kBars = 5 * kTile;
+    static constexpr uint32_t kMisc = kBars + 256;
+    static constexpr uint32_t kBytes = kMisc + 64;
+    static constexpr uint32_t kAlloc = kBytes + 1024;
+};
+
+template <int D, bool CAUSAL, bool ROPE>
+__global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_constant__ BsParams p) {
+    using L = BsLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sm = smem_addr(smg);
+    const uint32_t bar0 = sm + L::kBars;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smg + L::kMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smg + L::kMisc + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const FwdParams& f = p.f;
+    const int i = blockIdx.y;
+    const int b = blockIdx.x / f.Hq, h = blockIdx.x % f.Hq;
+    const int g = h / (f.Hq / f.Hkv);
+    const int q0 = i * 128;
+    const int e0 = p.row_ptr[i];
+    const int nblk = p.row_ptr[i + 1] - e0;  // listed tiles, visited from the last listed down
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        bwd_init_bars(bar0, 128);  // P is handed over by the 128 softmax threads
+    }
+    if (warp == kBsWarpTma && lane == 0) {
+        tma_prefetch_desc(&f.tm_q);
+        tma_prefetch_desc(&f.tm_k);
+        tma_prefetch_desc(&f.tm_v);
+    }
+    if (warp == kBsWarpMma) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl ctl{abort_flag, f.status, f.wait_limit_ns};
+
+    if (warp < 4) {
+        // ---- softmax warpgroup: thread t owns query row q0 + t (TMEM lane t)
+        const int t = threadIdx.x;
+        const int row = q0 + t;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
+        const uint32_t tS = trow, tO = trow + 128u;
+        const float c = f.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int it = 0; it < nblk && ok; ++it) {
+            const int kv0 = p.col_idx[e0 + nblk - 1 - it] * 128;
+            ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
+            if (!ok) break;
+            tc_fence_after();
+            // keys [kv0, kv0 + limit) are visible to this row
+            int limit = min(128, f.S - kv0);
+            if (CAUSAL) limit = min(limit, row - kv0 + 1);
+            const bool masked = __any_sync(0xffffffffu, limit < 128);
+            const float mx = masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit);
+            const float m_new = fmaxf(m_used, mx);
+            if (it == 0) {
+                m_used = m_new;
+            } else {
+                const bool need = (m_new - m_used) * c > kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = ex2_approx((m_used - m_new) * c);
+                        m_used = m_new;
+                        l *= alpha;
+                    }
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t r[32];
+                        tmem_load_32(tO + cc, r);
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            float x0, x1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2), x0, x1);
+                            r[j] = __float_as_uint(x0);
+                            r[j + 1] = __float_as_uint(x1);
+                        }
+                        tmem_store_32(tO + cc, r);
+                    }
+                }
+            }
+            const float mc = m_used * c;
+            l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
+            tmem_store_wait();
+            tc_fence_before();
+            mbar_arrive(bar_at(bar0, BB_P_FULL));
+        }
+        // epilogue: O / l in bf16, LSE in natural log (a row that saw nothing: 0 and -inf)
+        const bool have = nblk > 0;
+        if (ok && (!have || bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax))) {
+            tc_fence_after();
+            const bool store = row < f.S;
+            const float inv_l = (have && l > 0.f) ? 1.0f / l : 0.f;
+            __nv_bfloat16* dst = f.o + ((static_cast<size_t>(b) * f.S + (store ? row : 0)) * f.Hq + h) * D;
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t r[32];
+                if (have) tmem_load_32(tO + cc, r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2)
+                    pk[j / 2] = have ? pack_bf16x2(__uint_as_float(r[j]) * inv_l, __uint_as_float(r[j + 1]) * inv_l) : 0u;
+                if (store) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            if (store && f.lse != nullptr)
+                f.lse[(static_cast<size_t>(b) * f.Hq + h) * f.S + row] =
+                    have ? (m_used * c + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+    } else if (warp < kBsWarpTma) {
+        // ---- RoPE warps: Q once, then each streamed K tile
+        if (ROPE && nblk > 0) {
+            const int t = threadIdx.x - kBsWarpRope * 32;
+            RopeConsts k;
+            rope_load_consts<D>(f, t, k);
+            uint64_t cb[4], sb[4];
+            rope_load_base<D>(f, i, t, cb, sb);
+            bool ok = bwd_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusRope);
+            if (ok) {
+                rope_rotate_tile<D, false>(smg + L::kQ, k, cb, sb, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_at(bar0, BB_RES_ROT));
+            }
+            for (int it = 0; it < nblk && ok; ++it) {
+                const int s = it & 1;
+                rope_load_base<D>(f, p.col_idx[e0 + nblk - 1 - it], t, cb, sb);
+                ok = bwd_wait(bar_at(bar0, BB_STR_FULL + s), (it >> 1) & 1, ctl, kStatusRope);
+                if (!ok) break;
+                rope_rotate_tile<D, false>(smg + L::kStr0 + s * 2 * L::kTile, k, cb, sb, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_at(bar0, BB_STR_ROT + s));
+            }
+        }
+    } else if (warp == kBsWarpTma) {
+        // ---- producer: Q once, then K and V of each listed tile
+        if (lane == 0 && nblk > 0) {
+            const uint32_t rb = bar_at(bar0, BB_RES_FULL);
+            mbar_arrive_expect_tx(rb, L::kTile);
+#pragma unroll
+            for (int sub = 0; sub < D / 64; ++sub)
+                tma_load_4d(sm + L::kQ + sub * kSubTileBytes, &f.tm_q, rb, sub * 64, h, q0, b);
+            for (int it = 0; it < nblk; ++it) {
+                const int s = it & 1, n = it >> 1;
+                const int kv0 = p.col_idx[e0 + nblk - 1 - it] * 128;
+                if (n >= 1 && !mbar_wait(bar_at(bar0, BB_STR_EMPTY + s), (n - 1) & 1, ctl, kStatusProducer)) break;
+                const uint32_t fb = bar_at(bar0, BB_STR_FULL + s);
+                mbar_arrive_expect_tx(fb, 2 * L::kTile);
+                const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile;
+#pragma unroll
+                for (int sub = 0; sub < D / 64; ++sub) {
+                    tma_load_4d(ka + sub * kSubTileBytes, &f.tm_k, fb, sub * 64, g, kv0, b);
+                    tma_load_4d(ka + L::kTile + sub * kSubTileBytes, &f.tm_v, fb, sub * 64, g, kv0, b);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kBsWarpMma && lane == 0 && nblk > 0) {
+        // ---- MMA issuer: S = Q K^T (K-major, fp16 after RoPE), then O += P V (P from TMEM, V MN-major)
+        const uint32_t kIdescS = umma_idesc_f16(ROPE ? 0u : 1u, 0u, 128, 128);
+        constexpr uint32_t kIdescPV = umma_idesc_f16(1u, 1u, 128, D);
+        const uint32_t tS = tmem, tO = tmem + 128u;
+        const uint64_t qdesc = sw128_desc(sm + L::kQ, 16u, 1024u);
+        bool ok = mbar_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
+        if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
+        for (int it = 0; it < nblk && ok; ++it) {
+            const int s = it & 1, n = it >> 1;
+            ok = mbar_wait(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
+            if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile, va = ka + L::kTile;
+            const uint64_t kdesc = sw128_desc(ka, 16u, 1024u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
+                        kk > 0 ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_S_FULL));
+            ok = mbar_wait(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t vdesc = sw128_desc(va, kSubTileBytes, 1024u);
+            // 16 keys per step: 2048 bytes of V, 8 TMEM columns of P
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, (it > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
+        }
+        if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));
+        bwd_drain(bar0, ctl);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBsWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace attn

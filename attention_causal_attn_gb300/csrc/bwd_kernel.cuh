@@ -236,7 +236,7 @@ __device__ __forceinline__ void bwd_drain(uint32_t bar0, const WaitCtl& ctl) {
     }
 }
 
-__device__ __forceinline__ void bwd_init_bars(uint32_t bar0) {
+__device__ __forceinline__ void bwd_init_bars(uint32_t bar0, uint32_t p_count = kBwdEw) {
     mbar_init(bar_at(bar0, BB_RES_FULL), 1);
     mbar_init(bar_at(bar0, BB_RES_ROT), 128);
     for (int s = 0; s < 2; ++s) {
@@ -245,7 +245,7 @@ __device__ __forceinline__ void bwd_init_bars(uint32_t bar0) {
         mbar_init(bar_at(bar0, BB_STR_EMPTY + s), 1);
     }
     mbar_init(bar_at(bar0, BB_S_FULL), 1);
-    mbar_init(bar_at(bar0, BB_P_FULL), kBwdEw);
+    mbar_init(bar_at(bar0, BB_P_FULL), p_count);
     mbar_init(bar_at(bar0, BB_ACC_FULL), 1);
     mbar_init(bar_at(bar0, BB_DRAIN), 1);
     fence_barrier_init();

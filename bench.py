@@ -504,6 +504,79 @@ def run_backward(args, w, rank, world, local_rank):
     }
 
 
+# --------------------------------------------------------------------- block-sparse forward
+def visible_pairs(S, row_ptr, col_idx, causal, block=128):
+    """(query, key) pairs a block mask leaves visible: each listed block's rows x keys, triangular on the diagonal."""
+    total = 0
+    for r in range(len(row_ptr) - 1):
+        rows = min(block, S - block * r)
+        for c in col_idx[row_ptr[r]:row_ptr[r + 1]]:
+            keys = min(block, S - block * int(c))
+            if causal and int(c) == r:
+                total += rows * (rows + 1) // 2
+            else:
+                total += rows * keys
+    return total
+
+
+def run_blocksparse(args, w, rank, world, local_rank):
+    """One step = one attn_fwd_blocksparse call over the workload's block mask."""
+    import torch
+    import attention_causal_attn_gb300 as attn
+    attn.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if "block_mask" not in w:
+        raise SystemExit("--blocksparse needs a workload with a block mask (bigbird_s4096)")
+    B, Hq, Hkv, S, D = w["B"], w["Hq"], w["Hkv"], w["S"], w["D"]
+    q_h, k_h, v_h = si.make_qkv(B, Hq, Hkv, S, D, outliers=w["outliers"], seed=replica_seed(rank))
+    rp, ci = si.bigbird_block_mask(S, causal=w["causal"], **w["block_mask"])
+    q, k, v = (torch.from_numpy(x).view(torch.bfloat16).to(dev) for x in (q_h, k_h, v_h))
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(causal=w["causal"], rope_base=w["rope_base"], stream=stream)
+    o, lse = attn.attn_fwd_blocksparse(q, k, v, rp, ci, **kw)
+    for _ in range(max(args.warmup, 3)):
+        attn.attn_fwd_blocksparse(q, k, v, rp, ci, o, lse, **kw)
+    attn.attn_check(stream=stream, device=dev)
+    small = 3 * q.numel() * 2 < (256 << 20)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
+    times = []
+    with ClockSampler(local_rank) as clocks:
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.attn_fwd_blocksparse(q, k, v, rp, ci, o, lse, **kw)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+    attn.attn_check(stream=stream, device=dev)
+    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    pairs = visible_pairs(S, rp, ci, w["causal"])
+    flops = 4.0 * D * pairs * B * Hq
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks, _ = load_peaks()
+    nb = len(rp) - 1
+    cfg = workload_config(args.workload, w)
+    cfg["step"] = "block-sparse forward over the workload's mask"
+    cfg["active_blocks"] = int(rp[-1])
+    cfg["active_share"] = round(int(rp[-1]) / (nb * nb), 4)
+    cfg["l2"] = "L2 flushed between steps" if flush is not None else "inputs larger than L2"
+    return {
+        "metric": "block-sparse attention forward TFLOP/s", "value": round(tf, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": float(peaks["bf16_tflops"]),
+                     "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4), "traffic": None,
+                     "kernel": "bs_fwd_kernel",
+                     "algorithmic": "4*D FLOPs per visible (query, key) pair of the mask, median step time"},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+
+
 # --------------------------------------------------------------------- reference arm
 def run_reference(args, w, rank):
     if rank != 0:
@@ -552,6 +625,8 @@ def main():
     ap.add_argument("--seq", type=int, default=None, help="override the workload's sequence length")
     ap.add_argument("--decode", action="store_true",
                     help="time one decode step (attn_decode) on the workload's cache shape instead of the prefill")
+    ap.add_argument("--blocksparse", action="store_true",
+                    help="time the block-sparse forward on a workload with a block mask (bigbird_s4096)")
     ap.add_argument("--backward", action="store_true",
                     help="time one backward step (attn_bwd) on the workload instead of the forward")
     ap.add_argument("--l2-fetch-bytes", type=int, default=None,
@@ -582,6 +657,8 @@ def main():
         line = run_decode(args, w, rank, world, local_rank)
     elif args.backward:
         line = run_backward(args, w, rank, world, local_rank)
+    elif args.blocksparse:
+        line = run_blocksparse(args, w, rank, world, local_rank)
     else:
         line = run_ours(args, w, rank, world, local_rank)
     if line is not None:

@@ -229,6 +229,27 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              void* stream);
 
 /*
+ * attn_fwd_blocksparse — the forward over a block-sparse mask ("AttnFuse: A
+ * Composable DSL for Compiling Attentions to Fused GPU Kernels", sec. 4.3
+ * Block-Sparse Attention: a CSR BlockMask lists each row's active key
+ * blocks, and the kernel visits only those).
+ *   Blocks are 128 x 128 (query tile x key tile), shared by every batch
+ *   element and head: key j is visible to query i iff block (i/128, j/128) is
+ *   listed, and j <= i when causal.
+ *   row_ptr  host int32 [ceil(S/128) + 1], row_ptr[0] = 0, non-decreasing.
+ *   col_idx  host int32 [row_ptr[last]]: each row's key tiles, strictly
+ *            ascending, in [0, ceil(S/128)); with causal, at most the row.
+ *   q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base   as attn_fwd (no
+ *            window).  A query row that sees no key gets O = 0, LSE = -inf.
+ * The library keeps a device copy of each distinct mask until
+ * attn_release_cache().  Asynchronous on `stream`.
+ * Errors: as attn_fwd; ATTN_ERR_SHAPE for a malformed mask.
+ */
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                         int S, int D, int causal, double rope_base, const int* row_ptr, const int* col_idx,
+                         void* stream);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

@@ -141,6 +141,10 @@ WORKLOADS = {
                               window_k=None, outliers=0.01),
     "window_s131072": dict(B=1, Hq=32, Hkv=8, S=131072, D=128, causal=True, rope_base=500000.0,
                            window_k=1.0, outliers=0.0),
+    # block-sparse forward ("AttnFuse", sec. 4.3: BigBird at N = 4096): a BigBird-style mask over
+    # 128 x 128 blocks, the diagonal, one global block row/column and one seeded random block per row
+    "bigbird_s4096": dict(B=4, Hq=32, Hkv=32, S=4096, D=128, causal=False, rope_base=None,
+                          window_k=None, outliers=0.0, block_mask=dict(window=0, n_global=1, n_random=1)),
 }
 
 

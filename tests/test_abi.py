@@ -19,7 +19,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
     assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated",
-                          "attn_decode", "attn_bwd", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
+                          "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for n in names:
@@ -105,6 +105,31 @@ def test_backward_checks_arguments_on_the_host(lib):
     assert call(causal=2) == E["ATTN_ERR_UNSUPPORTED"]
     assert call(dq=24) == E["ATTN_ERR_ALIGN"]
     assert call(lse=18) == E["ATTN_ERR_ALIGN"]
+
+
+def test_blocksparse_mask_is_checked_on_the_host(lib):
+    E = attn.ATTN_STATUS
+    import numpy as np
+
+    def call(rp, ci, causal=0, S=256):
+        rp = np.asarray(rp, np.int32)
+        ci = np.asarray(ci, np.int32)
+        return lib.attn_fwd_blocksparse(16, 16, 16, 16, None, 1, 2, 2, S, 128, causal, 1e4, rp.ctypes.data,
+                                        ci.ctypes.data if ci.size else None, None)
+    assert call([1, 1, 2], [0, 1]) == E["ATTN_ERR_SHAPE"]         # row_ptr[0] != 0
+    assert call([0, 2, 1], [0, 1]) == E["ATTN_ERR_SHAPE"]         # decreasing
+    assert call([0, 1, 2], [0, 2]) == E["ATTN_ERR_SHAPE"]         # column out of range
+    assert call([0, 2, 2], [1, 0]) == E["ATTN_ERR_SHAPE"]         # not ascending
+    assert call([0, 2, 2], [0, 0]) == E["ATTN_ERR_SHAPE"]         # repeated
+    assert call([0, 2, 2], [0, 1], causal=1) == E["ATTN_ERR_SHAPE"]  # above the diagonal
+    assert lib.attn_fwd_blocksparse(16, 16, 16, 16, None, 1, 2, 2, 256, 128, 0, 1e4, None, None,
+                                    None) == E["ATTN_ERR_NULL"]
+
+
+def test_create_block_mask_lists_the_predicate():
+    rp, ci = attn.create_block_mask(lambda qb, kb: kb <= qb and (qb - kb) % 2 == 0, 640)
+    assert rp.tolist() == [0, 1, 2, 4, 6, 9]
+    assert ci.tolist() == [0, 1, 0, 2, 1, 3, 0, 2, 4]
 
 
 def test_rope_tables_are_float64_cos_sin_rounded(lib):

@@ -346,3 +346,61 @@ def test_backward_matches_oracle(B, Hq, Hkv, S, D, causal, base):
     _check_grad(dv.float().cpu().numpy(), rv, tag + " dV")
     _check_grad(dk.float().cpu().numpy(), rk, tag + " dK")
     _check_grad(dq.float().cpu().numpy(), rq, tag + " dQ")
+
+
+# ---------------------------------------------------------------- block-sparse forward
+BS = [
+    # B, Hq, Hkv, S, D, causal, rope_base, mask
+    (2, 4, 2, 1000, 128, False, 10000.0, "bigbird"),
+    (1, 4, 4, 1024, 128, True, 10000.0, "bigbird"),
+    (1, 2, 1, 300, 64, True, None, "full"),
+    (2, 3, 3, 640, 128, False, 500000.0, "empty_row"),
+    (1, 2, 2, 4096, 128, False, 10000.0, "bigbird"),
+]
+
+
+def _bs_mask(kind, S, causal):
+    nb = (S + 127) // 128
+    if kind == "bigbird":
+        return si.bigbird_block_mask(S, window=0, n_global=1, n_random=1, seed=S, causal=causal)
+    if kind == "full":
+        return attn.create_block_mask(lambda qb, kb: (kb <= qb) or not causal, S)
+    return attn.create_block_mask(lambda qb, kb: qb != 2 and (kb == qb or kb == 0), S)  # block row 2 empty
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base,kind", BS)
+def test_blocksparse_forward_matches_oracle(B, Hq, Hkv, S, D, causal, base, kind):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=700 + S)
+    rp, ci = _bs_mask(kind, S, causal)
+    o, lse = attn.attn_fwd_blocksparse(_dev(q), _dev(k), _dev(v), rp, ci, causal=causal, rope_base=base)
+    attn.attn_check()
+    if S <= 1024:
+        o_ref, lse_ref = oracle.attn_full_bs(q, k, v, rp, ci, causal=causal, rope_base=base)
+        og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+        empty = np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(lg), empty)
+        assert np.all(og.transpose(0, 2, 1, 3)[empty] == 0.0)
+        keep = ~empty
+        _check(og.transpose(0, 2, 1, 3)[keep], lg[keep], o_ref.transpose(0, 2, 1, 3)[keep], lse_ref[keep],
+               f"block-sparse {kind} S={S}")
+    else:  # sampled rows
+        rows = si.sample_rows(S, S, n=128)
+        rb = np.zeros(len(rows), int)
+        rh = np.arange(len(rows)) % Hq
+        o_ref, lse_ref = oracle.attn_rows_bs(q, k, v, rp, ci, rb, rh, rows, causal=causal, rope_base=base)
+        og = o.float().cpu().numpy()[rb, rows, rh]
+        lg = lse.cpu().numpy()[rb, rh, rows]
+        _check(og, lg, o_ref, lse_ref, f"block-sparse {kind} S={S} (sampled)")
+
+
+def test_blocksparse_full_mask_matches_dense_forward():
+    """Every block listed: the same attention as the dense kernel (both round operands alike)."""
+    B, Hq, Hkv, S, D, base = 1, 4, 2, 700, 128, 10000.0
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=777)
+    qd, kd, vd = _dev(q), _dev(k), _dev(v)
+    rp, ci = attn.create_block_mask(lambda qb, kb: kb <= qb, S)
+    o, lse = attn.attn_fwd_blocksparse(qd, kd, vd, rp, ci, causal=True, rope_base=base)
+    o_d, lse_d = attn.attn_fwd(qd, kd, vd, causal=True, rope_base=base)
+    attn.attn_check()
+    assert (o.float() - o_d.float()).abs().max().item() <= 1e-2
+    assert (lse - lse_d).abs().max().item() <= 1e-3

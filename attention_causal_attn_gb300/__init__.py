@@ -16,7 +16,8 @@ import numpy as np
 
 from ._build import INCLUDE, LIB, build
 
-__all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse",
+           "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -62,6 +63,8 @@ def load_library(path: str | None = None):
         lib.attn_bwd.argtypes = [vp] * 9 + [i] * 6 + [d, vp]
         lib.attn_fwd_blocksparse.restype = i
         lib.attn_fwd_blocksparse.argtypes = [vp] * 5 + [i] * 6 + [d, vp, vp, vp]
+        lib.attn_bwd_blocksparse.restype = i
+        lib.attn_bwd_blocksparse.argtypes = [vp] * 9 + [i] * 6 + [d, vp, vp, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i
@@ -201,8 +204,11 @@ def attn_decode(q, k, v, o=None, lse=None, *, rope_base=None, window_k=None, ret
     return o, lse
 
 
-def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream=None):
-    """Gradients (dq, dk, dv) of the forward for upstream gradient dO; o and lse are the forward's outputs."""
+def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream=None, block_mask=None):
+    """Gradients (dq, dk, dv) of the forward for upstream gradient dO; o and lse are the forward's outputs.
+
+    block_mask: the (row_ptr, col_idx) of attn_fwd_blocksparse, or None for the dense forward.
+    """
     import torch
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
         if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
@@ -219,10 +225,19 @@ def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     lib = load_library()
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+            dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S, D, 1 if causal else 0, float(rope_base) if rope_base else 0.0)
     with torch.cuda.device(q.device):
-        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(),
-                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S, D, 1 if causal else 0,
-                          float(rope_base) if rope_base else 0.0, _stream_handle(stream, q.device))
+        if block_mask is None:
+            rc = lib.attn_bwd(*args, _stream_handle(stream, q.device))
+        else:
+            import numpy as np
+            rp = np.ascontiguousarray(block_mask[0], dtype=np.int32)
+            ci = np.ascontiguousarray(block_mask[1], dtype=np.int32)
+            if rp.shape != ((S + 127) // 128 + 1,):
+                raise ValueError("row_ptr must have ceil(S/128) + 1 entries")
+            rc = lib.attn_bwd_blocksparse(*args, rp.ctypes.data, ci.ctypes.data if ci.size else None,
+                                          _stream_handle(stream, q.device))
     if rc != 0:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv

@@ -804,10 +804,16 @@ int launch_bwd(const attn::BwdParams& bp, int dev, int ntiles, cudaStream_t st) 
 }
 }  // namespace
 
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
-                        double rope_base, void* stream) {
+int check_mask(const int* row_ptr, const int* col_idx, int nrows, bool causal);
+int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out);
+
+// The backward; row_ptr / col_idx: an optional host CSR block mask (null: dense).
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+             void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+             const int* row_ptr, const int* col_idx, void* stream) {
     int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, 0.0);
+    const int ntiles = (S + 127) / 128;
+    if (arc == ATTN_OK && row_ptr != nullptr) arc = check_mask(row_ptr, col_idx, ntiles, causal != 0);
     if (arc == ATTN_OK && (dO == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr))
         arc = ATTN_ERR_NULL;
     if (arc == ATTN_OK && (static_cast<long long>(B) * Hq > INT_MAX / 2)) arc = ATTN_ERR_SHAPE;
@@ -824,6 +830,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     float2* rope_tab = nullptr;
     float2* split_tab = nullptr;
     float* dlt = nullptr;
+    int* mask = nullptr;
+    const int nnz = row_ptr != nullptr ? row_ptr[ntiles] : 0;
     const size_t rows = static_cast<size_t>(B) * Hq * S;
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -843,6 +851,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
             ds.floats = rows;
         }
         dlt = ds.buf;
+        if (row_ptr != nullptr && (rc = get_mask(dev, row_ptr, col_idx, ntiles, &mask)) != ATTN_OK) return rc;
         bp.f.status = g_dev[dev].status;
     }
     if (!encode_bshd(&bp.f.tm_q, q, B, S, Hq, D) || !encode_bshd(&bp.f.tm_k, k, B, S, Hkv, D) ||
@@ -863,6 +872,10 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     bp.rot_base = rope ? split_tab : nullptr;
     bp.rot_row = rope ? split_tab + static_cast<size_t>((S + 31) / 32) * (D / 2) : nullptr;
     bp.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+    bp.q_ptr = mask;
+    bp.q_idx = mask != nullptr ? mask + ntiles + 1 : nullptr;
+    bp.k_ptr = mask != nullptr ? mask + ntiles + 1 + nnz : nullptr;
+    bp.k_idx = mask != nullptr ? mask + 2 * (ntiles + 1) + nnz : nullptr;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned dot_blocks = static_cast<unsigned>((rows + 7) / 8);
@@ -874,7 +887,6 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                                                                static_cast<const __nv_bfloat16*>(dO), dlt, B, S, Hq);
     cudaError_t e;
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("backward row-reduction launch", e);
-    const int ntiles = (S + 127) / 128;
     if (D == 128) {
         if (causal) return rope ? launch_bwd<128, true, true>(bp, dev, ntiles, st) : launch_bwd<128, true, false>(bp, dev, ntiles, st);
         return rope ? launch_bwd<128, false, true>(bp, dev, ntiles, st) : launch_bwd<128, false, false>(bp, dev, ntiles, st);
@@ -889,10 +901,29 @@ namespace {
 struct MaskEntry {
     int dev;
     std::vector<int> csr;  // row_ptr then col_idx, as given
-    int* d = nullptr;
+    int* d = nullptr;      // row_ptr | col_idx | col_ptr | row_idx (the same mask by columns)
 };
 std::vector<MaskEntry> g_masks;  // device copies of the block masks seen, by content
+}  // namespace
 
+// A CSR block mask over nrows x nrows tiles: row_ptr[0] = 0, non-decreasing; each row's columns
+// ascending, distinct, in range, and at most the row with the causal mask (tiles above the
+// diagonal hold no visible key).
+int check_mask(const int* row_ptr, const int* col_idx, int nrows, bool causal) {
+    if (row_ptr[0] != 0) return ATTN_ERR_SHAPE;
+    for (int r = 0; r < nrows; ++r) {
+        if (row_ptr[r + 1] < row_ptr[r]) return ATTN_ERR_SHAPE;
+        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
+            if (col_idx == nullptr) return ATTN_ERR_NULL;
+            const int cidx = col_idx[e];
+            if (cidx < 0 || cidx >= nrows || (causal && cidx > r) || (e > row_ptr[r] && cidx <= col_idx[e - 1]))
+                return ATTN_ERR_SHAPE;
+        }
+    }
+    return ATTN_OK;
+}
+
+// The device copy of a (checked) mask, with its column-major form; caller holds g_mu.
 int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out) {
     const int nnz = row_ptr[nrows];
     for (auto& e : g_masks) {
@@ -907,10 +938,20 @@ int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** o
     me.dev = dev;
     me.csr.assign(row_ptr, row_ptr + nrows + 1);
     me.csr.insert(me.csr.end(), col_idx, col_idx + nnz);
+    // by columns: col_ptr[c] .. col_ptr[c+1] list the rows that list c, ascending
+    std::vector<int> all(me.csr);
+    std::vector<int> col_ptr(nrows + 1, 0), row_idx(nnz);
+    for (int e = 0; e < nnz; ++e) ++col_ptr[col_idx[e] + 1];
+    for (int c = 0; c < nrows; ++c) col_ptr[c + 1] += col_ptr[c];
+    std::vector<int> fill(col_ptr.begin(), col_ptr.end() - 1);
+    for (int r = 0; r < nrows; ++r)
+        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e) row_idx[fill[col_idx[e]]++] = r;
+    all.insert(all.end(), col_ptr.begin(), col_ptr.end());
+    all.insert(all.end(), row_idx.begin(), row_idx.end());
     cudaError_t e;
-    if ((e = cudaMalloc(&me.d, me.csr.size() * sizeof(int))) != cudaSuccess)
+    if ((e = cudaMalloc(&me.d, all.size() * sizeof(int))) != cudaSuccess)
         return cuda_fail("cudaMalloc(block mask)", e, ATTN_ERR_OOM);
-    if ((e = cudaMemcpy(me.d, me.csr.data(), me.csr.size() * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) {
+    if ((e = cudaMemcpy(me.d, all.data(), all.size() * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) {
         cudaFree(me.d);
         return cuda_fail("cudaMemcpy(block mask)", e);
     }
@@ -918,6 +959,8 @@ int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** o
     g_masks.push_back(std::move(me));
     return ATTN_OK;
 }
+
+namespace {
 
 template <int D, bool CAUSAL, bool ROPE>
 int launch_bs(const attn::BsParams& bp, int dev, int nrows, cudaStream_t st) {
@@ -947,19 +990,8 @@ extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v,
                            (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
         arc = ATTN_ERR_ALIGN;
     if (arc != ATTN_OK) return arc;
-    // the mask: row_ptr[0] = 0, non-decreasing; each row's columns ascending, distinct, in range,
-    // and at most the row with the causal mask (tiles above the diagonal hold no visible key)
     const int nrows = (S + 127) / 128;
-    if (row_ptr[0] != 0) return ATTN_ERR_SHAPE;
-    for (int r = 0; r < nrows; ++r) {
-        if (row_ptr[r + 1] < row_ptr[r]) return ATTN_ERR_SHAPE;
-        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e) {
-            if (col_idx == nullptr) return ATTN_ERR_NULL;
-            const int cidx = col_idx[e];
-            if (cidx < 0 || cidx >= nrows || (causal && cidx > r) || (e > row_ptr[r] && cidx <= col_idx[e - 1]))
-                return ATTN_ERR_SHAPE;
-        }
-    }
+    if ((arc = check_mask(row_ptr, col_idx, nrows, causal != 0)) != ATTN_OK) return arc;
     const bool rope = rope_base > 0.0 && std::isfinite(rope_base);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
@@ -995,6 +1027,20 @@ extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v,
     }
     if (causal) return rope ? launch_bs<64, true, true>(bp, dev, nrows, st) : launch_bs<64, true, false>(bp, dev, nrows, st);
     return rope ? launch_bs<64, false, true>(bp, dev, nrows, st) : launch_bs<64, false, false>(bp, dev, nrows, st);
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
+                        double rope_base, void* stream) {
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, rope_base, nullptr, nullptr, stream);
+}
+
+extern "C" int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                    const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
+                                    int D, int causal, double rope_base, const int* row_ptr, const int* col_idx,
+                                    void* stream) {
+    if (row_ptr == nullptr) return ATTN_ERR_NULL;
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, rope_base, row_ptr, col_idx, stream);
 }
 
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,

@@ -36,6 +36,12 @@ struct BwdParams {
     const float2* rot_base; // (cos, sin)(32*m*theta_r), [m][r] (RoPE only)
     const float2* rot_row;  // (cos, sin)(rr*theta_r), [rr][r], rr < 32
     float inv_sqrt_d;
+    // block mask (null: dense).  The dQ kernel walks row i's listed key tiles (CSR), the dK/dV
+    // kernel key tile j's listed query tiles (the same mask by columns).
+    const int* q_ptr;       // [ntiles + 1]
+    const int* q_idx;
+    const int* k_ptr;       // [ntiles + 1]
+    const int* k_idx;
 };
 
 // Dlt for every row: one warp per (b, s, h) row of O and dO; dlt is [B][H][S].
@@ -110,16 +116,23 @@ __device__ __forceinline__ void bwd_factor2(const BwdParams& p, int pos, int r, 
 
 // Epilogue of one row held in TMEM columns [taddr, taddr + D): scale, rotate back by the row's
 // position (RoPE), round to bf16 and store D contiguous elements at dst.
+// zero: the tile saw no listed block; the row is 0 and TMEM is not read.
 template <int D, bool ROPE>
 __device__ __forceinline__ void bwd_store_row(const BwdParams& p, uint32_t taddr, float scale, int pos, bool store,
-                                              __nv_bfloat16* dst, int c_begin = 0, int c_end = D / 2) {
+                                              __nv_bfloat16* dst, int c_begin = 0, int c_end = D / 2,
+                                              bool zero = false) {
     constexpr int kHalf = D / 2;
 #pragma unroll
     for (int c0 = 0; c0 < kHalf; c0 += 32) {
         if (c0 < c_begin || c0 >= c_end) continue;  // pairs [c_begin, c_end) of this thread's share
         uint32_t x[32], y[32];
-        tmem_load_32(taddr + c0, x);
-        tmem_load_32(taddr + kHalf + c0, y);
+        if (zero) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = y[e] = 0u;
+        } else {
+            tmem_load_32(taddr + c0, x);
+            tmem_load_32(taddr + kHalf + c0, y);
+        }
         uint32_t px[16], py[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -273,8 +286,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const int G = f.Hq / f.Hkv;
     const int kv0 = j * 128;
     const int i_lo = CAUSAL ? j : 0;
-    const int per_head = ntiles - i_lo;
-    const int iters = G * per_head;  // iteration it: head g*G + it / per_head, query tile i_lo + it % per_head
+    const int lbase = p.k_ptr != nullptr ? p.k_ptr[j] : 0;
+    const int per_head = p.k_ptr != nullptr ? p.k_ptr[j + 1] - lbase : ntiles - i_lo;
+    const int iters = G * per_head;  // iteration it: head g*G + it / per_head, query tile qtile(it % per_head)
+    auto qtile = [&](int x) { return p.k_ptr != nullptr ? p.k_idx[lbase + x] : i_lo + x; };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -305,7 +320,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         bool ok = true;
         for (int it = 0; it < iters && ok; ++it) {
             const int s = it & 1;
-            const int q0 = (i_lo + it % per_head) * 128;
+            const int q0 = qtile(it % per_head) * 128;
             ok = bwd_wait(bar_at(bar0, BB_STR_FULL + s), (it >> 1) & 1, ctl, kStatusSoftmax);  // per-column values
             if (!ok) break;
             ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
@@ -322,15 +337,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
         }
-        if (ok && bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax)) {
+        const bool none = iters == 0;  // no listed query tile: dK = dV = 0
+        if (ok && (none || bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax))) {
             tc_fence_after();
             const int key = kv0 + t;
             const bool store = key < f.S;
             const size_t off = ((static_cast<size_t>(b) * f.S + (store ? key : 0)) * f.Hkv + g) * D;
             if (half == 0)
-                bwd_store_row<D, false>(p, tdV, 1.0f, key, store, p.dv + off);
+                bwd_store_row<D, false>(p, tdV, 1.0f, key, store, p.dv + off, 0, D / 2, none);
             else
-                bwd_store_row<D, ROPE>(p, tdK, p.inv_sqrt_d, key, store, p.dk + off);
+                bwd_store_row<D, ROPE>(p, tdK, p.inv_sqrt_d, key, store, p.dk + off, 0, D / 2, none);
         }
     } else if (warp < kBwdWarpTma) {
         // ---- RoPE warps: the resident K tile once, then each streamed Q tile
@@ -348,7 +364,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             }
             for (int it = 0; it < iters && ok; ++it) {
                 const int s = it & 1;
-                rope_load_base<D>(f, i_lo + it % per_head, t, cb, sb);
+                rope_load_base<D>(f, qtile(it % per_head), t, cb, sb);
                 ok = bwd_wait(bar_at(bar0, BB_STR_FULL + s), (it >> 1) & 1, ctl, kStatusRope);
                 if (!ok) break;
                 rope_rotate_tile<D, false>(smg + L::kStr0 + s * 2 * L::kTile, k, cb, sb, t);
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         for (int it = 0; it < iters; ++it) {
             const int s = it & 1, n = it >> 1;
             const int h = g * G + it / per_head;
-            const int q0 = (i_lo + it % per_head) * 128;
+            const int q0 = qtile(it % per_head) * 128;
             // the tile's per-row values are read before the slot frees up, off the refill's path
             const float* lse_row = p.lse + (static_cast<size_t>(b) * f.Hq + h) * f.S;
             const float* dlt_row = p.dlt + (static_cast<size_t>(b) * f.Hq + h) * f.S;
@@ -481,7 +497,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const int b = blockIdx.x / f.Hq, h = blockIdx.x % f.Hq;
     const int g = h / (f.Hq / f.Hkv);
     const int q0 = i * 128;
-    const int iters = CAUSAL ? i + 1 : ntiles;  // iteration it: key tile it
+    const int lbase = p.q_ptr != nullptr ? p.q_ptr[i] : 0;
+    const int iters = p.q_ptr != nullptr ? p.q_ptr[i + 1] - lbase : (CAUSAL ? i + 1 : ntiles);
+    auto ktile = [&](int x) { return p.q_ptr != nullptr ? p.q_idx[lbase + x] : x; };  // key tile of iteration x
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -518,7 +536,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
             if (!ok) break;
             tc_fence_after();
-            const int lim = q0 + t - (it * 128 + 64 * half);  // key columns c > lim follow the query
+            const int lim = q0 + t - (ktile(it) * 128 + 64 * half);  // key columns c > lim follow the query
             const uint32_t hS = tS + 64u * half, hdP = tdP + 64u * half;
             if (CAUSAL && __any_sync(0xffffffffu, lim < 63))
                 bwd_ew_row<ROPE, true>(hS, hdP, l2, dl, c, lim);
@@ -528,14 +546,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
         }
-        if (ok && bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax)) {
+        const bool none = iters == 0;  // no listed key tile: dQ = 0
+        if (ok && (none || bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax))) {
             tc_fence_after();
             const bool store = row < f.S;
             const size_t off = ((static_cast<size_t>(b) * f.S + (store ? row : 0)) * f.Hq + h) * D;
             // each warpgroup stores its share of the row's pairs (all of them at D = 64: one share)
             if (D == 128 || half == 0)
                 bwd_store_row<D, ROPE>(p, tdQ, p.inv_sqrt_d, row, store, p.dq + off, D == 128 ? 32 * half : 0,
-                                       D == 128 ? 32 * half + 32 : D / 2);
+                                       D == 128 ? 32 * half + 32 : D / 2, none);
         }
     } else if (warp < kBwdWarpTma) {
         // ---- RoPE warps: the resident Q tile once, then each streamed K tile
@@ -553,7 +572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             }
             for (int it = 0; it < iters && ok; ++it) {
                 const int s = it & 1;
-                rope_load_base<D>(f, it, t, cb, sb);
+                rope_load_base<D>(f, ktile(it), t, cb, sb);
                 ok = bwd_wait(bar_at(bar0, BB_STR_FULL + s), (it >> 1) & 1, ctl, kStatusRope);
                 if (!ok) break;
                 rope_rotate_tile<D, false>(smg + L::kStr0 + s * 2 * L::kTile, k, cb, sb, t);
@@ -579,8 +598,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                 const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile;
 #pragma unroll
                 for (int sub = 0; sub < D / 64; ++sub) {
-                    tma_load_4d(ka + sub * kSubTileBytes, &f.tm_k, fb, sub * 64, g, it * 128, b);
-                    tma_load_4d(ka + L::kTile + sub * kSubTileBytes, &f.tm_v, fb, sub * 64, g, it * 128, b);
+                    tma_load_4d(ka + sub * kSubTileBytes, &f.tm_k, fb, sub * 64, g, ktile(it) * 128, b);
+                    tma_load_4d(ka + L::kTile + sub * kSubTileBytes, &f.tm_v, fb, sub * 64, g, ktile(it) * 128, b);
                 }
             }
         }

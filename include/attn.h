@@ -250,6 +250,21 @@ int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, f
                          void* stream);
 
 /*
+ * attn_bwd_blocksparse — attn_bwd under the block mask of
+ * attn_fwd_blocksparse ("AttnFuse", sec. 4.3: the backward also iterates
+ * only over active blocks).  The dQ kernel walks each row's listed key
+ * tiles, the dK/dV kernel each key tile's listing rows (the library builds
+ * that column-major copy with the device copy of the mask).  o and lse are
+ * attn_fwd_blocksparse's outputs.  A query row that sees no key gets dQ = 0
+ * and passes nothing to dK, dV; a key tile no row lists gets dK = dV = 0.
+ * Arguments and errors: as attn_bwd, plus the mask of attn_fwd_blocksparse
+ * (ATTN_ERR_NULL without row_ptr, ATTN_ERR_SHAPE for a malformed mask).
+ */
+int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D,
+                         int causal, double rope_base, const int* row_ptr, const int* col_idx, void* stream);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

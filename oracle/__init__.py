@@ -52,6 +52,9 @@ def _load():
             lib.oracle_rope_rotate.argtypes = [u16p] + [ctypes.c_int] * 4 + [ctypes.c_double, f64p]
             lib.oracle_attn_bwd.restype = ctypes.c_int
             lib.oracle_attn_bwd.argtypes = [f64p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_double] + [f64p] * 3
+            lib.oracle_attn_bwd_bs.restype = ctypes.c_int
+            lib.oracle_attn_bwd_bs.argtypes = [f64p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int,
+                                                                                  i32p, i32p] + [f64p] * 3
             lib.oracle_attn_rows_bs.restype = ctypes.c_int
             lib.oracle_attn_rows_bs.argtypes = [u16p, u16p, u16p] + [ctypes.c_int] * 6 + [
                 ctypes.c_double, ctypes.c_int, i32p, i32p, ctypes.c_int, i32p, i32p, i32p, f64p, f64p]
@@ -137,10 +140,11 @@ def bf16_to_f64(x) -> np.ndarray:
     return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def attn_bwd(q, k, v, dO, *, causal=True, rope_base=None):
+def attn_bwd(q, k, v, dO, *, causal=True, rope_base=None, block_mask=None, block=128):
     """dQ [B,S,Hq,D], dK, dV [B,S,Hkv,D] (float64) of sum(O * dO) for the attention forward.
 
     q, k, v, dO: uint16 bf16 bits (widened exactly) or float64 arrays, BSHD.
+    block_mask: optional CSR (row_ptr, col_idx) over block x block tiles.
     """
     def f64(a):
         return bf16_to_f64(a) if a.dtype == np.uint16 else np.ascontiguousarray(a, dtype=np.float64)
@@ -150,10 +154,15 @@ def attn_bwd(q, k, v, dO, *, causal=True, rope_base=None):
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
-    rc = _load().oracle_attn_bwd(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
-                                 _ptr(dO, ctypes.c_double), B, Hq, Hkv, S, D, 1 if causal else 0,
-                                 float(rope_base) if rope_base else 0.0, _ptr(dq, ctypes.c_double),
-                                 _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double))
+    args = (_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
+            _ptr(dO, ctypes.c_double), B, Hq, Hkv, S, D, 1 if causal else 0, float(rope_base) if rope_base else 0.0)
+    outs = (_ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double))
+    if block_mask is None:
+        rc = _load().oracle_attn_bwd(*args, *outs)
+    else:
+        rp = np.ascontiguousarray(block_mask[0], dtype=np.int32)
+        ci = np.ascontiguousarray(block_mask[1], dtype=np.int32) if len(block_mask[1]) else np.zeros(1, np.int32)
+        rc = _load().oracle_attn_bwd_bs(*args, int(block), _ptr(rp, ctypes.c_int), _ptr(ci, ctypes.c_int), *outs)
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dq, dk, dv

@@ -259,9 +259,10 @@ long long oracle_pruned_terms(int S, int D, double rope_base, double window_k) {
  * Outputs dq [B][S][Hq][D], dk, dv [B][S][Hkv][D], float64.
  * Returns 0, or -1 on bad arguments.
  */
-int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dO,
-                    int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
-                    double* dq, double* dk, double* dv) {
+static int attn_bwd_masked(const double* q, const double* k, const double* v, const double* dO,
+                           int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                           const char* active, int block, int nb,
+                           double* dq, double* dk, double* dv) {
     if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 1024) return -1;
     const int rope_on = rope_base > 0.0;
     const int G = Hq / Hkv;
@@ -301,6 +302,8 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
         for (int h = g * G; h < (g + 1) * G; ++h) {
             for (int i = 0; i < S; ++i) {
                 const int last = causal ? i : S - 1;
+                /* key j is visible iff j <= last and (no mask, or block (i/block, j/block) listed) */
+#define VISIBLE(j) (active == NULL || active[(size_t)(i / block) * nb + (j) / block])
                 const double* qi = q + (((size_t)b * S + i) * Hq + h) * D;
                 const double* doi = dO + (((size_t)b * S + i) * Hq + h) * D;
                 for (int r = 0; r < half; ++r) {
@@ -317,6 +320,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                 /* probabilities of row i */
                 double m = -INFINITY;
                 for (int j = 0; j <= last; ++j) {
+                    if (!VISIBLE(j)) continue;
                     double acc = 0.0;
                     for (int d = 0; d < D; ++d) acc += qr[d] * kr[(size_t)j * D + d];
                     p[j] = acc * inv_sqrt_d;
@@ -324,8 +328,13 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                 }
                 double l = 0.0;
                 for (int j = 0; j <= last; ++j) {
-                    p[j] = exp(p[j] - m);
+                    p[j] = VISIBLE(j) ? exp(p[j] - m) : 0.0; /* a hidden key has probability 0 */
                     l += p[j];
+                }
+                if (l == 0.0) { /* a row that sees no key: no gradient flows through it */
+                    double* dqi = dq + (((size_t)b * S + i) * Hq + h) * D;
+                    for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+                    continue;
                 }
                 for (int j = 0; j <= last; ++j) p[j] /= l;
                 /* dV, dP and the row's Dlt */
@@ -344,6 +353,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                 /* dS, then the gradients wrt the rotated q and k */
                 for (int d = 0; d < D; ++d) dqr[d] = 0.0;
                 for (int j = 0; j <= last; ++j) {
+                    if (!VISIBLE(j)) continue;
                     const double ds = p[j] * (dp[j] - dlt) * inv_sqrt_d;
                     for (int d = 0; d < D; ++d) {
                         dqr[d] += ds * kr[(size_t)j * D + d];
@@ -388,7 +398,40 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
         free(p);
         free(dp);
     }
+#undef VISIBLE
     return 0;
+}
+
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dO,
+                    int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                    double* dq, double* dk, double* dv) {
+    return attn_bwd_masked(q, k, v, dO, B, Hq, Hkv, S, D, causal, rope_base, NULL, 1, 1, dq, dk, dv);
+}
+
+/*
+ * The same gradients under a block-sparse mask ("AttnFuse", sec. 4.3: the
+ * backward also sees only the listed blocks): key j is visible to query i iff
+ * block (i / block, j / block) is listed in the CSR mask (and j <= i when
+ * causal); hidden keys have probability 0, and a row that sees no key passes
+ * no gradient.  Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_bwd_bs(const double* q, const double* k, const double* v, const double* dO,
+                       int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                       int block, const int* row_ptr, const int* col_idx,
+                       double* dq, double* dk, double* dv) {
+    if (block < 1 || S < 1) return -1;
+    const int nb = (S + block - 1) / block;
+    for (int r = 0; r < nb; ++r) {
+        if (row_ptr[r + 1] < row_ptr[r]) return -1;
+        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e)
+            if (col_idx[e] < 0 || col_idx[e] >= nb) return -1;
+    }
+    char* active = (char*)calloc((size_t)nb * nb, 1);
+    for (int r = 0; r < nb; ++r)
+        for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e) active[(size_t)r * nb + col_idx[e]] = 1;
+    const int rc = attn_bwd_masked(q, k, v, dO, B, Hq, Hkv, S, D, causal, rope_base, active, block, nb, dq, dk, dv);
+    free(active);
+    return rc;
 }
 
 /*

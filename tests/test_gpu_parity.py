@@ -404,3 +404,28 @@ def test_blocksparse_full_mask_matches_dense_forward():
     attn.attn_check()
     assert (o.float() - o_d.float()).abs().max().item() <= 1e-2
     assert (lse - lse_d).abs().max().item() <= 1e-3
+
+
+BS_BWD = [
+    # B, Hq, Hkv, S, D, causal, rope_base, mask
+    (1, 4, 2, 1000, 128, False, 10000.0, "bigbird"),
+    (1, 2, 2, 640, 128, True, 10000.0, "bigbird"),
+    (2, 2, 1, 384, 64, False, None, "empty_row"),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base,kind", BS_BWD)
+def test_blocksparse_backward_matches_oracle(B, Hq, Hkv, S, D, causal, base, kind):
+    """attn_bwd under a block mask, on attn_fwd_blocksparse's own O and LSE, against the masked chain rule."""
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=800 + S)
+    dO = si.bshd_bf16(801 + S, 9, B, S, Hq, D)
+    rp, ci = _bs_mask(kind, S, causal)
+    qd, kd, vd, dOd = _dev(q), _dev(k), _dev(v), _dev(dO)
+    o, lse = attn.attn_fwd_blocksparse(qd, kd, vd, rp, ci, causal=causal, rope_base=base)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dOd, causal=causal, rope_base=base, block_mask=(rp, ci))
+    attn.attn_check()
+    rq, rk, rv = oracle.attn_bwd(q, k, v, dO, causal=causal, rope_base=base, block_mask=(rp, ci))
+    tag = f"block-sparse backward {kind} S={S}"
+    _check_grad(dv.float().cpu().numpy(), rv, tag + " dV")
+    _check_grad(dk.float().cpu().numpy(), rk, tag + " dK")
+    _check_grad(dq.float().cpu().numpy(), rq, tag + " dQ")

@@ -156,3 +156,60 @@ def test_gqa_backward_equals_mha_with_repeated_kv():
     np.testing.assert_allclose(dq, dq2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(dk, dk2.reshape(1, 17, 2, 2, 16).sum(axis=3), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dv, dv2.reshape(1, 17, 2, 2, 16).sum(axis=3), rtol=0, atol=1e-12)
+
+
+def _mask_autograd_ref(q, k, v, dO, causal, base, cell):
+    """torch autograd through float64 SDPA with a cell mask; rows that see nothing are left out."""
+    G = q.shape[2] // k.shape[2]
+    qt, kt, vt = (torch.from_numpy(oracle.bf16_to_f64(a)).requires_grad_(True) for a in (q, k, v))
+    qr = _rope_torch(qt, base) if base else qt
+    kr = _rope_torch(kt, base) if base else kt
+    qh = qr.permute(0, 2, 1, 3)
+    kh = kr.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    vh = vt.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    seen = torch.from_numpy(cell.any(axis=1))
+    s = torch.matmul(qh, kh.transpose(-1, -2)) / math.sqrt(q.shape[-1])
+    s = s.masked_fill(~torch.from_numpy(cell), float("-inf"))
+    pr = torch.softmax(s[..., seen, :], dim=-1)
+    o = torch.matmul(pr, vh)
+    dOt = torch.from_numpy(oracle.bf16_to_f64(dO)).permute(0, 2, 1, 3)[..., seen, :]
+    (o * dOt).sum().backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+@pytest.mark.parametrize("causal,base", [(False, 10000.0), (True, None)])
+def test_block_sparse_backward_equals_masked_autograd(causal, base):
+    """Under a CSR block mask (with one empty block row): torch autograd with the expanded cell mask."""
+    S, blk = 37, 8
+    q, k, v, dO = _inputs(1, 4, 2, S, 16, seed=31)
+    nb = (S + blk - 1) // blk
+    rows = [[0, 2], [1], [], [0, 3], [1, 2, 4]]
+    if causal:
+        rows = [[c for c in r if c <= i] for i, r in enumerate(rows)]
+    rp = np.zeros(nb + 1, np.int32)
+    rp[1:] = np.cumsum([len(r) for r in rows])
+    ci = np.array([c for r in rows for c in r], np.int32)
+    act = np.zeros((nb, nb), bool)
+    for i, r in enumerate(rows):
+        act[i, r] = True
+    cell = act[np.arange(S)[:, None] // blk, np.arange(S)[None, :] // blk]
+    if causal:
+        cell &= np.tril(np.ones((S, S), bool))
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dO, causal=causal, rope_base=base, block_mask=(rp, ci), block=blk)
+    rq, rk, rv = _mask_autograd_ref(q, k, v, dO, causal, base, cell)
+    np.testing.assert_allclose(dq, rq, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, rk, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, rv, rtol=0, atol=1e-11)
+    assert np.all(dq[:, 16:24] == 0.0)  # block row 2 sees nothing
+
+
+def test_block_sparse_backward_with_every_block_is_dense():
+    S, blk = 40, 16
+    q, k, v, dO = _inputs(1, 2, 1, S, 16, seed=32)
+    nb = (S + blk - 1) // blk
+    rp = np.arange(nb + 1, dtype=np.int32) * nb
+    ci = np.tile(np.arange(nb, dtype=np.int32), nb)
+    a = oracle.attn_bwd(q, k, v, dO, causal=True, rope_base=10000.0, block_mask=(rp, ci), block=blk)
+    b = oracle.attn_bwd(q, k, v, dO, causal=True, rope_base=10000.0)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)

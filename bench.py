@@ -468,7 +468,15 @@ def run_backward(args, w, rank, world, local_rank):
     q, k, v, dO = (torch.from_numpy(x).view(torch.bfloat16).to(dev) for x in (q_h, k_h, v_h, do_h))
     stream = torch.cuda.current_stream(dev)
     kw = dict(causal=w["causal"], rope_base=w["rope_base"], stream=stream)
-    o, lse = attn.attn_fwd(q, k, v, **kw)
+    mask = None
+    if args.blocksparse:  # the backward of the block-sparse forward, over the workload's mask
+        if "block_mask" not in w:
+            raise SystemExit("--blocksparse needs a workload with a block mask (bigbird_s4096)")
+        mask = si.bigbird_block_mask(S, causal=w["causal"], **w["block_mask"])
+        o, lse = attn.attn_fwd_blocksparse(q, k, v, *mask, **kw)
+        kw["block_mask"] = mask
+    else:
+        o, lse = attn.attn_fwd(q, k, v, **kw)
     for _ in range(max(args.warmup, 3)):
         attn.attn_bwd(q, k, v, o, lse, dO, **kw)
     attn.attn_check(stream=stream, device=dev)
@@ -484,13 +492,17 @@ def run_backward(args, w, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
     ms = float(np.median([a.elapsed_time(b) for a, b in times]))
-    # useful backward work: 2.5 x the forward's 2*B*Hq*S^2*D causal FLOPs (dV, dP, dQ, dK and the
-    # recomputed S); the kernels execute 7/5 of it, S and dP being formed in both tile kernels
-    flops = 2.5 * 2.0 * B * Hq * S * S * D * (1.0 if w["causal"] else 2.0)
+    # useful backward work: 2.5 x the forward's 4*D FLOPs per visible (query, key) pair (dV, dP, dQ, dK
+    # and the recomputed S); the kernels execute 7/5 of it, S and dP being formed in both tile kernels
+    pairs = visible_pairs(S, *mask, w["causal"]) if mask is not None else S * S * (0.5 if w["causal"] else 1.0)
+    flops = 2.5 * 4.0 * D * pairs * B * Hq
     tf = flops / (ms * 1e-3) / 1e12
     peaks, _ = load_peaks()
     cfg = workload_config(args.workload, w)
     cfg["step"] = "backward: dO.O rows, dK/dV kernel, dQ kernel on the forward's O and LSE"
+    if mask is not None:
+        cfg["step"] += ", over the block mask"
+        cfg["active_blocks"] = int(mask[0][-1])
     cfg["l2"] = "inputs larger than L2" if 4 * q.numel() * 2 > (256 << 20) else "inputs may stay in L2 between steps"
     return {
         "metric": "attention backward TFLOP/s", "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -499,7 +511,8 @@ def run_backward(args, w, rank, world, local_rank):
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": float(peaks["bf16_tflops"]),
                      "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4), "traffic": None,
                      "kernel": "bwd_dot_kernel + bwd_dkdv_kernel + bwd_dq_kernel",
-                     "algorithmic": "5*B*Hq*S^2*D useful causal FLOPs per step, median step time"},
+                     "algorithmic": "10*D FLOPs per visible (query, key) pair and head (2.5 x the forward's), "
+                                    "median step time"},
         "gpu_launches": 3 * args.steps, "clocks": clocks.summary(),
     }
 
@@ -657,7 +670,7 @@ def main():
         line = run_decode(args, w, rank, world, local_rank)
     elif args.backward:
         line = run_backward(args, w, rank, world, local_rank)
-    elif args.blocksparse:
+    elif args.blocksparse:  # forward; with --backward the branch above times its backward
         line = run_blocksparse(args, w, rank, world, local_rank)
     else:
         line = run_ours(args, w, rank, world, local_rank)

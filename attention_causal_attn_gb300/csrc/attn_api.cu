@@ -796,9 +796,9 @@ int launch_bwd(const attn::BwdParams& bp, int dev, int ntiles, cudaStream_t st) 
         g_bwd_configured[dev] |= bit;
     }
     const int B = bp.f.B, Hq = bp.f.Hq, Hkv = bp.f.Hkv;
-    kv<<<dim3(static_cast<unsigned>(B * Hkv), static_cast<unsigned>(ntiles)), attn::kBwdThreads, smem, st>>>(bp);
+    kv<<<static_cast<unsigned>(static_cast<long long>(B) * Hkv * ntiles), attn::kBwdThreads, smem, st>>>(bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("dK/dV kernel launch", e);
-    kq<<<dim3(static_cast<unsigned>(B * Hq), static_cast<unsigned>(ntiles)), attn::kBwdThreads, smem, st>>>(bp);
+    kq<<<static_cast<unsigned>(static_cast<long long>(B) * Hq * ntiles), attn::kBwdThreads, smem, st>>>(bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("dQ kernel launch", e);
     return ATTN_OK;
 }
@@ -816,7 +816,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     if (arc == ATTN_OK && row_ptr != nullptr) arc = check_mask(row_ptr, col_idx, ntiles, causal != 0);
     if (arc == ATTN_OK && (dO == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr))
         arc = ATTN_ERR_NULL;
-    if (arc == ATTN_OK && (static_cast<long long>(B) * Hq > INT_MAX / 2)) arc = ATTN_ERR_SHAPE;
+    if (arc == ATTN_OK && static_cast<long long>(B) * Hq * ((S + 127) / 128) > INT_MAX) arc = ATTN_ERR_SHAPE;  // CTAs
     if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
                            !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
                            (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
@@ -872,6 +872,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     bp.rot_base = rope ? split_tab : nullptr;
     bp.rot_row = rope ? split_tab + static_cast<size_t>((S + 31) / 32) * (D / 2) : nullptr;
     bp.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+    bp.head_major = mask == nullptr ? 1 : 0;
     bp.q_ptr = mask;
     bp.q_idx = mask != nullptr ? mask + ntiles + 1 : nullptr;
     bp.k_ptr = mask != nullptr ? mask + ntiles + 1 + nnz : nullptr;
@@ -974,7 +975,7 @@ int launch_bs(const attn::BsParams& bp, int dev, int nrows, cudaStream_t st) {
             return cuda_fail("cudaFuncSetAttribute(block-sparse)", e);
         g_bwd_configured[dev] |= bit;
     }
-    kern<<<dim3(static_cast<unsigned>(bp.f.B * bp.f.Hq), static_cast<unsigned>(nrows)), attn::kBsThreads, smem, st>>>(bp);
+    kern<<<static_cast<unsigned>(static_cast<long long>(bp.f.B) * bp.f.Hq * nrows), attn::kBsThreads, smem, st>>>(bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("block-sparse kernel launch", e);
     return ATTN_OK;
 }
@@ -985,7 +986,7 @@ extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v,
                                     const int* col_idx, void* stream) {
     int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, 0.0);
     if (arc == ATTN_OK && row_ptr == nullptr) arc = ATTN_ERR_NULL;
-    if (arc == ATTN_OK && (static_cast<long long>(B) * Hq > INT_MAX / 2)) arc = ATTN_ERR_SHAPE;
+    if (arc == ATTN_OK && static_cast<long long>(B) * Hq * ((S + 127) / 128) > INT_MAX) arc = ATTN_ERR_SHAPE;  // CTAs
     if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
                            (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
         arc = ATTN_ERR_ALIGN;

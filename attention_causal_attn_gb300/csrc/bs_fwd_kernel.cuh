@@ -2,8 +2,9 @@
 // a CSR BlockMask lists the active key blocks of each row of blocks, and the
 // kernel visits only those, so its work is proportional to the active share).
 //
-// Blocks are the kernel's 128 x 128 tiles.  CTA (b * Hq + h, i) computes query
-// tile i of head h: Q is loaded and rotated once, then the listed key tiles
+// Blocks are the kernel's 128 x 128 tiles.  CTA i * (B * Hq) + b * Hq + h
+// computes query tile i of head h (tile by tile across heads, so a mask's
+// heavy rows start first): Q is loaded and rotated once, then the listed key tiles
 // are streamed (two slots) in descending order, each through
 //   S = Q K^T (tcgen05, TMEM)  ->  online softmax, P in bf16 over S  ->  O += P V.
 // Roles as in the backward kernels: one elementwise warpgroup (one thread per
@@ -47,8 +48,9 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smg + L::kMisc + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const FwdParams& f = p.f;
-    const int i = blockIdx.y;
-    const int b = blockIdx.x / f.Hq, h = blockIdx.x % f.Hq;
+    const int bhs = f.B * f.Hq;
+    const int i = static_cast<int>(blockIdx.x / bhs);
+    const int b = static_cast<int>(blockIdx.x % bhs) / f.Hq, h = static_cast<int>(blockIdx.x % bhs) % f.Hq;
     const int g = h / (f.Hq / f.Hkv);
     const int q0 = i * 128;
     const int e0 = p.row_ptr[i];

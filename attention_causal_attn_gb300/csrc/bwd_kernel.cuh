@@ -42,7 +42,22 @@ struct BwdParams {
     const int* q_idx;
     const int* k_ptr;       // [ntiles + 1]
     const int* k_idx;
+    // CTA order: 1 = a head's tiles together (they share the streamed tiles in L2; dense masks),
+    // 0 = tile by tile across heads (a mask's heavy rows or columns first)
+    int head_major;
 };
+
+// (tile, batch-head) of CTA x among bh batch-heads x ntiles tiles, in the order p.head_major picks.
+__device__ __forceinline__ void bwd_cta_coords(const BwdParams& p, int bh, int ntiles, int& tile, int& bhi) {
+    const long long x = blockIdx.x;
+    if (p.head_major) {
+        tile = static_cast<int>(x % ntiles);
+        bhi = static_cast<int>(x / ntiles);
+    } else {
+        tile = static_cast<int>(x / bh);
+        bhi = static_cast<int>(x % bh);
+    }
+}
 
 // Dlt for every row: one warp per (b, s, h) row of O and dO; dlt is [B][H][S].
 template <int D>
@@ -265,9 +280,10 @@ __device__ __forceinline__ void bwd_init_bars(uint32_t bar0, uint32_t p_count = 
     fence_proxy_async_smem();
 }
 
-// dK and dV of one 128-key tile j of KV head g: CTA (b * Hkv + g, j) walks the query tiles
-// i >= j (all of them without the causal mask) of each of the group's query heads; the
-// heaviest tiles (small j) are launched first.
+// dK and dV of one 128-key tile j of KV head g (CTA order: bwd_cta_coords) walk the query tiles
+// i >= j (all of them without the causal mask) of each of the group's query heads.  With the
+// head-major order the CTAs of one KV head run together and read the Q and dO tiles they all
+// stream from L2 rather than HBM.
 // TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).
 template <int D, bool CAUSAL, bool ROPE>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
@@ -281,8 +297,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const FwdParams& f = p.f;
     const int ntiles = (f.S + 127) / 128;
-    const int j = blockIdx.y;
-    const int b = blockIdx.x / f.Hkv, g = blockIdx.x % f.Hkv;
+    int j, bg;
+    bwd_cta_coords(p, f.B * f.Hkv, ntiles, j, bg);
+    const int b = bg / f.Hkv, g = bg % f.Hkv;
     const int G = f.Hq / f.Hkv;
     const int kv0 = j * 128;
     const int i_lo = CAUSAL ? j : 0;
@@ -478,8 +495,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     }
 }
 
-// dQ of one 128-row query tile i of head h: CTA (b * Hq + h, y) walks the key tiles j <= i (all
-// of them without the causal mask); with the mask the heaviest tiles go first (i = ntiles-1-y).
+// dQ of one 128-row query tile i of head h (CTA order: bwd_cta_coords) walks the key tiles j <= i
+// (all of them without the causal mask); the heaviest tiles go first under the causal mask
+// (i = ntiles-1-y).
 // TMEM: S [0,128), dP [128,256), dQ [256, 256+D).
 template <int D, bool CAUSAL, bool ROPE>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -493,8 +511,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const FwdParams& f = p.f;
     const int ntiles = (f.S + 127) / 128;
-    const int i = CAUSAL ? ntiles - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
-    const int b = blockIdx.x / f.Hq, h = blockIdx.x % f.Hq;
+    int y, bh;
+    bwd_cta_coords(p, f.B * f.Hq, ntiles, y, bh);
+    const int i = (CAUSAL && p.q_ptr == nullptr) ? ntiles - 1 - y : y;
+    const int b = bh / f.Hq, h = bh % f.Hq;
     const int g = h / (f.Hq / f.Hkv);
     const int q0 = i * 128;
     const int lbase = p.q_ptr != nullptr ? p.q_ptr[i] : 0;

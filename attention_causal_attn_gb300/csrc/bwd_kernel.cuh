@@ -189,8 +189,10 @@ __device__ __forceinline__ void bwd_ew_cols(uint32_t tS, uint32_t tdP, const flo
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 32) {
         uint32_t rs[32], rd[32];
-        tmem_load_32(tS + cc, rs);
-        tmem_load_32(tdP + cc, rd);
+        tmem_load_32_async(tS + cc, rs);  // both loads in flight, one wait
+        tmem_load_32_async(tdP + cc, rd);
+        tmem_wait_ld_32(rs);
+        tmem_wait_ld_32(rd);
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -220,8 +222,10 @@ __device__ __forceinline__ void bwd_ew_row(uint32_t tS, uint32_t tdP, float l2, 
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 32) {
         uint32_t rs[32], rd[32];
-        tmem_load_32(tS + cc, rs);
-        tmem_load_32(tdP + cc, rd);
+        tmem_load_32_async(tS + cc, rs);  // both loads in flight, one wait
+        tmem_load_32_async(tdP + cc, rd);
+        tmem_wait_ld_32(rs);
+        tmem_wait_ld_32(rd);
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {

@@ -58,6 +58,9 @@ def _load():
             lib.oracle_attn_rows_bs.restype = ctypes.c_int
             lib.oracle_attn_rows_bs.argtypes = [u16p, u16p, u16p] + [ctypes.c_int] * 6 + [
                 ctypes.c_double, ctypes.c_int, i32p, i32p, ctypes.c_int, i32p, i32p, i32p, f64p, f64p]
+            lib.oracle_attn_rows_local.restype = ctypes.c_int
+            lib.oracle_attn_rows_local.argtypes = [u16p, u16p, u16p] + [ctypes.c_int] * 6 + [
+                ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, i32p, i32p, f64p, f64p]
             lib.oracle_threads.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -194,4 +197,31 @@ def attn_full_bs(q, k, v, row_ptr, col_idx, **kw):
     B, S, Hq, D = q.shape
     bb, hh, ii = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(S), indexing="ij")
     o, lse = attn_rows_bs(q, k, v, row_ptr, col_idx, bb.ravel(), hh.ravel(), ii.ravel(), **kw)
+    return o.reshape(B, Hq, S, D).transpose(0, 2, 1, 3).copy(), lse.reshape(B, Hq, S)
+
+
+def attn_rows_local(q, k, v, rows_b, rows_h, rows_i, *, causal=True, rope_base=None, window=0, alibi=False):
+    """Sliding-window (|i-j| < window) and/or ALiBi attention for the listed rows: (O [n, D], LSE [n])."""
+    q, k, v = (np.ascontiguousarray(a, dtype=np.uint16) for a in (q, k, v))
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    rb, rh, ri = (np.ascontiguousarray(a, dtype=np.int32) for a in (rows_b, rows_h, rows_i))
+    n = len(rb)
+    o = np.empty((n, D), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    rc = _load().oracle_attn_rows_local(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+                                        B, Hq, Hkv, S, D, 1 if causal else 0, float(rope_base) if rope_base else 0.0,
+                                        int(window), 1 if alibi else 0, n, _ptr(rb, ctypes.c_int),
+                                        _ptr(rh, ctypes.c_int), _ptr(ri, ctypes.c_int), _ptr(o, ctypes.c_double),
+                                        _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return o, lse
+
+
+def attn_full_local(q, k, v, **kw):
+    """Sliding-window / ALiBi O [B, S, Hq, D] and LSE [B, Hq, S] (float64) for every query row."""
+    B, S, Hq, D = q.shape
+    bb, hh, ii = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(S), indexing="ij")
+    o, lse = attn_rows_local(q, k, v, bb.ravel(), hh.ravel(), ii.ravel(), **kw)
     return o.reshape(B, Hq, S, D).transpose(0, 2, 1, 3).copy(), lse.reshape(B, Hq, S)

@@ -514,3 +514,69 @@ int oracle_attn_rows_bs(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     free(active);
     return 0;
 }
+
+/*
+ * Attention with a sliding window and/or ALiBi ("AttnFuse", sec. 3: the
+ * sliding_window and alibi combinators; sliding windows and linear biases
+ * after its refs. 6 and 7), for a list of query rows, from the definitions:
+ *   visible(i, j) = (j <= i when causal) and (|i - j| < window when window > 0)
+ *   s_ij = q'_i . k'_j / sqrt(D) - m_h |i - j|   (ALiBi on: m_h = 2^(-8 (h+1) / Hq))
+ * then the row's maximum, exponentials, weighted sum and LSE as in
+ * oracle_attn_rows, over the visible keys only.
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_rows_local(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                           int window, int alibi,
+                           int n_rows, const int* row_b, const int* row_h, const int* row_i,
+                           double* o_out, double* lse_out) {
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 1024 || window < 0)
+        return -1;
+    for (int n = 0; n < n_rows; ++n)
+        if (row_b[n] < 0 || row_b[n] >= B || row_h[n] < 0 || row_h[n] >= Hq || row_i[n] < 0 || row_i[n] >= S)
+            return -1;
+    const int rope_on = rope_base > 0.0;
+    const int G = Hq / Hkv;
+    double theta[512];
+    if (rope_on) rope_thetas(D, rope_base, theta);
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int n = 0; n < n_rows; ++n) {
+        const int b = row_b[n], h = row_h[n], i = row_i[n], g = h / G;
+        const double slope = alibi ? pow(2.0, -8.0 * (double)(h + 1) / (double)Hq) : 0.0;
+        double qrot[1024], krot[1024];
+        rope_rotate(q + (((size_t)b * S + i) * Hq + h) * D, D, theta, (double)i, rope_on, qrot);
+        double* s = (double*)malloc(sizeof(double) * (size_t)S);
+        int* key = (int*)malloc(sizeof(int) * (size_t)S);
+        int cnt = 0;
+        for (int j = 0; j < S; ++j) {
+            const int dist = i >= j ? i - j : j - i;
+            if (causal && j > i) continue;
+            if (window > 0 && dist >= window) continue;
+            rope_rotate(k + (((size_t)b * S + j) * Hkv + g) * D, D, theta, (double)j, rope_on, krot);
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qrot[d] * krot[d];
+            s[cnt] = acc * inv_sqrt_d - slope * (double)dist;
+            key[cnt++] = j;
+        }
+        double* o = o_out + (size_t)n * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        double m = s[0];
+        for (int c = 1; c < cnt; ++c)
+            if (s[c] > m) m = s[c];
+        double l = 0.0;
+        for (int c = 0; c < cnt; ++c) {
+            s[c] = exp(s[c] - m);
+            l += s[c];
+        }
+        for (int c = 0; c < cnt; ++c) {
+            const uint16_t* vj = v + (((size_t)b * S + key[c]) * Hkv + g) * D;
+            for (int d = 0; d < D; ++d) o[d] += s[c] * bf16_to_f64(vj[d]);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+        lse_out[n] = m + log(l);
+        free(s);
+        free(key);
+    }
+    return 0;
+}

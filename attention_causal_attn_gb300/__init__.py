@@ -17,7 +17,7 @@ import numpy as np
 from ._build import INCLUDE, LIB, build
 
 __all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse",
-           "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+           "attn_fwd_local", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -65,6 +65,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_blocksparse.argtypes = [vp] * 5 + [i] * 6 + [d, vp, vp, vp]
         lib.attn_bwd_blocksparse.restype = i
         lib.attn_bwd_blocksparse.argtypes = [vp] * 9 + [i] * 6 + [d, vp, vp, vp]
+        lib.attn_fwd_local.restype = i
+        lib.attn_fwd_local.argtypes = [vp] * 5 + [i] * 6 + [d, i, i, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_check.restype = i
@@ -291,6 +293,26 @@ def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, o=None, lse=None, *, causal:
                                       _stream_handle(stream, q.device))
     if rc != 0:
         raise AttnError(rc, "attn_fwd_blocksparse")
+    return o, lse
+
+
+def attn_fwd_local(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=None, window: int = 0,
+                   alibi: bool = False, return_lse: bool = True, stream=None):
+    """The forward with a sliding window (|i - j| < window) and/or the ALiBi bias; returns (o, lse)."""
+    import torch
+    B, S, Hq, D, Hkv = _check_bshd(q, k, v)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_local(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, B, Hq, Hkv, S, D, 1 if causal else 0,
+                                float(rope_base) if rope_base else 0.0, int(window), 1 if alibi else 0,
+                                _stream_handle(stream, q.device))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_local")
     return o, lse
 
 

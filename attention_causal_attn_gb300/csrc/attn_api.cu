@@ -963,12 +963,12 @@ int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** o
 
 namespace {
 
-template <int D, bool CAUSAL, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
 int launch_bs(const attn::BsParams& bp, int dev, int nrows, cudaStream_t st) {
     constexpr int kMin = 120 * 1024;  // one CTA per SM: each takes all 512 TMEM columns
     constexpr int smem = static_cast<int>(attn::BsLayout<D>::kAlloc) > kMin ? static_cast<int>(attn::BsLayout<D>::kAlloc) : kMin;
-    constexpr unsigned bit = 1u << (8 | (D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0));
-    auto kern = attn::bs_fwd_kernel<D, CAUSAL, ROPE>;
+    constexpr unsigned bit = 1u << (8 | (EXT ? 16 : 0) | (D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0));
+    auto kern = attn::bs_fwd_kernel<D, CAUSAL, ROPE, EXT>;
     cudaError_t e;
     if (!(g_bwd_configured[dev] & bit)) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
@@ -981,9 +981,10 @@ int launch_bs(const attn::BsParams& bp, int dev, int nrows, cudaStream_t st) {
 }
 }  // namespace
 
-extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                                    int Hkv, int S, int D, int causal, double rope_base, const int* row_ptr,
-                                    const int* col_idx, void* stream) {
+// The block-sparse forward, with the sliding window and ALiBi of the EXT variant when `ext`.
+int bs_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S, int D,
+            int causal, double rope_base, const int* row_ptr, const int* col_idx, bool ext, int window, int alibi,
+            void* stream) {
     int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, 0.0);
     if (arc == ATTN_OK && row_ptr == nullptr) arc = ATTN_ERR_NULL;
     if (arc == ATTN_OK && static_cast<long long>(B) * Hq * ((S + 127) / 128) > INT_MAX) arc = ATTN_ERR_SHAPE;  // CTAs
@@ -1021,13 +1022,51 @@ extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v,
     bp.f.wait_limit_ns = kWaitLimitNs;
     bp.row_ptr = dmask;
     bp.col_idx = dmask + nrows + 1;
+    bp.window = window;
+    bp.alibi = alibi;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (ext) {
+        if (D == 128) {
+            if (causal) return rope ? launch_bs<128, true, true, true>(bp, dev, nrows, st) : launch_bs<128, true, false, true>(bp, dev, nrows, st);
+            return rope ? launch_bs<128, false, true, true>(bp, dev, nrows, st) : launch_bs<128, false, false, true>(bp, dev, nrows, st);
+        }
+        if (causal) return rope ? launch_bs<64, true, true, true>(bp, dev, nrows, st) : launch_bs<64, true, false, true>(bp, dev, nrows, st);
+        return rope ? launch_bs<64, false, true, true>(bp, dev, nrows, st) : launch_bs<64, false, false, true>(bp, dev, nrows, st);
+    }
     if (D == 128) {
         if (causal) return rope ? launch_bs<128, true, true>(bp, dev, nrows, st) : launch_bs<128, true, false>(bp, dev, nrows, st);
         return rope ? launch_bs<128, false, true>(bp, dev, nrows, st) : launch_bs<128, false, false>(bp, dev, nrows, st);
     }
     if (causal) return rope ? launch_bs<64, true, true>(bp, dev, nrows, st) : launch_bs<64, true, false>(bp, dev, nrows, st);
     return rope ? launch_bs<64, false, true>(bp, dev, nrows, st) : launch_bs<64, false, false>(bp, dev, nrows, st);
+}
+
+extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                    int Hkv, int S, int D, int causal, double rope_base, const int* row_ptr,
+                                    const int* col_idx, void* stream) {
+    return bs_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base, row_ptr, col_idx, false, 0, 0, stream);
+}
+
+extern "C" int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                              int Hkv, int S, int D, int causal, double rope_base, int window, int alibi,
+                              void* stream) {
+    if (window < 0 || (alibi != 0 && alibi != 1)) return ATTN_ERR_UNSUPPORTED;
+    if (S < 1 || S > kMaxS) return ATTN_ERR_SHAPE;
+    // the tiles any row of a query tile can see: keys in [128 i - window + 1, 128 i + 127 (+ window - 1)]
+    const int nrows = (S + 127) / 128;
+    std::vector<int> row_ptr(1, 0), col_idx;
+    for (int i = 0; i < nrows; ++i) {
+        long long lo = 0, hi = causal ? 128LL * i + 127 : S - 1LL;
+        if (window > 0) {
+            lo = std::max(0LL, 128LL * i - window + 1);
+            if (!causal) hi = 128LL * i + 127 + window - 1;
+        }
+        hi = std::min(hi, S - 1LL);
+        for (long long t = lo / 128; t <= hi / 128; ++t) col_idx.push_back(static_cast<int>(t));
+        row_ptr.push_back(static_cast<int>(col_idx.size()));
+    }
+    return bs_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base, row_ptr.data(),
+                   col_idx.empty() ? nullptr : col_idx.data(), true, window, alibi, stream);
 }
 
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

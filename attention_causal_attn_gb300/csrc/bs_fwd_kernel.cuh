@@ -11,6 +11,11 @@
 // query row, the prefill's softmax arithmetic and lazy rescale), four RoPE
 // warps, a TMA warp and an MMA warp.  A row of blocks with nothing listed
 // writes O = 0 and LSE = -inf.  Every wait is bounded.
+//
+// The EXT variant adds the sliding_window and alibi combinators ("AttnFuse",
+// sec. 3): key j is visible to query i only when |i - j| < window, and the
+// score gains -m_h |i - j| with m_h = 2^(-8 (h+1) / Hq); its softmax keeps
+// the running maximum in log2 units of the biased score.
 #pragma once
 
 #include "bwd_kernel.cuh"
@@ -21,7 +26,44 @@ struct BsParams {
     FwdParams f;           // tm_q, tm_k, tm_v, o, lse, RoPE factor table, shape, scale, status, wait limit
     const int* row_ptr;    // [ceil(S/128) + 1]
     const int* col_idx;    // listed key tiles of each row of tiles, ascending
+    int window;            // EXT: visible iff |i - j| < window (0: no window)
+    int alibi;             // EXT: ALiBi bias on
 };
+
+// EXT: the score of column col of a tile for this row in log2 units (biased), or -inf when the
+// key lies outside [lo, hi).  rel0 = first key of the tile - row; m2 = m_h * log2(e).
+__device__ __forceinline__ float ext_score(uint32_t raw, int col, int lo, int hi, float c, float m2, int rel0) {
+    const float dist = fabsf(static_cast<float>(rel0 + col));
+    return (col >= lo && col < hi) ? __uint_as_float(raw) * c - m2 * dist : -INFINITY;
+}
+
+__device__ __forceinline__ float ext_row_max(uint32_t tS, int lo, int hi, float c, float m2, int rel0) {
+    float mx = -INFINITY;
+    tmem_stream_128(tS, [&](const uint32_t (&r)[32], int cc) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, ext_score(r[j], cc + j, lo, hi, c, m2, rel0));
+    });
+    return mx;
+}
+
+// P = exp2(score - m) in bf16 over the S columns (hidden keys 0), and the row sum of P.
+__device__ __forceinline__ float ext_exp_to_p(uint32_t tS, int lo, int hi, float c, float m2, int rel0, float m) {
+    float sum = 0.f;
+    tmem_stream_128(tS, [&](const uint32_t (&r)[32], int cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const float v0 = ext_score(r[j], cc + j, lo, hi, c, m2, rel0);
+            const float v1 = ext_score(r[j + 1], cc + j + 1, lo, hi, c, m2, rel0);
+            const float p0 = v0 == -INFINITY ? 0.f : ex2_approx(v0 - m);
+            const float p1 = v1 == -INFINITY ? 0.f : ex2_approx(v1 - m);
+            sum += p0 + p1;
+            pk[j / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_store_16(tS + cc / 2, pk);
+    });
+    return sum;
+}
 
 constexpr int kBsThreads = 320;  // warps 0-3 softmax, 4-7 RoPE, 8 TMA, 9 MMA
 constexpr int kBsWarpRope = 4, kBsWarpTma = 8, kBsWarpMma = 9;
@@ -37,7 +79,7 @@ struct BsLayout {
     static constexpr uint32_t kAlloc = kBytes + 1024;
 };
 
-template <int D, bool CAUSAL, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
 __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_constant__ BsParams p) {
     using L = BsLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -82,6 +124,10 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
         const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const uint32_t tS = trow, tO = trow + 128u;
         const float c = f.scale_log2;
+        // EXT: m_used is the running maximum of the biased score in log2 units
+        const float m2 = (EXT && p.alibi) ? exp2f(-8.f * static_cast<float>(h + 1) / static_cast<float>(f.Hq)) *
+                                                1.4426950408889634f
+                                          : 0.f;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int it = 0; it < nblk && ok; ++it) {
@@ -89,20 +135,29 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
             if (!ok) break;
             tc_fence_after();
-            // keys [kv0, kv0 + limit) are visible to this row
+            // keys [kv0, kv0 + limit) are visible to this row (EXT: columns [lo, limit))
             int limit = min(128, f.S - kv0);
             if (CAUSAL) limit = min(limit, row - kv0 + 1);
+            int lo = 0;
+            if (EXT && p.window > 0) {
+                lo = max(0, row - p.window + 1 - kv0);
+                if (!CAUSAL) limit = min(limit, row + p.window - kv0);
+            }
+            const int rel0 = kv0 - row;
             const bool masked = __any_sync(0xffffffffu, limit < 128);
-            const float mx = masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit);
+            float mx;
+            if constexpr (EXT) mx = ext_row_max(tS, lo, limit, c, m2, rel0);
+            else mx = masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit);
             const float m_new = fmaxf(m_used, mx);
+            const float unit = EXT ? 1.f : c;  // m is in log2 units with EXT, raw score units without
             if (it == 0) {
                 m_used = m_new;
             } else {
-                const bool need = (m_new - m_used) * c > kRescaleThreshold;
+                const bool need = (m_new - m_used) * unit > kRescaleThreshold;
                 if (__any_sync(0xffffffffu, need)) {
                     float alpha = 1.f;
                     if (need) {
-                        alpha = ex2_approx((m_used - m_new) * c);
+                        alpha = m_used == -INFINITY ? 0.f : ex2_approx((m_used - m_new) * unit);
                         m_used = m_new;
                         l *= alpha;
                     }
@@ -122,8 +177,12 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                     }
                 }
             }
-            const float mc = m_used * c;
-            l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
+            if constexpr (EXT) {
+                l += ext_exp_to_p(tS, lo, limit, c, m2, rel0, m_used);
+            } else {
+                const float mc = m_used * c;
+                l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
+            }
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
@@ -151,7 +210,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             }
             if (store && f.lse != nullptr)
                 f.lse[(static_cast<size_t>(b) * f.Hq + h) * f.S + row] =
-                    have ? (m_used * c + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    have ? ((EXT ? m_used : m_used * c) + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
     } else if (warp < kBsWarpTma) {
         // ---- RoPE warps: Q once, then each streamed K tile

@@ -590,6 +590,64 @@ def run_blocksparse(args, w, rank, world, local_rank):
     }
 
 
+# --------------------------------------------------------------------- sliding window / ALiBi
+def run_local(args, w, rank, world, local_rank):
+    """One step = one attn_fwd_local call (sliding window and/or ALiBi) on the workload."""
+    import torch
+    import attention_causal_attn_gb300 as attn
+    attn.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if "local" not in w:
+        raise SystemExit("--local needs a workload with a window or ALiBi (sliding_window_s4096, alibi_s4096)")
+    B, Hq, Hkv, S, D = w["B"], w["Hq"], w["Hkv"], w["S"], w["D"]
+    win, alibi = w["local"]["window"], w["local"]["alibi"]
+    q_h, k_h, v_h = si.make_qkv(B, Hq, Hkv, S, D, outliers=w["outliers"], seed=replica_seed(rank))
+    q, k, v = (torch.from_numpy(x).view(torch.bfloat16).to(dev) for x in (q_h, k_h, v_h))
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(causal=w["causal"], rope_base=w["rope_base"], window=win, alibi=alibi, stream=stream)
+    o, lse = attn.attn_fwd_local(q, k, v, **kw)
+    for _ in range(max(args.warmup, 3)):
+        attn.attn_fwd_local(q, k, v, o, lse, **kw)
+    attn.attn_check(stream=stream, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if 3 * q.numel() * 2 < (256 << 20) else None
+    times = []
+    with ClockSampler(local_rank) as clocks:
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.attn_fwd_local(q, k, v, o, lse, **kw)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+    attn.attn_check(stream=stream, device=dev)
+    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    i = np.arange(S, dtype=np.int64)
+    if w["causal"]:
+        pairs = int(np.minimum(i + 1, win).sum()) if win else S * (S + 1) // 2
+    else:
+        pairs = int((np.minimum(i + win, S) - np.maximum(i - win + 1, 0)).sum()) if win else S * S
+    tf = 4.0 * D * pairs * B * Hq / (ms * 1e-3) / 1e12
+    peaks, _ = load_peaks()
+    cfg = workload_config(args.workload, w)
+    cfg["step"] = "forward with the sliding window / ALiBi bias"
+    cfg["window"], cfg["alibi"] = win, alibi
+    cfg["l2"] = "L2 flushed between steps" if flush is not None else "inputs larger than L2"
+    return {
+        "metric": "local attention forward TFLOP/s", "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": float(peaks["bf16_tflops"]),
+                     "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4), "traffic": None,
+                     "kernel": "bs_fwd_kernel (EXT)",
+                     "algorithmic": "4*D FLOPs per visible (query, key) pair, median step time"},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+
+
 # --------------------------------------------------------------------- reference arm
 def run_reference(args, w, rank):
     if rank != 0:
@@ -638,6 +696,8 @@ def main():
     ap.add_argument("--seq", type=int, default=None, help="override the workload's sequence length")
     ap.add_argument("--decode", action="store_true",
                     help="time one decode step (attn_decode) on the workload's cache shape instead of the prefill")
+    ap.add_argument("--local", action="store_true",
+                    help="time the sliding-window / ALiBi forward (sliding_window_s4096, alibi_s4096)")
     ap.add_argument("--blocksparse", action="store_true",
                     help="time the block-sparse forward on a workload with a block mask (bigbird_s4096)")
     ap.add_argument("--backward", action="store_true",
@@ -670,6 +730,8 @@ def main():
         line = run_decode(args, w, rank, world, local_rank)
     elif args.backward:
         line = run_backward(args, w, rank, world, local_rank)
+    elif args.local:
+        line = run_local(args, w, rank, world, local_rank)
     elif args.blocksparse:  # forward; with --backward the branch above times its backward
         line = run_blocksparse(args, w, rank, world, local_rank)
     else:

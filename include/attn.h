@@ -265,6 +265,21 @@ int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void
                          int causal, double rope_base, const int* row_ptr, const int* col_idx, void* stream);
 
 /*
+ * attn_fwd_local — the forward with the sliding_window and alibi combinators
+ * of "AttnFuse: A Composable DSL for Compiling Attentions to Fused GPU
+ * Kernels" (sec. 3; sliding windows and linear biases after its refs. 6, 7).
+ *   window > 0: key j is visible to query i only when |i - j| < window
+ *               (with causal: the last `window` keys up to and including i).
+ *   alibi = 1:  the score gains -m_h |i - j|, m_h = 2^(-8 (h+1) / Hq).
+ * The library lists the 128 x 128 tiles the window reaches and runs the
+ * block-sparse kernel over them, masking and biasing cell by cell.
+ * q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base: as attn_fwd.
+ * Errors: as attn_fwd; ATTN_ERR_UNSUPPORTED for window < 0 or alibi not 0/1.
+ */
+int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
+                   int D, int causal, double rope_base, int window, int alibi, void* stream);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

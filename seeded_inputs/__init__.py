@@ -145,6 +145,11 @@ WORKLOADS = {
     # 128 x 128 blocks, the diagonal, one global block row/column and one seeded random block per row
     "bigbird_s4096": dict(B=4, Hq=32, Hkv=32, S=4096, D=128, causal=False, rope_base=None,
                           window_k=None, outliers=0.0, block_mask=dict(window=0, n_global=1, n_random=1)),
+    # sliding window and ALiBi ("AttnFuse", sec. 6.1: GPT-2-small geometry B=4, H=12, D=64)
+    "sliding_window_s4096": dict(B=4, Hq=12, Hkv=12, S=4096, D=64, causal=True, rope_base=None,
+                                 window_k=None, outliers=0.0, local=dict(window=512, alibi=False)),
+    "alibi_s4096": dict(B=4, Hq=12, Hkv=12, S=4096, D=64, causal=True, rope_base=None,
+                        window_k=None, outliers=0.0, local=dict(window=0, alibi=True)),
 }
 
 

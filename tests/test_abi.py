@@ -19,7 +19,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
     assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated",
-                          "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
+                          "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "attn_fwd_local", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for n in names:
@@ -129,6 +129,16 @@ def test_blocksparse_mask_is_checked_on_the_host(lib):
     assert lib.attn_bwd_blocksparse(*([16] * 9), 1, 2, 2, 256, 128, 0, 1e4, bad.ctypes.data, ci.ctypes.data,
                                     None) == E["ATTN_ERR_SHAPE"]
     assert lib.attn_bwd_blocksparse(*([16] * 9), 1, 2, 2, 256, 128, 0, 1e4, None, None, None) == E["ATTN_ERR_NULL"]
+
+
+def test_local_entry_checks_arguments_on_the_host(lib):
+    E = attn.ATTN_STATUS
+    call = lambda **kw: lib.attn_fwd_local(16, 16, 16, 16, None, 1, 2, 2, kw.get("S", 256), kw.get("D", 128),
+                                            kw.get("causal", 1), 1e4, kw.get("window", 64), kw.get("alibi", 0), None)
+    assert call(window=-1) == E["ATTN_ERR_UNSUPPORTED"]
+    assert call(alibi=2) == E["ATTN_ERR_UNSUPPORTED"]
+    assert call(D=80) == E["ATTN_ERR_SHAPE"]
+    assert call(S=0) == E["ATTN_ERR_SHAPE"]
 
 
 def test_create_block_mask_lists_the_predicate():

@@ -429,3 +429,35 @@ def test_blocksparse_backward_matches_oracle(B, Hq, Hkv, S, D, causal, base, kin
     _check_grad(dv.float().cpu().numpy(), rv, tag + " dV")
     _check_grad(dk.float().cpu().numpy(), rk, tag + " dK")
     _check_grad(dq.float().cpu().numpy(), rq, tag + " dQ")
+
+
+# ---------------------------------------------------------------- sliding window and ALiBi
+LOCAL = [
+    # B, Hq, Hkv, S, D, causal, rope_base, window, alibi
+    (1, 4, 4, 1000, 64, True, None, 256, False),     # GPT-2-small head size, causal sliding window
+    (2, 4, 2, 700, 128, True, 10000.0, 0, True),     # ALiBi over the whole causal range, RoPE, GQA
+    (1, 2, 2, 640, 64, False, None, 100, True),      # both, non-causal window
+    (1, 3, 3, 300, 128, True, 10000.0, 1, True),     # a window of one key: O_i = V_i
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base,window,alibi", LOCAL)
+def test_local_forward_matches_oracle(B, Hq, Hkv, S, D, causal, base, window, alibi):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=900 + S)
+    o, lse = attn.attn_fwd_local(_dev(q), _dev(k), _dev(v), causal=causal, rope_base=base, window=window,
+                                 alibi=alibi)
+    attn.attn_check()
+    o_ref, lse_ref = oracle.attn_full_local(q, k, v, causal=causal, rope_base=base, window=window, alibi=alibi)
+    tag = f"local w={window} alibi={alibi} S={S}"
+    if window != 1:
+        _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, tag)
+        return
+    # one key per row: O_i = V_i, and LSE_i is the single score, whose error is not averaged over
+    # keys.  Rounding the rotated q', k' to fp16 (relative 2^-11 each) bounds it by
+    # 2 * 2^-11 * sum_d |q'_d k'_d| / sqrt(D) (+ fp32 slack).
+    _check(o.float().cpu().numpy(), None, o_ref, None, tag)
+    qr = oracle.rope_rotate(q, base) if base else si.bf16_bits_to_f64(q)
+    kr = oracle.rope_rotate(k, base) if base else si.bf16_bits_to_f64(k)
+    kr = np.repeat(kr, Hq // Hkv, axis=2)
+    bound = 2 * 2.0 ** -11 * np.abs(qr * kr).sum(-1).transpose(0, 2, 1) / np.sqrt(D) + 1e-5
+    assert np.all(np.abs(lse.cpu().numpy() - lse_ref) <= bound), f"{tag}: LSE beyond the fp16 rounding bound"

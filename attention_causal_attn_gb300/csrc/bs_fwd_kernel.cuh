@@ -7,9 +7,11 @@
 // heavy rows start first): Q is loaded and rotated once, then the listed key tiles
 // are streamed (two slots) in descending order, each through
 //   S = Q K^T (tcgen05, TMEM)  ->  online softmax, P in bf16 over S  ->  O += P V.
-// Roles as in the backward kernels: one elementwise warpgroup (one thread per
-// query row, the prefill's softmax arithmetic and lazy rescale), four RoPE
-// warps, a TMA warp and an MMA warp.  A row of blocks with nothing listed
+// Roles as in the backward kernels: two softmax warpgroups (one thread per
+// query row and half of the 128 key columns), four RoPE warps, a TMA warp and
+// an MMA warp.  Each half keeps its own running maximum and sum (log2 units)
+// and its own O accumulator in TMEM, fed by its half of P; the halves merge
+// by their maxima once, in the epilogue.  A row of blocks with nothing listed
 // writes O = 0 and LSE = -inf.  Every wait is bounded.
 //
 // The EXT variant adds the sliding_window and alibi combinators ("AttnFuse",
@@ -37,36 +39,8 @@ __device__ __forceinline__ float ext_score(uint32_t raw, int col, int lo, int hi
     return (col >= lo && col < hi) ? __uint_as_float(raw) * c - m2 * dist : -INFINITY;
 }
 
-__device__ __forceinline__ float ext_row_max(uint32_t tS, int lo, int hi, float c, float m2, int rel0) {
-    float mx = -INFINITY;
-    tmem_stream_128(tS, [&](const uint32_t (&r)[32], int cc) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, ext_score(r[j], cc + j, lo, hi, c, m2, rel0));
-    });
-    return mx;
-}
-
-// P = exp2(score - m) in bf16 over the S columns (hidden keys 0), and the row sum of P.
-__device__ __forceinline__ float ext_exp_to_p(uint32_t tS, int lo, int hi, float c, float m2, int rel0, float m) {
-    float sum = 0.f;
-    tmem_stream_128(tS, [&](const uint32_t (&r)[32], int cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const float v0 = ext_score(r[j], cc + j, lo, hi, c, m2, rel0);
-            const float v1 = ext_score(r[j + 1], cc + j + 1, lo, hi, c, m2, rel0);
-            const float p0 = v0 == -INFINITY ? 0.f : ex2_approx(v0 - m);
-            const float p1 = v1 == -INFINITY ? 0.f : ex2_approx(v1 - m);
-            sum += p0 + p1;
-            pk[j / 2] = pack_bf16x2(p0, p1);
-        }
-        tmem_store_16(tS + cc / 2, pk);
-    });
-    return sum;
-}
-
-constexpr int kBsThreads = 320;  // warps 0-3 softmax, 4-7 RoPE, 8 TMA, 9 MMA
-constexpr int kBsWarpRope = 4, kBsWarpTma = 8, kBsWarpMma = 9;
+constexpr int kBsThreads = 448;  // warps 0-7 softmax (two halves), 8-11 RoPE, 12 TMA, 13 MMA
+constexpr int kBsWarpRope = 8, kBsWarpTma = 12, kBsWarpMma = 13;
 
 template <int D>
 struct BsLayout {
@@ -75,9 +49,79 @@ struct BsLayout {
     static constexpr uint32_t kStr0 = kTile;  // slot s: K at kStr0 + 2 s kTile, V after it
     static constexpr uint32_t kBars = 5 * kTile;
     static constexpr uint32_t kMisc = kBars + 256;
-    static constexpr uint32_t kBytes = kMisc + 64;
+    static constexpr uint32_t kMerge = kMisc + 64;  // [2 halves][128 rows] float2 (m, l)
+    static constexpr uint32_t kBytes = kMerge + 2 * 128 * 8;
     static constexpr uint32_t kAlloc = kBytes + 1024;
 };
+
+// Without the EXT terms: the raw-score maximum of one half (columns [c0, c0 + 64), keys at or past
+// limit hidden), and P = exp2(S c - m c) packed into the half's first 32 columns with its sum, by
+// the prefill's own chunk routines (raw scores, paired fp32 arithmetic).
+template <bool MASKED>
+__device__ __forceinline__ float half_row_max_raw(uint32_t tS, int c0, int limit) {
+    uint32_t a[32], b[32];
+    tmem_load_32_async(tS + c0, a);
+    tmem_load_32_async(tS + c0 + 32, b);
+    tmem_wait_ld_32(a);
+    tmem_wait_ld_32(b);
+    return row_max32<MASKED>(b, c0 + 32, limit, row_max32<MASKED>(a, c0, limit, -INFINITY));
+}
+
+template <bool MASKED>
+__device__ __forceinline__ float half_exp_to_p_raw(uint32_t tS, int c0, int limit, float c, float mc) {
+    const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+    uint64_t sum2 = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t r[32], pk[16];
+        tmem_load_32(tS + c0 + cc, r);
+        exp_pack32<MASKED>(r, c0 + cc, limit, c2, nmc2, sum2, pk);
+        tmem_store_16(tS + c0 + cc / 2, pk);
+    }
+    float s0, s1;
+    f2_unpack(sum2, s0, s1);
+    return s0 + s1;
+}
+
+// Row maximum of one half (columns [c0, c0 + 64)) of a tile, of score(raw, column).
+template <typename F>
+__device__ __forceinline__ float half_row_max(uint32_t tS, int c0, F score) {
+    uint32_t a[32], b[32];
+    tmem_load_32_async(tS + c0, a);
+    tmem_load_32_async(tS + c0 + 32, b);
+    tmem_wait_ld_32(a);
+    tmem_wait_ld_32(b);
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        m0 = fmaxf(m0, score(a[j], c0 + j));
+        m1 = fmaxf(m1, score(b[j], c0 + 32 + j));
+    }
+    return fmaxf(m0, m1);
+}
+
+// P = exp2(score - m) (0 for hidden keys) of one half in bf16, packed into the half's own first 32
+// columns (never a column still to be read); returns the half's sum of P.
+template <typename F>
+__device__ __forceinline__ float half_exp_to_p(uint32_t tS, int c0, F score, float m) {
+    float sum = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t r[32];
+        tmem_load_32(tS + c0 + cc, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const float v0 = score(r[j], c0 + cc + j), v1 = score(r[j + 1], c0 + cc + j + 1);
+            const float p0 = v0 == -INFINITY ? 0.f : ex2_approx(v0 - m);
+            const float p1 = v1 == -INFINITY ? 0.f : ex2_approx(v1 - m);
+            sum += p0 + p1;
+            pk[j / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_store_16(tS + c0 + cc / 2, pk);
+    }
+    return sum;
+}
 
 template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
 __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_constant__ BsParams p) {
@@ -100,7 +144,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        bwd_init_bars(bar0, 128);  // P is handed over by the 128 softmax threads
+        bwd_init_bars(bar0, 256);  // P is handed over by the 256 softmax threads
     }
     if (warp == kBsWarpTma && lane == 0) {
         tma_prefetch_desc(&f.tm_q);
@@ -117,14 +161,14 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, f.status, f.wait_limit_ns};
 
-    if (warp < 4) {
-        // ---- softmax warpgroup: thread t owns query row q0 + t (TMEM lane t)
-        const int t = threadIdx.x;
+    if (warp < 8) {
+        // ---- softmax warpgroups: thread t owns query row q0 + t (TMEM lane t) and key columns
+        // [64 x, 64 x + 64) of every tile, x = half; scores, maxima and sums in log2 units
+        const int t = threadIdx.x % 128, x = threadIdx.x / 128;
         const int row = q0 + t;
         const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
-        const uint32_t tS = trow, tO = trow + 128u;
+        const uint32_t tS = trow, tO = trow + 128u + static_cast<uint32_t>(x * D);  // this half's O
         const float c = f.scale_log2;
-        // EXT: m_used is the running maximum of the biased score in log2 units
         const float m2 = (EXT && p.alibi) ? exp2f(-8.f * static_cast<float>(h + 1) / static_cast<float>(f.Hq)) *
                                                 1.4426950408889634f
                                           : 0.f;
@@ -135,7 +179,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
             if (!ok) break;
             tc_fence_after();
-            // keys [kv0, kv0 + limit) are visible to this row (EXT: columns [lo, limit))
+            // keys kv0 + [lo, limit) are visible to this row
             int limit = min(128, f.S - kv0);
             if (CAUSAL) limit = min(limit, row - kv0 + 1);
             int lo = 0;
@@ -144,12 +188,17 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                 if (!CAUSAL) limit = min(limit, row + p.window - kv0);
             }
             const int rel0 = kv0 - row;
+            auto score = [&](uint32_t raw, int col) {
+                if (EXT) return ext_score(raw, col, lo, limit, c, m2, rel0);
+                return col < limit ? __uint_as_float(raw) * c : -INFINITY;
+            };
+            // EXT: m in log2 units of the biased score; otherwise raw score units (as the prefill)
             const bool masked = __any_sync(0xffffffffu, limit < 128);
             float mx;
-            if constexpr (EXT) mx = ext_row_max(tS, lo, limit, c, m2, rel0);
-            else mx = masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit);
+            if constexpr (EXT) mx = half_row_max(tS, 64 * x, score);
+            else mx = masked ? half_row_max_raw<true>(tS, 64 * x, limit) : half_row_max_raw<false>(tS, 64 * x, limit);
             const float m_new = fmaxf(m_used, mx);
-            const float unit = EXT ? 1.f : c;  // m is in log2 units with EXT, raw score units without
+            const float unit = EXT ? 1.f : c;
             if (it == 0) {
                 m_used = m_new;
             } else {
@@ -177,40 +226,62 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                     }
                 }
             }
-            if constexpr (EXT) {
-                l += ext_exp_to_p(tS, lo, limit, c, m2, rel0, m_used);
-            } else {
-                const float mc = m_used * c;
-                l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
+            if constexpr (EXT) l += half_exp_to_p(tS, 64 * x, score, m_used);
+            else {
+                // a half that has seen no key yet (m = -inf: every key it held was masked) gets P = 0
+                const float mc = m_used == -INFINITY ? 0.f : m_used * c;
+                l += masked ? half_exp_to_p_raw<true>(tS, 64 * x, limit, c, mc)
+                            : half_exp_to_p_raw<false>(tS, 64 * x, limit, c, mc);
             }
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
         }
-        // epilogue: O / l in bf16, LSE in natural log (a row that saw nothing: 0 and -inf)
+        // epilogue: merge the halves by their maxima; each half writes D/2 output channels
         const bool have = nblk > 0;
-        if (ok && (!have || bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax))) {
+        if (ok && have) ok = bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax);
+        float2* ml = reinterpret_cast<float2*>(smg + L::kMerge);
+        ml[x * 128 + t] = make_float2(EXT ? m_used : m_used * c, l);  // log2 units
+        mbar_arrive(bar_at(bar0, BB_MERGE));
+        if (ok) ok = bwd_wait(bar_at(bar0, BB_MERGE), 0, ctl, kStatusSoftmax);
+        if (ok) {
             tc_fence_after();
+            const float2 mine = ml[x * 128 + t], other = ml[(1 - x) * 128 + t];
+            const float ma = x == 0 ? mine.x : other.x, mb = x == 0 ? other.x : mine.x;
+            const float la = x == 0 ? mine.y : other.y, lb = x == 0 ? other.y : mine.y;
+            const float M = fmaxf(ma, mb);
+            const float sa = ma == -INFINITY ? 0.f : ex2_approx(ma - M), sb = mb == -INFINITY ? 0.f : ex2_approx(mb - M);
+            const float Lsum = la * sa + lb * sb;
+            const float inv = (have && Lsum > 0.f) ? 1.0f / Lsum : 0.f;
             const bool store = row < f.S;
-            const float inv_l = (have && l > 0.f) ? 1.0f / l : 0.f;
             __nv_bfloat16* dst = f.o + ((static_cast<size_t>(b) * f.S + (store ? row : 0)) * f.Hq + h) * D;
+            const uint32_t tOa = trow + 128u, tOb = trow + 128u + D;
 #pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
-                uint32_t r[32];
-                if (have) tmem_load_32(tO + cc, r);
+            for (int cc = 0; cc < D / 2; cc += 32) {
+                const int d0 = x * (D / 2) + cc;  // this half's output channels
+                uint32_t ra[32], rb[32];
+                if (have) {
+                    tmem_load_32_async(tOa + d0, ra);
+                    tmem_load_32_async(tOb + d0, rb);
+                    tmem_wait_ld_32(ra);
+                    tmem_wait_ld_32(rb);
+                }
                 uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 32; j += 2)
-                    pk[j / 2] = have ? pack_bf16x2(__uint_as_float(r[j]) * inv_l, __uint_as_float(r[j + 1]) * inv_l) : 0u;
+                for (int j = 0; j < 32; j += 2) {
+                    const float o0 = have ? (__uint_as_float(ra[j]) * sa + __uint_as_float(rb[j]) * sb) * inv : 0.f;
+                    const float o1 = have ? (__uint_as_float(ra[j + 1]) * sa + __uint_as_float(rb[j + 1]) * sb) * inv : 0.f;
+                    pk[j / 2] = pack_bf16x2(o0, o1);
+                }
                 if (store) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + d0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
-            if (store && f.lse != nullptr)
+            if (x == 0 && store && f.lse != nullptr)
                 f.lse[(static_cast<size_t>(b) * f.Hq + h) * f.S + row] =
-                    have ? ((EXT ? m_used : m_used * c) + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    (have && Lsum > 0.f) ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         }
     } else if (warp < kBsWarpTma) {
         // ---- RoPE warps: Q once, then each streamed K tile
@@ -284,10 +355,14 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             if (!ok) break;
             tc_fence_after();
             const uint64_t vdesc = sw128_desc(va, kSubTileBytes, 1024u);
+            // each half of P (keys 0-63, 64-127, packed in its half's first 32 columns) into its own O;
             // 16 keys per step: 2048 bytes of V, 8 TMEM columns of P
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, (it > 0 || kk > 0) ? 1u : 0u);
+            for (int hx = 0; hx < 2; ++hx)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_ts(tO + static_cast<uint32_t>(hx * D), tS + 64u * hx + kk * 8u,
+                            desc_advance(vdesc, (4 * hx + kk) * 128u), kIdescPV, (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
         }
         if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));

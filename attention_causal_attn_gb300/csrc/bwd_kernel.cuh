@@ -118,6 +118,7 @@ enum : int {
     BB_P_FULL,        // P and dS written to TMEM
     BB_ACC_FULL,      // last accumulation done
     BB_DRAIN,
+    BB_MERGE,         // block-sparse forward: both halves' (m, l) are in shared memory
     BB_NUM
 };
 static_assert(BB_NUM * 8 <= 256, "barrier block");
@@ -280,6 +281,7 @@ __device__ __forceinline__ void bwd_init_bars(uint32_t bar0, uint32_t p_count = 
     mbar_init(bar_at(bar0, BB_P_FULL), p_count);
     mbar_init(bar_at(bar0, BB_ACC_FULL), 1);
     mbar_init(bar_at(bar0, BB_DRAIN), 1);
+    mbar_init(bar_at(bar0, BB_MERGE), kBwdEw);
     fence_barrier_init();
     fence_proxy_async_smem();
 }

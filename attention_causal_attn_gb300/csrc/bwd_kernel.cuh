@@ -118,7 +118,6 @@ enum : int {
     BB_P_FULL,        // P and dS written to TMEM
     BB_ACC_FULL,      // last accumulation done
     BB_DRAIN,
-    BB_MERGE,         // block-sparse forward: both halves' (m, l) are in shared memory
     BB_NUM
 };
 static_assert(BB_NUM * 8 <= 256, "barrier block");
@@ -269,7 +268,7 @@ __device__ __forceinline__ void bwd_drain(uint32_t bar0, const WaitCtl& ctl) {
     }
 }
 
-__device__ __forceinline__ void bwd_init_bars(uint32_t bar0, uint32_t p_count = kBwdEw) {
+__device__ __forceinline__ void bwd_init_bars(uint32_t bar0) {
     mbar_init(bar_at(bar0, BB_RES_FULL), 1);
     mbar_init(bar_at(bar0, BB_RES_ROT), 128);
     for (int s = 0; s < 2; ++s) {
@@ -278,10 +277,9 @@ __device__ __forceinline__ void bwd_init_bars(uint32_t bar0, uint32_t p_count = 
         mbar_init(bar_at(bar0, BB_STR_EMPTY + s), 1);
     }
     mbar_init(bar_at(bar0, BB_S_FULL), 1);
-    mbar_init(bar_at(bar0, BB_P_FULL), p_count);
+    mbar_init(bar_at(bar0, BB_P_FULL), kBwdEw);
     mbar_init(bar_at(bar0, BB_ACC_FULL), 1);
     mbar_init(bar_at(bar0, BB_DRAIN), 1);
-    mbar_init(bar_at(bar0, BB_MERGE), kBwdEw);
     fence_barrier_init();
     fence_proxy_async_smem();
 }

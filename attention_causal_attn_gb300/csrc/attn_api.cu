@@ -805,7 +805,10 @@ int launch_bwd(const attn::BwdParams& bp, int dev, int ntiles, cudaStream_t st) 
 }  // namespace
 
 int check_mask(const int* row_ptr, const int* col_idx, int nrows, bool causal);
-int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out);
+namespace {
+struct MaskEntry;
+}
+int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out, MaskEntry** entry = nullptr);
 
 // The backward; row_ptr / col_idx: an optional host CSR block mask (null: dense).
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
@@ -899,10 +902,16 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
 // ---------------------------------------------------------------------------
 // Block-sparse forward ("AttnFuse", sec. 4.3 Block-Sparse Attention).
 namespace {
+struct MaskSched {
+    long long bh;
+    int ctas;
+    int* d;  // tasks | offsets (ctas + 1)
+};
 struct MaskEntry {
     int dev;
     std::vector<int> csr;  // row_ptr then col_idx, as given
     int* d = nullptr;      // row_ptr | col_idx | col_ptr | row_idx (the same mask by columns)
+    std::vector<MaskSched> sched;  // persistent forward schedules, by batch-heads
 };
 std::vector<MaskEntry> g_masks;  // device copies of the block masks seen, by content
 }  // namespace
@@ -925,13 +934,14 @@ int check_mask(const int* row_ptr, const int* col_idx, int nrows, bool causal) {
 }
 
 // The device copy of a (checked) mask, with its column-major form; caller holds g_mu.
-int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out) {
+int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out, MaskEntry** entry) {
     const int nnz = row_ptr[nrows];
     for (auto& e : g_masks) {
         if (e.dev != dev || e.csr.size() != static_cast<size_t>(nrows + 1 + nnz)) continue;
         if (std::equal(row_ptr, row_ptr + nrows + 1, e.csr.begin()) &&
             std::equal(col_idx, col_idx + nnz, e.csr.begin() + nrows + 1)) {
             *out = e.d;
+            if (entry != nullptr) *entry = &e;
             return ATTN_OK;
         }
     }
@@ -958,13 +968,38 @@ int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** o
     }
     *out = me.d;
     g_masks.push_back(std::move(me));
+    if (entry != nullptr) *entry = &g_masks.back();
+    return ATTN_OK;
+}
+
+// The persistent block-sparse forward's task lists for a mask and B * Hq, built once
+// (attn_host::build_mask_schedule) and kept on the device; caller holds g_mu.
+int get_mask_sched(int dev, MaskEntry& me, int nrows, long long bh, const MaskSched** out) {
+    for (auto& s : me.sched)
+        if (s.bh == bh) {
+            *out = &s;
+            return ATTN_OK;
+        }
+    const attn_host::MaskSchedule sc = attn_host::build_mask_schedule(me.csr.data(), nrows, bh, g_dev[dev].sms);
+    std::vector<int> all(sc.tasks.begin(), sc.tasks.end());
+    all.insert(all.end(), sc.offsets.begin(), sc.offsets.end());
+    MaskSched ms{bh, sc.ctas, nullptr};
+    cudaError_t e;
+    if ((e = cudaMalloc(&ms.d, all.size() * sizeof(int))) != cudaSuccess)
+        return cuda_fail("cudaMalloc(block-sparse schedule)", e, ATTN_ERR_OOM);
+    if ((e = cudaMemcpy(ms.d, all.data(), all.size() * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) {
+        cudaFree(ms.d);
+        return cuda_fail("cudaMemcpy(block-sparse schedule)", e);
+    }
+    me.sched.push_back(ms);
+    *out = &me.sched.back();
     return ATTN_OK;
 }
 
 namespace {
 
 template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
-int launch_bs(const attn::BsParams& bp, int dev, int nrows, cudaStream_t st) {
+int launch_bs(const attn::BsParams& bp, int dev, int ctas, cudaStream_t st) {
     constexpr int kMin = 120 * 1024;  // one CTA per SM: each takes all 512 TMEM columns
     constexpr int smem = static_cast<int>(attn::BsLayout<D>::kAlloc) > kMin ? static_cast<int>(attn::BsLayout<D>::kAlloc) : kMin;
     constexpr unsigned bit = 1u << (8 | (EXT ? 16 : 0) | (D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0));
@@ -975,7 +1010,7 @@ int launch_bs(const attn::BsParams& bp, int dev, int nrows, cudaStream_t st) {
             return cuda_fail("cudaFuncSetAttribute(block-sparse)", e);
         g_bwd_configured[dev] |= bit;
     }
-    kern<<<static_cast<unsigned>(static_cast<long long>(bp.f.B) * bp.f.Hq * nrows), attn::kBsThreads, smem, st>>>(bp);
+    kern<<<static_cast<unsigned>(ctas), attn::kBsThreads, smem, st>>>(bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("block-sparse kernel launch", e);
     return ATTN_OK;
 }
@@ -1000,12 +1035,20 @@ int bs_impl(const void* q, const void* k, const void* v, void* o, float* lse, in
     attn::BsParams bp;
     float2* rope_tab = nullptr;
     int* dmask = nullptr;
+    int ctas = 0;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         int rc = probe_device(dev);
         if (rc != ATTN_OK) return rc;
         if (rope && (rc = get_rope(dev, S, D, rope_base, &rope_tab)) != ATTN_OK) return rc;
-        if ((rc = get_mask(dev, row_ptr, col_idx, nrows, &dmask)) != ATTN_OK) return rc;
+        MaskEntry* me = nullptr;
+        if ((rc = get_mask(dev, row_ptr, col_idx, nrows, &dmask, &me)) != ATTN_OK) return rc;
+        const MaskSched* ms = nullptr;
+        if ((rc = get_mask_sched(dev, *me, nrows, static_cast<long long>(B) * Hq, &ms)) != ATTN_OK) return rc;
+        const long long ntasks = static_cast<long long>(B) * Hq * nrows;
+        bp.tasks = ms->d;
+        bp.task_off = ms->d + ntasks;
+        ctas = ms->ctas;
         bp.f.status = g_dev[dev].status;
     }
     if (!encode_bshd(&bp.f.tm_q, q, B, S, Hq, D) || !encode_bshd(&bp.f.tm_k, k, B, S, Hkv, D) ||
@@ -1027,18 +1070,18 @@ int bs_impl(const void* q, const void* k, const void* v, void* o, float* lse, in
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (ext) {
         if (D == 128) {
-            if (causal) return rope ? launch_bs<128, true, true, true>(bp, dev, nrows, st) : launch_bs<128, true, false, true>(bp, dev, nrows, st);
-            return rope ? launch_bs<128, false, true, true>(bp, dev, nrows, st) : launch_bs<128, false, false, true>(bp, dev, nrows, st);
+            if (causal) return rope ? launch_bs<128, true, true, true>(bp, dev, ctas, st) : launch_bs<128, true, false, true>(bp, dev, ctas, st);
+            return rope ? launch_bs<128, false, true, true>(bp, dev, ctas, st) : launch_bs<128, false, false, true>(bp, dev, ctas, st);
         }
-        if (causal) return rope ? launch_bs<64, true, true, true>(bp, dev, nrows, st) : launch_bs<64, true, false, true>(bp, dev, nrows, st);
-        return rope ? launch_bs<64, false, true, true>(bp, dev, nrows, st) : launch_bs<64, false, false, true>(bp, dev, nrows, st);
+        if (causal) return rope ? launch_bs<64, true, true, true>(bp, dev, ctas, st) : launch_bs<64, true, false, true>(bp, dev, ctas, st);
+        return rope ? launch_bs<64, false, true, true>(bp, dev, ctas, st) : launch_bs<64, false, false, true>(bp, dev, ctas, st);
     }
     if (D == 128) {
-        if (causal) return rope ? launch_bs<128, true, true>(bp, dev, nrows, st) : launch_bs<128, true, false>(bp, dev, nrows, st);
-        return rope ? launch_bs<128, false, true>(bp, dev, nrows, st) : launch_bs<128, false, false>(bp, dev, nrows, st);
+        if (causal) return rope ? launch_bs<128, true, true>(bp, dev, ctas, st) : launch_bs<128, true, false>(bp, dev, ctas, st);
+        return rope ? launch_bs<128, false, true>(bp, dev, ctas, st) : launch_bs<128, false, false>(bp, dev, ctas, st);
     }
-    if (causal) return rope ? launch_bs<64, true, true>(bp, dev, nrows, st) : launch_bs<64, true, false>(bp, dev, nrows, st);
-    return rope ? launch_bs<64, false, true>(bp, dev, nrows, st) : launch_bs<64, false, false>(bp, dev, nrows, st);
+    if (causal) return rope ? launch_bs<64, true, true>(bp, dev, ctas, st) : launch_bs<64, true, false>(bp, dev, ctas, st);
+    return rope ? launch_bs<64, false, true>(bp, dev, ctas, st) : launch_bs<64, false, false>(bp, dev, ctas, st);
 }
 
 extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -1184,6 +1227,7 @@ extern "C" void attn_release_cache(void) {
     for (auto& e : g_masks) {
         cudaSetDevice(e.dev);
         cudaFree(e.d);
+        for (auto& ms : e.sched) cudaFree(ms.d);
     }
     g_masks.clear();
     for (int d = 0; d < kMaxDevices; ++d) {

@@ -192,4 +192,33 @@ Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas
     return sc;
 }
 
+MaskSchedule build_mask_schedule(const int* row_ptr, int nrows, long long bh, int num_ctas) {
+    MaskSchedule sc;
+    const long long n = static_cast<long long>(nrows) * bh;
+    sc.ctas = static_cast<int>(std::max<long long>(1, std::min<long long>(num_ctas, n)));
+    // rows of tiles by cost, heaviest first; every batch-head of a row costs the same
+    std::vector<int> rows(nrows);
+    std::iota(rows.begin(), rows.end(), 0);
+    auto cost = [&](int i) { return static_cast<double>(row_ptr[i + 1] - row_ptr[i]) + kMaskTileFixedCost; };
+    std::stable_sort(rows.begin(), rows.end(), [&](int a, int b) { return cost(a) > cost(b); });
+    using Load = std::pair<double, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int c = 0; c < sc.ctas; ++c) heap.push({0.0, c});
+    std::vector<std::vector<int32_t>> bins(sc.ctas);
+    for (int i : rows)
+        for (long long x = 0; x < bh; ++x) {
+            Load top = heap.top();
+            heap.pop();
+            bins[top.second].push_back(static_cast<int32_t>(i * bh + x));
+            top.first += cost(i);
+            heap.push(top);
+        }
+    sc.offsets.push_back(0);
+    for (auto& bin : bins) {
+        sc.tasks.insert(sc.tasks.end(), bin.begin(), bin.end());
+        sc.offsets.push_back(static_cast<int32_t>(sc.tasks.size()));
+    }
+    return sc;
+}
+
 }  // namespace attn_host

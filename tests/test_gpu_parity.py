@@ -393,6 +393,72 @@ def test_blocksparse_forward_matches_oracle(B, Hq, Hkv, S, D, causal, base, kind
         _check(og, lg, o_ref, lse_ref, f"block-sparse {kind} S={S} (sampled)")
 
 
+# Shapes with several tasks (query tile, batch, head) per CTA of the persistent block-sparse
+# kernel (B * Hq * ceil(S/128) well above the 152 CTAs), so ring slots, barrier phases and the
+# overlap of one task's epilogue with the next task's loads and products run across tasks.
+# Rows are sampled over every batch, head and query tile.
+BS_MANY = [
+    # B, Hq, Hkv, S, D, causal, rope_base, mask
+    (4, 16, 8, 2048, 128, True, 10000.0, "bigbird"),     # 1024 tasks, RoPE, GQA
+    (8, 8, 8, 1024, 64, False, None, "empty_row"),       # 512 tasks: rows of 0, 1 and 2 listed tiles
+    (2, 16, 16, 4000, 128, False, 500000.0, "bigbird"),  # 1024 tasks, ragged last tile
+]
+
+
+def _sample_bhi(seed, B, Hq, S, n):
+    w = si.uniform_words(seed, 4242, 0, 3 * n)
+    rb = (w[:n] % np.uint64(B)).astype(np.int64)
+    rh = (w[n:2 * n] % np.uint64(Hq)).astype(np.int64)
+    ri = (w[2 * n:] % np.uint64(S)).astype(np.int64)
+    # every batch-head's last row and a row of every query tile of batch-head (0, 0)
+    bb, hh = np.meshgrid(np.arange(B), np.arange(Hq), indexing="ij")
+    tiles = np.arange(0, S, 128) + 127
+    rb = np.concatenate([rb, bb.ravel(), np.zeros(len(tiles), np.int64)])
+    rh = np.concatenate([rh, hh.ravel(), np.zeros(len(tiles), np.int64)])
+    ri = np.concatenate([ri, np.full(B * Hq, S - 1), np.minimum(tiles, S - 1)])
+    return rb, rh, ri
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base,kind", BS_MANY)
+def test_blocksparse_forward_many_tasks_per_cta(B, Hq, Hkv, S, D, causal, base, kind):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=750 + S)
+    rp, ci = _bs_mask(kind, S, causal)
+    o, lse = attn.attn_fwd_blocksparse(_dev(q), _dev(k), _dev(v), rp, ci, causal=causal, rope_base=base)
+    attn.attn_check()
+    rb, rh, ri = _sample_bhi(S + B, B, Hq, S, 768)
+    o_ref, lse_ref = oracle.attn_rows_bs(q, k, v, rp, ci, rb, rh, ri, causal=causal, rope_base=base)
+    og = o.float().cpu().numpy()[rb, ri, rh]
+    lg = lse.cpu().numpy()[rb, rh, ri]
+    empty = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lg), empty)
+    assert np.all(og[empty] == 0.0)
+    _check(og[~empty], lg[~empty], o_ref[~empty], lse_ref[~empty], f"block-sparse {kind} S={S} B={B} Hq={Hq}")
+    # the same call again gives the same bits (static schedule, no atomics)
+    o2, lse2 = attn.attn_fwd_blocksparse(_dev(q), _dev(k), _dev(v), rp, ci, causal=causal, rope_base=base)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+LOCAL_MANY = [
+    # B, Hq, Hkv, S, D, causal, rope_base, window, alibi
+    (4, 12, 12, 4096, 64, True, None, 512, False),   # the sliding-window workload's shape
+    (4, 12, 12, 2048, 64, True, None, 0, True),      # ALiBi, 768 tasks
+    (2, 8, 4, 3000, 128, False, 10000.0, 300, True),  # both, non-causal, RoPE, ragged
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base,window,alibi", LOCAL_MANY)
+def test_local_forward_many_tasks_per_cta(B, Hq, Hkv, S, D, causal, base, window, alibi):
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=950 + S)
+    o, lse = attn.attn_fwd_local(_dev(q), _dev(k), _dev(v), causal=causal, rope_base=base, window=window,
+                                 alibi=alibi)
+    attn.attn_check()
+    rb, rh, ri = _sample_bhi(S + 7, B, Hq, S, 768)
+    o_ref, lse_ref = oracle.attn_rows_local(q, k, v, rb, rh, ri, causal=causal, rope_base=base, window=window,
+                                            alibi=alibi)
+    _check(o.float().cpu().numpy()[rb, ri, rh], lse.cpu().numpy()[rb, rh, ri], o_ref, lse_ref,
+           f"local w={window} alibi={alibi} S={S} B={B} Hq={Hq}")
+
+
 def test_blocksparse_full_mask_matches_dense_forward():
     """Every block listed: the same attention as the dense kernel (both round operands alike)."""
     B, Hq, Hkv, S, D, base = 1, 4, 2, 700, 128, 10000.0

@@ -905,7 +905,7 @@ namespace {
 struct MaskSched {
     long long bh;
     int ctas;
-    int* d;  // tasks | offsets (ctas + 1)
+    int* d;  // tasks | offsets (2 ctas + 1)
 };
 struct MaskEntry {
     int dev;
@@ -998,11 +998,11 @@ int get_mask_sched(int dev, MaskEntry& me, int nrows, long long bh, const MaskSc
 
 namespace {
 
-template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
+template <int D, bool CAUSAL, bool ROPE, int EXT = 0>
 int launch_bs(const attn::BsParams& bp, int dev, int ctas, cudaStream_t st) {
     constexpr int kMin = 120 * 1024;  // one CTA per SM: each takes all 512 TMEM columns
     constexpr int smem = static_cast<int>(attn::BsLayout<D>::kAlloc) > kMin ? static_cast<int>(attn::BsLayout<D>::kAlloc) : kMin;
-    constexpr unsigned bit = 1u << (8 | (EXT ? 16 : 0) | (D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0));
+    constexpr unsigned bit = 1u << (8 + 8 * EXT + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0) + (ROPE ? 4 : 0));
     auto kern = attn::bs_fwd_kernel<D, CAUSAL, ROPE, EXT>;
     cudaError_t e;
     if (!(g_bwd_configured[dev] & bit)) {
@@ -1069,12 +1069,20 @@ int bs_impl(const void* q, const void* k, const void* v, void* o, float* lse, in
     bp.alibi = alibi;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (ext) {
-        if (D == 128) {
-            if (causal) return rope ? launch_bs<128, true, true, true>(bp, dev, ctas, st) : launch_bs<128, true, false, true>(bp, dev, ctas, st);
-            return rope ? launch_bs<128, false, true, true>(bp, dev, ctas, st) : launch_bs<128, false, false, true>(bp, dev, ctas, st);
+        if (alibi) {
+            if (D == 128) {
+                if (causal) return rope ? launch_bs<128, true, true, 2>(bp, dev, ctas, st) : launch_bs<128, true, false, 2>(bp, dev, ctas, st);
+                return rope ? launch_bs<128, false, true, 2>(bp, dev, ctas, st) : launch_bs<128, false, false, 2>(bp, dev, ctas, st);
+            }
+            if (causal) return rope ? launch_bs<64, true, true, 2>(bp, dev, ctas, st) : launch_bs<64, true, false, 2>(bp, dev, ctas, st);
+            return rope ? launch_bs<64, false, true, 2>(bp, dev, ctas, st) : launch_bs<64, false, false, 2>(bp, dev, ctas, st);
         }
-        if (causal) return rope ? launch_bs<64, true, true, true>(bp, dev, ctas, st) : launch_bs<64, true, false, true>(bp, dev, ctas, st);
-        return rope ? launch_bs<64, false, true, true>(bp, dev, ctas, st) : launch_bs<64, false, false, true>(bp, dev, ctas, st);
+        if (D == 128) {
+            if (causal) return rope ? launch_bs<128, true, true, 1>(bp, dev, ctas, st) : launch_bs<128, true, false, 1>(bp, dev, ctas, st);
+            return rope ? launch_bs<128, false, true, 1>(bp, dev, ctas, st) : launch_bs<128, false, false, 1>(bp, dev, ctas, st);
+        }
+        if (causal) return rope ? launch_bs<64, true, true, 1>(bp, dev, ctas, st) : launch_bs<64, true, false, 1>(bp, dev, ctas, st);
+        return rope ? launch_bs<64, false, true, 1>(bp, dev, ctas, st) : launch_bs<64, false, false, 1>(bp, dev, ctas, st);
     }
     if (D == 128) {
         if (causal) return rope ? launch_bs<128, true, true>(bp, dev, ctas, st) : launch_bs<128, true, false>(bp, dev, ctas, st);

@@ -3,26 +3,28 @@
 // kernel visits only those, so its work is proportional to the active share).
 //
 // Blocks are the kernel's 128 x 128 tiles.  A task is one query tile of one
-// (batch, head).  One persistent CTA per SM runs a host-built list of tasks
-// (heaviest rows first, balanced by listed tiles), so that the fixed costs of
-// a task overlap the neighbouring tasks: the next task's K/V tiles and its Q
-// load and rotation start while the current task's softmax runs its merge and
-// output stores, and its first Q K^T products form before those stores end.
-// Per task, Q is loaded and rotated once; the listed key tiles are visited in
-// descending order and dealt alternately to two softmax streams, as the
-// prefill deals two query tiles to its two stages:
-//   S_s = Q K^T (tcgen05, TMEM)  ->  online softmax of stream s, P in bf16 over S_s  ->  O_s += P V.
-// Each stream keeps its own running maximum, sum and O accumulator; the two
-// merge by their maxima once, in the epilogue.  While one stream's softmax
-// works, the tensor cores form the other stream's S and accumulate its last
-// P V.  K and V tiles sit in separate three-slot rings, so a K slot refills as
-// soon as its S is formed.  Roles: two softmax warpgroups (one thread per query
-// row), four RoPE warps, a TMA warp and an MMA warp.  A row of blocks with
-// nothing listed writes O = 0 and LSE = -inf.  Every wait is bounded.
+// (batch, head): Q is loaded and rotated once, and the listed key tiles are
+// visited in descending order,
+//   S = Q K^T (tcgen05, TMEM)  ->  online softmax, P in bf16 over S  ->  O += P V.
+// One persistent CTA per SM runs two task streams side by side, as the prefill
+// runs its two query-tile stages: each stream has its own Q slot, S and O in
+// TMEM, and softmax warpgroup (one thread per query row), and walks its own
+// host-built task list (heaviest tasks first, the streams balanced by listed
+// tiles).  The tensor cores alternate between the streams: while one stream's
+// softmax works on its S, they accumulate the other stream's P V and form its
+// next S.  One stream's task boundary (the epilogue, the next Q load and
+// rotation) thus overlaps the other stream's tiles.  K and V tiles of both
+// streams pass through one K ring (three slots) and one V ring (two slots) in
+// the order the tensor cores consume them.  Roles: two softmax warpgroups,
+// four RoPE warps, a TMA warp and an MMA warp.  A row of blocks with nothing
+// listed writes O = 0 and LSE = -inf.  Every wait is bounded.
 //
-// The EXT variant adds the sliding_window and alibi combinators ("AttnFuse",
+// The EXT variants add the sliding_window and alibi combinators ("AttnFuse",
 // sec. 3): key j is visible to query i only when |i - j| < window, and the
-// score gains -m_h |i - j| with m_h = 2^(-8 (h+1) / Hq).
+// score gains -m_h |i - j| with m_h = 2^(-8 (h+1) / Hq).  EXT = 1 is the window
+// alone, EXT = 2 ALiBi with or without the window; each instance carries only
+// the softmax forms it can take, which keeps the code within the instruction
+// cache.
 #pragma once
 
 #include "bwd_kernel.cuh"
@@ -35,67 +37,68 @@ struct BsParams {
     const int* col_idx;    // listed key tiles of each row of tiles, ascending
     int window;            // EXT: visible iff |i - j| < window (0: no window)
     int alibi;             // EXT: ALiBi bias on
-    const int* tasks;      // task t = query tile * (B * Hq) + b * Hq + h, per-CTA lists
-    const int* task_off;   // [gridDim.x + 1]: CTA c runs tasks[task_off[c] .. task_off[c+1])
+    const int* tasks;      // task t = query tile * (B * Hq) + b * Hq + h
+    const int* task_off;   // [2 gridDim.x + 1]: stream s of CTA c runs tasks[task_off[2c+s] .. task_off[2c+s+1])
 };
 
 constexpr int kBsThreads = 448;  // warps 0-7 softmax (two streams), 8-11 RoPE, 12 TMA, 13 MMA
 constexpr int kBsWarpRope = 8, kBsWarpTma = 12, kBsWarpMma = 13;
-constexpr int kBsSlots = 3;      // K slots and V slots
+constexpr int kBsMaxSlots = 5;  // barrier room per ring
 
 template <int D>
 struct BsLayout {
+    // ring depths: with D = 128 this is what fits beside the two Q slots in 227 KB; deeper rings
+    // (up to five slots at D = 64) measured no faster
+    static constexpr int KS = 3, VS = 2;
+    static_assert(KS <= kBsMaxSlots && VS <= kBsMaxSlots, "ring depth");
     static constexpr uint32_t kTile = 128u * D * 2u;
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK0 = kTile;                   // K slot r at kK0 + r kTile
-    static constexpr uint32_t kV0 = kK0 + kBsSlots * kTile;  // V slot r at kV0 + r kTile
-    static constexpr uint32_t kBars = kV0 + kBsSlots * kTile;
-    static constexpr uint32_t kMisc = kBars + 256;
+    static constexpr uint32_t kQ0 = 0;                 // Q slot of stream s at kQ0 + s kTile
+    static constexpr uint32_t kK0 = 2 * kTile;         // K slot r at kK0 + r kTile
+    static constexpr uint32_t kV0 = kK0 + KS * kTile;  // V slot r at kV0 + r kTile
+    static constexpr uint32_t kBars = kV0 + VS * kTile;
+    static constexpr uint32_t kMisc = kBars + 512;
     static constexpr uint32_t kBytes = kMisc + 64;
     static constexpr uint32_t kAlloc = kBytes + 1024;
-    // epilogue: [2 streams][128 rows] float2 (m, l) over the Q tile, which every product of the
-    // task has read by then; the next task's Q is loaded once both streams have read it
-    static constexpr uint32_t kMerge = kQ;
 };
 
 enum : int {
-    BS_Q_FULL = 0,
-    BS_Q_ROT,
-    BS_Q_EMPTY,                         // both streams read the merge values: Q may be reloaded
-    BS_K_FULL,                          // [3]
-    BS_K_ROT = BS_K_FULL + kBsSlots,    // [3]
-    BS_K_EMPTY = BS_K_ROT + kBsSlots,   // [3] S of the slot's tile formed
-    BS_V_FULL = BS_K_EMPTY + kBsSlots,  // [3]
-    BS_V_EMPTY = BS_V_FULL + kBsSlots,  // [3] P V of the slot's tile done
-    BS_S_FULL = BS_V_EMPTY + kBsSlots,  // [2] per stream
-    BS_P_FULL = BS_S_FULL + 2,          // [2] per stream
-    BS_O_FULL = BS_P_FULL + 2,
-    BS_O_FREE,                          // both streams read O_0 and O_1: the next task may accumulate
-    BS_DRAIN,
-    BS_MERGE,
+    BS_Q_FULL = 0,                         // [2] per stream
+    BS_Q_ROT = BS_Q_FULL + 2,              // [2]
+    BS_Q_EMPTY = BS_Q_ROT + 2,             // [2] the task's last S formed: the slot may be reloaded
+    BS_K_FULL = BS_Q_EMPTY + 2,              // [K slots]
+    BS_K_ROT = BS_K_FULL + kBsMaxSlots,      // [K slots]
+    BS_K_EMPTY = BS_K_ROT + kBsMaxSlots,     // [K slots] S of the slot's tile formed
+    BS_V_FULL = BS_K_EMPTY + kBsMaxSlots,    // [V slots]
+    BS_V_EMPTY = BS_V_FULL + kBsMaxSlots,    // [V slots] P V of the slot's tile done
+    BS_S_FULL = BS_V_EMPTY + kBsMaxSlots,    // [2] per stream
+    BS_P_FULL = BS_S_FULL + 2,             // [2]
+    BS_O_FULL = BS_P_FULL + 2,             // [2] the task's last P V done
+    BS_O_FREE = BS_O_FULL + 2,             // [2] the epilogue read O: the next task may accumulate
+    BS_DRAIN = BS_O_FREE + 2,
     BS_NUM
 };
-static_assert(BS_NUM * 8 <= 256, "barrier block");
+static_assert(BS_NUM * 8 <= 512, "barrier block");
 
 __device__ __forceinline__ void bs_init_bars(uint32_t bar0) {
-    mbar_init(bar_at(bar0, BS_Q_FULL), 1);
-    mbar_init(bar_at(bar0, BS_Q_ROT), 128);
-    mbar_init(bar_at(bar0, BS_Q_EMPTY), 256);
-    for (int r = 0; r < kBsSlots; ++r) {
+    for (int s = 0; s < 2; ++s) {
+        mbar_init(bar_at(bar0, BS_Q_FULL + s), 1);
+        mbar_init(bar_at(bar0, BS_Q_ROT + s), 128);
+        mbar_init(bar_at(bar0, BS_Q_EMPTY + s), 1);
+        mbar_init(bar_at(bar0, BS_S_FULL + s), 1);
+        mbar_init(bar_at(bar0, BS_P_FULL + s), 128);
+        mbar_init(bar_at(bar0, BS_O_FULL + s), 1);
+        mbar_init(bar_at(bar0, BS_O_FREE + s), 128);
+    }
+    for (int r = 0; r < kBsMaxSlots; ++r) {
         mbar_init(bar_at(bar0, BS_K_FULL + r), 1);
         mbar_init(bar_at(bar0, BS_K_ROT + r), 128);
         mbar_init(bar_at(bar0, BS_K_EMPTY + r), 1);
+    }
+    for (int r = 0; r < kBsMaxSlots; ++r) {
         mbar_init(bar_at(bar0, BS_V_FULL + r), 1);
         mbar_init(bar_at(bar0, BS_V_EMPTY + r), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-        mbar_init(bar_at(bar0, BS_S_FULL + s), 1);
-        mbar_init(bar_at(bar0, BS_P_FULL + s), 128);
-    }
-    mbar_init(bar_at(bar0, BS_O_FULL), 1);
-    mbar_init(bar_at(bar0, BS_O_FREE), 256);
     mbar_init(bar_at(bar0, BS_DRAIN), 1);
-    mbar_init(bar_at(bar0, BS_MERGE), 256);
     fence_barrier_init();
     fence_proxy_async_smem();
 }
@@ -194,7 +197,45 @@ __device__ __forceinline__ BsTask bs_task(const BsParams& p, int ti) {
     return k;
 }
 
-template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
+// A stream's position in its flattened tile sequence (the listed tiles of its
+// non-empty tasks, task by task).  The TMA, RoPE and MMA roles each walk both
+// streams' sequences in the same interleaved order.
+struct BsCursor {
+    int ti, te;  // current task index, end of the stream's list
+    int it;      // tile of the current task
+    BsTask k;
+    __device__ __forceinline__ void skip_empty(const BsParams& p) {
+        for (; ti < te; ++ti) {
+            k = bs_task(p, ti);
+            if (k.nblk > 0) return;
+        }
+    }
+    __device__ __forceinline__ void init(const BsParams& p, int begin, int end) {
+        ti = begin;
+        te = end;
+        it = 0;
+        skip_empty(p);
+    }
+    __device__ __forceinline__ bool valid() const { return ti < te; }
+    __device__ __forceinline__ bool first() const { return it == 0; }
+    __device__ __forceinline__ bool last() const { return it == k.nblk - 1; }
+    __device__ __forceinline__ int ktile(const BsParams& p) const { return p.col_idx[k.e0 + k.nblk - 1 - it]; }
+    __device__ __forceinline__ void next(const BsParams& p) {
+        if (++it < k.nblk) return;
+        it = 0;
+        ++ti;
+        skip_empty(p);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void bs_swap(T& a, T& b) {
+    const T t = a;
+    a = b;
+    b = t;
+}
+
+template <int D, bool CAUSAL, bool ROPE, int EXT = 0>
 __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_constant__ BsParams p) {
     using L = BsLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -205,9 +246,9 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smg + L::kMisc + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const FwdParams& f = p.f;
-    const int t_begin = p.task_off[blockIdx.x], t_end = p.task_off[blockIdx.x + 1];
-    // Every role walks the same task list and skips the empty rows the same way; ring slots and
-    // barrier phases count K/V tiles (kit) and non-empty tasks (qn) over the whole list.
+    // stream 0 runs tasks [tb0, tb1), stream 1 runs [tb1, te1)
+    const int tb0 = p.task_off[2 * blockIdx.x], tb1 = p.task_off[2 * blockIdx.x + 1];
+    const int te1 = p.task_off[2 * blockIdx.x + 2];
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -229,36 +270,35 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
     const WaitCtl ctl{abort_flag, f.status, f.wait_limit_ns};
 
     if (warp < 8) {
-        // ---- softmax stream st (tiles st, st + 2, ... of each task): thread t owns query row 128 i + t
+        // ---- softmax of stream st: thread t owns query row 128 i + t (TMEM lane t) of each task
         const int t = threadIdx.x % 128, st = threadIdx.x / 128;
         const uint32_t trow = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const uint32_t tS = trow + 128u * st, tO = trow + 256u + static_cast<uint32_t>(st * D);
         const float c = f.scale_log2;
-        float2* ml = reinterpret_cast<float2*>(smg + L::kMerge);
-        int sit = 0, qn = 0;  // S tiles of this stream, non-empty tasks
+        const int tb = st ? tb1 : tb0, te = st ? te1 : tb1;
+        int sit = 0, oit = 0;  // S tiles and finished tasks of this stream (barrier phases)
         bool ok = true;
-        for (int ti = t_begin; ti < t_end && ok; ++ti) {
+        for (int ti = tb; ti < te && ok; ++ti) {
             const BsTask k = bs_task(p, ti);
             const int row = k.i * 128 + t;
             const bool store = row < f.S;
             __nv_bfloat16* dst = f.o + ((static_cast<size_t>(k.b) * f.S + (store ? row : 0)) * f.Hq + k.h) * D;
             const size_t lse_at = (static_cast<size_t>(k.b) * f.Hq + k.h) * f.S + row;
-            if (k.nblk == 0) {
-                // nothing listed: O = 0 (this stream's half of the channels), LSE = -inf
+            if (k.nblk == 0) {  // nothing listed: O = 0, LSE = -inf
                 if (store) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + st * (D / 2));
+                    uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                    for (int q = 0; q < D / 16; ++q) d4[q] = make_uint4(0u, 0u, 0u, 0u);
-                    if (st == 0 && f.lse != nullptr) f.lse[lse_at] = -INFINITY;
+                    for (int q = 0; q < D / 8; ++q) d4[q] = make_uint4(0u, 0u, 0u, 0u);
+                    if (f.lse != nullptr) f.lse[lse_at] = -INFINITY;
                 }
                 continue;
             }
-            const float m2 = (EXT && p.alibi) ? exp2f(-8.f * static_cast<float>(k.h + 1) / static_cast<float>(f.Hq)) *
+            const float m2 = (EXT == 2 && p.alibi) ? exp2f(-8.f * static_cast<float>(k.h + 1) / static_cast<float>(f.Hq)) *
                                                     1.4426950408889634f
                                               : 0.f;
             // m: raw score units (as the prefill), or log2 units of the biased score with EXT
             float m_used = -INFINITY, l = 0.f;
-            for (int it = st; it < k.nblk && ok; it += 2) {
+            for (int it = 0; it < k.nblk && ok; ++it) {
                 const int kv0 = p.col_idx[k.e0 + k.nblk - 1 - it] * 128;
                 ok = bwd_wait(bar_at(bar0, BS_S_FULL + st), sit & 1, ctl, kStatusSoftmax);
                 ++sit;
@@ -279,22 +319,22 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                 // 0 = the general form
                 int kind = 0;
                 float a_lin = 0.f, b_lin = 0.f;
-                if constexpr (EXT) {
-                    if (m2 == 0.f && __all_sync(0xffffffffu, lo <= 0)) {
-                        kind = 1;
-                    } else if (__all_sync(0xffffffffu, lo <= 0 && limit >= 128 && (kv0 >= row || kv0 + 127 <= row))) {
+                if constexpr (EXT == 1) {
+                    if (__all_sync(0xffffffffu, lo <= 0)) kind = 1;
+                } else if constexpr (EXT == 2) {
+                    if (__all_sync(0xffffffffu, lo <= 0 && limit >= 128 && (kv0 >= row || kv0 + 127 <= row))) {
                         kind = 2;
                         a_lin = kv0 >= row ? -m2 : m2;
                         b_lin = a_lin * static_cast<float>(rel0);
                     }
                 }
                 float mx;
-                if (EXT && kind == 0) mx = ext_row_max(tS, lo, limit, c, m2, static_cast<float>(rel0));
-                else if (EXT && kind == 2) mx = alibi_row_max(tS, c, a_lin, b_lin);
+                if (EXT != 0 && kind == 0) mx = ext_row_max(tS, lo, limit, c, m2, static_cast<float>(rel0));
+                else if (EXT == 2 && kind == 2) mx = alibi_row_max(tS, c, a_lin, b_lin);
                 else mx = (masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit)) * (EXT ? c : 1.f);
                 const float m_new = fmaxf(m_used, mx);
                 const float unit = EXT ? 1.f : c;
-                if (it == st) {
+                if (it == 0) {
                     m_used = m_new;
                 } else {
                     const bool need = (m_new - m_used) * unit > kRescaleThreshold;
@@ -306,7 +346,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                             l *= alpha;
                         }
                         const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
+#pragma unroll 1
                         for (int cc = 0; cc < D; cc += 32) {
                             uint32_t r[32];
                             tmem_load_32(tO + cc, r);
@@ -321,203 +361,235 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                         }
                     }
                 }
-                if (EXT && kind == 0) {
+                if (EXT != 0 && kind == 0) {
                     l += ext_exp_to_p(tS, lo, limit, c, m2, static_cast<float>(rel0), m_used);
-                } else if (EXT && kind == 2) {
+                } else if (EXT == 2 && kind == 2) {
                     l += alibi_exp_to_p(tS, c, a_lin, b_lin, m_used);  // m is finite: every key is seen
-                } else if (EXT) {
-                    const float mc = m_used == -INFINITY ? 0.f : m_used;  // log2 units
-                    l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
                 } else {
                     // a row that has seen only masked keys so far (m = -inf) gets P = 0
-                    const float mc = m_used == -INFINITY ? 0.f : m_used * c;
+                    const float mc = m_used == -INFINITY ? 0.f : m_used * (EXT ? 1.f : c);
                     l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
                 }
                 tmem_store_wait();
                 tc_fence_before();
                 mbar_arrive(bar_at(bar0, BS_P_FULL + st));
             }
-            // epilogue: merge the two streams by their maxima (log2 units); each writes D/2 channels
-            if (ok) ok = bwd_wait(bar_at(bar0, BS_O_FULL), qn & 1, ctl, kStatusSoftmax);
+            // epilogue: O / l in bf16, LSE in natural log
+            if (ok) ok = bwd_wait(bar_at(bar0, BS_O_FULL + st), oit & 1, ctl, kStatusSoftmax);
+            ++oit;
             if (!ok) break;
             tc_fence_after();
-            ml[st * 128 + t] = make_float2(EXT ? m_used : m_used * c, l);
-            mbar_arrive(bar_at(bar0, BS_MERGE));
-            ok = bwd_wait(bar_at(bar0, BS_MERGE), qn & 1, ctl, kStatusSoftmax);
-            if (!ok) break;
-            const float2 a = ml[t], bb = ml[128 + t];
-            fence_proxy_async_smem();  // the next task's Q copy overwrites the merge values
-            mbar_arrive(bar_at(bar0, BS_Q_EMPTY));
-            const float M = fmaxf(a.x, bb.x);
-            const float sa = a.x == -INFINITY ? 0.f : ex2_approx(a.x - M);
-            const float sb = bb.x == -INFINITY ? 0.f : ex2_approx(bb.x - M);
-            const float Lsum = a.y * sa + bb.y * sb;
-            const bool have1 = k.nblk >= 2;  // stream 1 sees tiles only from the second on
-            const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-            const uint32_t tO0 = trow + 256u, tO1 = trow + 256u + D;
+            const float inv = l > 0.f ? 1.0f / l : 0.f;
+            const uint64_t il2 = f2_pack(inv, inv);
 #pragma unroll
-            for (int cc = 0; cc < D / 2; cc += 32) {
-                const int d0 = st * (D / 2) + cc;  // this stream's output channels
-                uint32_t ra[32], rb[32];
-                tmem_load_32_async(tO0 + d0, ra);
-                if (have1) tmem_load_32_async(tO1 + d0, rb);
-                tmem_wait_ld_32(ra);
-                if (have1) tmem_wait_ld_32(rb);
-                if (cc + 32 >= D / 2) {  // last read of O_0 and O_1 by this thread
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t r[32];
+                tmem_load_32(tO + cc, r);
+                if (cc + 32 == D) {  // the last read of O_st by this thread
                     tc_fence_before();
-                    mbar_arrive(bar_at(bar0, BS_O_FREE));
+                    mbar_arrive(bar_at(bar0, BS_O_FREE + st));
                 }
                 uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    float o0 = __uint_as_float(ra[j]) * sa, o1 = __uint_as_float(ra[j + 1]) * sa;
-                    if (have1) {
-                        o0 += __uint_as_float(rb[j]) * sb;
-                        o1 += __uint_as_float(rb[j + 1]) * sb;
-                    }
-                    pk[j / 2] = pack_bf16x2(o0 * inv, o1 * inv);
+                for (int j = 0; j < 16; ++j) {
+                    float x0, x1;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il2), x0, x1);
+                    pk[j] = pack_bf16x2(x0, x1);
                 }
                 if (store) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + d0);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
-            if (st == 0 && store && f.lse != nullptr)
-                f.lse[lse_at] = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-            ++qn;
+            if (store && f.lse != nullptr)
+                f.lse[lse_at] = l > 0.f ? ((EXT ? m_used : m_used * c) + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
     } else if (warp < kBsWarpTma) {
-        // ---- RoPE warps: each task's Q once, then each of its K tiles in its slot
+        // ---- RoPE warps: Q of each task once, then each K tile in its slot, in the order the
+        // tensor cores consume them
         if (ROPE) {
             const int t = threadIdx.x - kBsWarpRope * 32;
             RopeConsts rc;
             rope_load_consts<D>(f, t, rc);
             uint64_t cb[4], sb[4];
-            int kit = 0, qn = 0;
-            bool ok = true;
-            for (int ti = t_begin; ti < t_end && ok; ++ti) {
-                const BsTask k = bs_task(p, ti);
-                if (k.nblk == 0) continue;
-                rope_load_base<D>(f, k.i, t, cb, sb);
-                ok = bwd_wait(bar_at(bar0, BS_Q_FULL), qn & 1, ctl, kStatusRope);
-                if (!ok) break;
-                rope_rotate_tile<D, false>(smg + L::kQ, rc, cb, sb, t);
-                fence_proxy_async_smem();
-                mbar_arrive(bar_at(bar0, BS_Q_ROT));
-                for (int it = 0; it < k.nblk && ok; ++it) {
-                    const int gi = kit + it, r = gi % kBsSlots;
-                    rope_load_base<D>(f, p.col_idx[k.e0 + k.nblk - 1 - it], t, cb, sb);
-                    ok = bwd_wait(bar_at(bar0, BS_K_FULL + r), (gi / kBsSlots) & 1, ctl, kStatusRope);
-                    if (!ok) break;
-                    rope_rotate_tile<D, false>(smg + L::kK0 + r * L::kTile, rc, cb, sb, t);
+            BsCursor c0, c1;
+            c0.init(p, tb0, tb1);
+            c1.init(p, tb1, te1);
+            int kq = 0, qn0 = 0, qn1 = 0;
+            auto rope_for_s = [&](const BsCursor& cu, int s, int& qn) -> bool {
+                if (cu.first()) {
+                    rope_load_base<D>(f, cu.k.i, t, cb, sb);
+                    if (!bwd_wait(bar_at(bar0, BS_Q_FULL + s), qn & 1, ctl, kStatusRope)) return false;
+                    ++qn;
+                    rope_rotate_tile<D, false>(smg + L::kQ0 + s * L::kTile, rc, cb, sb, t);
                     fence_proxy_async_smem();
-                    mbar_arrive(bar_at(bar0, BS_K_ROT + r));
+                    mbar_arrive(bar_at(bar0, BS_Q_ROT + s));
                 }
-                kit += k.nblk;
-                ++qn;
+                const int r = kq % L::KS;
+                rope_load_base<D>(f, cu.ktile(p), t, cb, sb);
+                if (!bwd_wait(bar_at(bar0, BS_K_FULL + r), (kq / L::KS) & 1, ctl, kStatusRope)) return false;
+                ++kq;
+                rope_rotate_tile<D, false>(smg + L::kK0 + r * L::kTile, rc, cb, sb, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar_at(bar0, BS_K_ROT + r));
+                return true;
+            };
+            // c0 is the stream whose turn it is (s); it swaps with c1 after each turn, so every
+            // step has one copy in the code
+            bool ok = true, go0 = false, go1 = false;
+            int s = 0;
+            while (ok && (c0.valid() || c1.valid())) {
+                if (c0.valid()) {
+                    if (go0) c0.next(p);
+                    go0 = true;
+                    if (c0.valid()) ok = rope_for_s(c0, s, qn0);
+                }
+                bs_swap(c0, c1);
+                bs_swap(qn0, qn1);
+                bs_swap(go0, go1);
+                s ^= 1;
             }
         }
     } else if (warp == kBsWarpTma) {
-        // ---- producer: per task, the first K/V tile, then Q (once the previous task's merge has
-        // read its copy of Q), then the other K/V tiles, into their rings
+        // ---- producer: Q, K and V tiles of both streams in the order the tensor cores consume
+        // them (S_0, S_1 first, then per round P V_0, the next S_0, P V_1, the next S_1)
         if (lane == 0) {
-            int kit = 0, qn = 0;
-            bool ok = true;
-            for (int ti = t_begin; ti < t_end && ok; ++ti) {
-                const BsTask k = bs_task(p, ti);
-                if (k.nblk == 0) continue;
-                for (int it = 0; it < k.nblk && ok; ++it) {
-                    const int gi = kit + it, r = gi % kBsSlots, n = gi / kBsSlots;
-                    const int kv0 = p.col_idx[k.e0 + k.nblk - 1 - it] * 128;
-                    if (n >= 1 && !mbar_wait(bar_at(bar0, BS_K_EMPTY + r), (n - 1) & 1, ctl, kStatusProducer)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t kb = bar_at(bar0, BS_K_FULL + r);
-                    mbar_arrive_expect_tx(kb, L::kTile);
+            BsCursor c0, c1;
+            c0.init(p, tb0, tb1);
+            c1.init(p, tb1, te1);
+            int kq = 0, vq = 0, ql0 = 0, ql1 = 0;
+            auto load_for_s = [&](const BsCursor& cu, int s, int& ql) -> bool {
+                if (cu.first()) {  // the task's Q, once the stream's previous task formed its last S
+                    if (ql >= 1 && !mbar_wait(bar_at(bar0, BS_Q_EMPTY + s), (ql - 1) & 1, ctl, kStatusProducer))
+                        return false;
+                    ++ql;
+                    const uint32_t qb = bar_at(bar0, BS_Q_FULL + s);
+                    mbar_arrive_expect_tx(qb, L::kTile);
 #pragma unroll
                     for (int sub = 0; sub < D / 64; ++sub)
-                        tma_load_4d(sm + L::kK0 + r * L::kTile + sub * kSubTileBytes, &f.tm_k, kb, sub * 64, k.g, kv0, k.b);
-                    if (n >= 1 && !mbar_wait(bar_at(bar0, BS_V_EMPTY + r), (n - 1) & 1, ctl, kStatusProducer)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t vb = bar_at(bar0, BS_V_FULL + r);
-                    mbar_arrive_expect_tx(vb, L::kTile);
-#pragma unroll
-                    for (int sub = 0; sub < D / 64; ++sub)
-                        tma_load_4d(sm + L::kV0 + r * L::kTile + sub * kSubTileBytes, &f.tm_v, vb, sub * 64, k.g, kv0, k.b);
-                    if (it == 0) {
-                        if (qn >= 1 && !mbar_wait(bar_at(bar0, BS_Q_EMPTY), (qn - 1) & 1, ctl, kStatusProducer)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t qb = bar_at(bar0, BS_Q_FULL);
-                        mbar_arrive_expect_tx(qb, L::kTile);
-#pragma unroll
-                        for (int sub = 0; sub < D / 64; ++sub)
-                            tma_load_4d(sm + L::kQ + sub * kSubTileBytes, &f.tm_q, qb, sub * 64, k.h, k.i * 128, k.b);
-                    }
+                        tma_load_4d(sm + L::kQ0 + s * L::kTile + sub * kSubTileBytes, &f.tm_q, qb, sub * 64, cu.k.h,
+                                    cu.k.i * 128, cu.k.b);
                 }
-                kit += k.nblk;
-                ++qn;
+                const int r = kq % L::KS, n = kq / L::KS;
+                if (n >= 1 && !mbar_wait(bar_at(bar0, BS_K_EMPTY + r), (n - 1) & 1, ctl, kStatusProducer)) return false;
+                ++kq;
+                const uint32_t kb = bar_at(bar0, BS_K_FULL + r);
+                mbar_arrive_expect_tx(kb, L::kTile);
+#pragma unroll
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_4d(sm + L::kK0 + r * L::kTile + sub * kSubTileBytes, &f.tm_k, kb, sub * 64, cu.k.g,
+                                cu.ktile(p) * 128, cu.k.b);
+                return true;
+            };
+            auto load_v = [&](const BsCursor& cu) -> bool {
+                const int r = vq % L::VS, n = vq / L::VS;
+                if (n >= 1 && !mbar_wait(bar_at(bar0, BS_V_EMPTY + r), (n - 1) & 1, ctl, kStatusProducer)) return false;
+                ++vq;
+                const uint32_t vb = bar_at(bar0, BS_V_FULL + r);
+                mbar_arrive_expect_tx(vb, L::kTile);
+#pragma unroll
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_4d(sm + L::kV0 + r * L::kTile + sub * kSubTileBytes, &f.tm_v, vb, sub * 64, cu.k.g,
+                                cu.ktile(p) * 128, cu.k.b);
+                return true;
+            };
+            // c0 is the stream whose turn it is (s), as in the RoPE loop: its first turn loads
+            // for S only, each later turn the V tile of its last S and then its next S
+            bool ok = true, go0 = false, go1 = false;
+            int s = 0;
+            while (ok && (c0.valid() || c1.valid())) {
+                if (c0.valid()) {
+                    if (go0) {
+                        ok = load_v(c0);
+                        c0.next(p);
+                    }
+                    go0 = true;
+                    if (ok && c0.valid()) ok = load_for_s(c0, s, ql0);
+                }
+                bs_swap(c0, c1);
+                bs_swap(ql0, ql1);
+                bs_swap(go0, go1);
+                s ^= 1;
             }
         }
         __syncwarp();
     } else if (warp == kBsWarpMma && lane == 0) {
-        // ---- MMA issuer.  Tile it of a task goes to stream it % 2: S_s = Q K^T (K-major, fp16 after
-        // RoPE), then, once that stream's softmax has handed P back, O_s += P V (P from TMEM, V
-        // MN-major).  Issue order S(it), then P V(it - 1): the tensor cores form one stream's S while
-        // the other stream's softmax works.  A task's first P V waits until the previous task's
-        // epilogue has read O_0 and O_1; its S products need not.
+        // ---- MMA issuer.  Per stream s: S_s = Q_s K^T (K-major, fp16 after RoPE), then, once the
+        // stream's softmax has handed P back, O_s += P V (P from TMEM, V MN-major) followed at once
+        // by the stream's next S, as the prefill issues its stages.  The streams alternate, so the
+        // tensor cores work on one stream while the other's softmax runs.  A task's first P V
+        // waits until the stream's previous epilogue has read O_s.
         const uint32_t kIdescS = umma_idesc_f16(ROPE ? 0u : 1u, 0u, 128, 128);
         constexpr uint32_t kIdescPV = umma_idesc_f16(1u, 1u, 128, D);
-        const uint64_t qdesc = sw128_desc(sm + L::kQ, 16u, 1024u);
-        int kit = 0, qn = 0, pc0 = 0, pc1 = 0;
-        bool ok = true;
-        for (int ti = t_begin; ti < t_end && ok; ++ti) {
-            const BsTask k = bs_task(p, ti);
-            if (k.nblk == 0) continue;
-            ok = mbar_wait(bar_at(bar0, BS_Q_FULL), qn & 1, ctl, kStatusMma);
-            if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BS_Q_ROT), qn & 1, ctl, kStatusMma);
-            for (int it = 0; it <= k.nblk && ok; ++it) {
-                if (it < k.nblk) {
-                    const int gi = kit + it, r = gi % kBsSlots, n = gi / kBsSlots, s = it & 1;
-                    ok = mbar_wait(bar_at(bar0, BS_K_FULL + r), n & 1, ctl, kStatusMma);
-                    if (ok && ROPE) ok = mbar_wait(bar_at(bar0, BS_K_ROT + r), n & 1, ctl, kStatusMma);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t kdesc = sw128_desc(sm + L::kK0 + r * L::kTile, 16u, 1024u);
-                    const uint32_t tS = tmem + 128u * s;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)),
-                                kIdescS, kk > 0 ? 1u : 0u);
-                    tc_commit(bar_at(bar0, BS_K_EMPTY + r));  // the K slot refills once this S is formed
-                    tc_commit(bar_at(bar0, BS_S_FULL + s));
-                }
-                if (it >= 1) {
-                    const int pt = it - 1, ps = pt & 1, gp = kit + pt, pr = gp % kBsSlots;
-                    const int pc = ps ? pc1++ : pc0++;
-                    ok = mbar_wait(bar_at(bar0, BS_P_FULL + ps), pc & 1, ctl, kStatusMma);
-                    if (ok) ok = mbar_wait(bar_at(bar0, BS_V_FULL + pr), (gp / kBsSlots) & 1, ctl, kStatusMma);
-                    if (ok && pt == 0 && qn >= 1) ok = mbar_wait(bar_at(bar0, BS_O_FREE), (qn - 1) & 1, ctl, kStatusMma);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t vdesc = sw128_desc(sm + L::kV0 + pr * L::kTile, kSubTileBytes, 1024u);
-                    const uint32_t tS = tmem + 128u * ps, tO = tmem + 256u + static_cast<uint32_t>(ps * D);
-                    // 16 keys per step: 2048 bytes of V, 8 TMEM columns of P
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV,
-                                (pt >= 2 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar_at(bar0, BS_V_EMPTY + pr));
-                }
+        BsCursor c0, c1;
+        c0.init(p, tb0, tb1);
+        c1.init(p, tb1, te1);
+        int kq = 0, vq = 0, qn0 = 0, qn1 = 0, pq0 = 0, pq1 = 0, dn0 = 0, dn1 = 0;
+        auto issue_s = [&](const BsCursor& cu, int s, int& qn) -> bool {
+            if (cu.first()) {
+                if (!mbar_wait(bar_at(bar0, BS_Q_FULL + s), qn & 1, ctl, kStatusMma)) return false;
+                if (ROPE && !mbar_wait(bar_at(bar0, BS_Q_ROT + s), qn & 1, ctl, kStatusMma)) return false;
+                ++qn;
             }
-            if (ok) tc_commit(bar_at(bar0, BS_O_FULL));
-            kit += k.nblk;
-            ++qn;
+            const int r = kq % L::KS, n = kq / L::KS;
+            if (!mbar_wait(bar_at(bar0, BS_K_FULL + r), n & 1, ctl, kStatusMma)) return false;
+            if (ROPE && !mbar_wait(bar_at(bar0, BS_K_ROT + r), n & 1, ctl, kStatusMma)) return false;
+            ++kq;
+            tc_fence_after();
+            const uint64_t qdesc = sw128_desc(sm + L::kQ0 + s * L::kTile, 16u, 1024u);
+            const uint64_t kdesc = sw128_desc(sm + L::kK0 + r * L::kTile, 16u, 1024u);
+            const uint32_t tS = tmem + 128u * s;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
+                        kk > 0 ? 1u : 0u);
+            tc_commit(bar_at(bar0, BS_K_EMPTY + r));         // the K slot refills once this S is formed
+            if (cu.last()) tc_commit(bar_at(bar0, BS_Q_EMPTY + s));  // and Q_s after the task's last S
+            tc_commit(bar_at(bar0, BS_S_FULL + s));
+            return true;
+        };
+        auto issue_pv = [&](const BsCursor& cu, int s, int& pq, int& dn) -> bool {
+            if (!mbar_wait(bar_at(bar0, BS_P_FULL + s), pq & 1, ctl, kStatusMma)) return false;
+            ++pq;
+            const int r = vq % L::VS, n = vq / L::VS;
+            if (!mbar_wait(bar_at(bar0, BS_V_FULL + r), n & 1, ctl, kStatusMma)) return false;
+            if (cu.first() && dn >= 1 && !mbar_wait(bar_at(bar0, BS_O_FREE + s), (dn - 1) & 1, ctl, kStatusMma))
+                return false;
+            ++vq;
+            tc_fence_after();
+            const uint64_t vdesc = sw128_desc(sm + L::kV0 + r * L::kTile, kSubTileBytes, 1024u);
+            const uint32_t tS = tmem + 128u * s, tO = tmem + 256u + static_cast<uint32_t>(s * D);
+            // 16 keys per step: 2048 bytes of V, 8 TMEM columns of P
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, (!cu.first() || kk > 0) ? 1u : 0u);
+            tc_commit(bar_at(bar0, BS_V_EMPTY + r));
+            if (cu.last()) {
+                tc_commit(bar_at(bar0, BS_O_FULL + s));
+                ++dn;
+            }
+            return true;
+        };
+        // c0 is the stream whose turn it is (s): its first turn forms S only, each later turn
+        // accumulates P V of its last S and forms its next S
+        bool ok = true, go0 = false, go1 = false;
+        int s = 0;
+        while (ok && (c0.valid() || c1.valid())) {
+            if (c0.valid()) {
+                if (go0) {
+                    ok = issue_pv(c0, s, pq0, dn0);
+                    c0.next(p);
+                }
+                go0 = true;
+                if (ok && c0.valid()) ok = issue_s(c0, s, qn0);
+            }
+            bs_swap(c0, c1);
+            bs_swap(qn0, qn1);
+            bs_swap(pq0, pq1);
+            bs_swap(dn0, dn1);
+            bs_swap(go0, go1);
+            s ^= 1;
         }
         tc_commit(bar_at(bar0, BS_DRAIN));
         const uint64_t t0 = global_timer_ns();

@@ -195,7 +195,8 @@ Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas
 MaskSchedule build_mask_schedule(const int* row_ptr, int nrows, long long bh, int num_ctas) {
     MaskSchedule sc;
     const long long n = static_cast<long long>(nrows) * bh;
-    sc.ctas = static_cast<int>(std::max<long long>(1, std::min<long long>(num_ctas, n)));
+    sc.ctas = static_cast<int>(std::max<long long>(1, std::min<long long>(num_ctas, (n + 1) / 2)));
+    const int nbins = 2 * sc.ctas;  // two task streams per CTA
     // rows of tiles by cost, heaviest first; every batch-head of a row costs the same
     std::vector<int> rows(nrows);
     std::iota(rows.begin(), rows.end(), 0);
@@ -203,8 +204,8 @@ MaskSchedule build_mask_schedule(const int* row_ptr, int nrows, long long bh, in
     std::stable_sort(rows.begin(), rows.end(), [&](int a, int b) { return cost(a) > cost(b); });
     using Load = std::pair<double, int>;
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-    for (int c = 0; c < sc.ctas; ++c) heap.push({0.0, c});
-    std::vector<std::vector<int32_t>> bins(sc.ctas);
+    for (int c = 0; c < nbins; ++c) heap.push({0.0, c});
+    std::vector<std::vector<int32_t>> bins(nbins);
     for (int i : rows)
         for (long long x = 0; x < bh; ++x) {
             Load top = heap.top();

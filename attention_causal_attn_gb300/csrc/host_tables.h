@@ -67,13 +67,14 @@ long long schedule_units(int B, int Hq, int Hkv, int S);
 // Static schedule of the persistent block-sparse forward.  A task is one query
 // tile i of one batch-head x, encoded i * bh + x.  Its cost is the number of
 // key tiles the mask lists for row i plus a fixed cost per task (the Q load
-// and rotation, the merge and the output stores).  Heaviest tasks go first
-// into the least loaded CTA; each CTA runs its tasks in that order, so CTAs
-// that run at the same time work on the same row of tiles.
+// and rotation and the output stores).  Each CTA runs two task streams; the
+// heaviest tasks go first into the least loaded stream, and each stream runs
+// its tasks in that order, so streams that run at the same time work on the
+// same row of tiles.
 constexpr double kMaskTileFixedCost = 1.0;
 struct MaskSchedule {
-    std::vector<int32_t> tasks;    // per-CTA lists, concatenated
-    std::vector<int32_t> offsets;  // ctas + 1 prefix offsets into tasks
+    std::vector<int32_t> tasks;    // per-stream lists, concatenated: stream s of CTA c is list 2c + s
+    std::vector<int32_t> offsets;  // 2 ctas + 1 prefix offsets into tasks
     int ctas = 0;
 };
 MaskSchedule build_mask_schedule(const int* row_ptr, int nrows, long long bh, int num_ctas);

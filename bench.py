@@ -344,6 +344,11 @@ def load_traffic(workload, kernel="attn_fwd_kernel"):
     return None
 
 
+def same_shape(args):
+    """True when the run keeps the workload's own shape (no batch or length override)."""
+    return args.batch is None and args.seq is None
+
+
 def kernel_source_sha():
     import hashlib
     h = hashlib.sha256()
@@ -583,7 +588,8 @@ def run_blocksparse(args, w, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": cfg,
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": float(peaks["bf16_tflops"]),
-                     "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4),
+                     "traffic": load_traffic(args.workload, "bs_fwd_kernel") if same_shape(args) else None,
                      "kernel": "bs_fwd_kernel",
                      "algorithmic": "4*D FLOPs per visible (query, key) pair of the mask, median step time"},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
@@ -641,7 +647,8 @@ def run_local(args, w, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": float(peaks["bf16_tflops"]),
-                     "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4),
+                     "traffic": load_traffic(args.workload, "bs_fwd_kernel") if same_shape(args) else None,
                      "kernel": "bs_fwd_kernel (EXT)",
                      "algorithmic": "4*D FLOPs per visible (query, key) pair, median step time"},
         "gpu_launches": args.steps, "clocks": clocks.summary(),

@@ -17,7 +17,7 @@ import numpy as np
 from ._build import INCLUDE, LIB, build
 
 __all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse",
-           "attn_fwd_local", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+           "attn_fwd_local", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_mask_schedule", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -69,6 +69,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_local.argtypes = [vp] * 5 + [i] * 6 + [d, i, i, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
+        lib.attn_mask_schedule.restype = i
+        lib.attn_mask_schedule.argtypes = [vp, i, ctypes.c_longlong, i, vp, vp, vp]
         lib.attn_check.restype = i
         lib.attn_check.argtypes = [vp]
         lib.attn_error_string.restype = ctypes.c_char_p
@@ -349,6 +351,25 @@ def attn_fwd_host(q, k, v, o=None, lse=None, *, causal: bool = True, rope_base=N
     if rc != 0:
         raise AttnError(rc, "attn_fwd_host")
     return o, lse
+
+
+def attn_mask_schedule(row_ptr, bh: int, num_ctas: int):
+    """The block-sparse forward's task schedule for a CSR mask: (tasks, offsets), int32; stream s of
+    CTA c runs tasks[offsets[2c+s]:offsets[2c+s+1]], task t = query tile * bh + batch-head."""
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    nrows = len(rp) - 1
+    ctas = ctypes.c_int(0)
+    lib = load_library()
+    rc = lib.attn_mask_schedule(rp.ctypes.data, nrows, int(bh), int(num_ctas), None, None, ctypes.byref(ctas))
+    if rc != 0:
+        raise AttnError(rc, "attn_mask_schedule")
+    tasks = np.zeros(max(nrows * int(bh), 1), dtype=np.int32)
+    offsets = np.zeros(2 * ctas.value + 1, dtype=np.int32)
+    rc = lib.attn_mask_schedule(rp.ctypes.data, nrows, int(bh), int(num_ctas), tasks.ctypes.data, offsets.ctypes.data,
+                                None)
+    if rc != 0:
+        raise AttnError(rc, "attn_mask_schedule")
+    return tasks[: nrows * int(bh)], offsets
 
 
 def attn_build_tables(S: int, D: int, rope_base: float, window_k=None, pos_offset: int = 0):

@@ -1134,6 +1134,20 @@ extern "C" int attn_bwd_blocksparse(const void* q, const void* k, const void* v,
     return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, rope_base, row_ptr, col_idx, stream);
 }
 
+extern "C" int attn_mask_schedule(const int* row_ptr, int nrows, long long bh, int num_ctas, int* tasks_out,
+                                  int* offsets_out, int* ctas_out) {
+    if (row_ptr == nullptr) return ATTN_ERR_NULL;
+    if (nrows < 1 || bh < 1 || num_ctas < 1 || static_cast<long long>(nrows) * bh > INT_MAX) return ATTN_ERR_SHAPE;
+    if (row_ptr[0] != 0) return ATTN_ERR_SHAPE;
+    for (int r = 0; r < nrows; ++r)
+        if (row_ptr[r + 1] < row_ptr[r]) return ATTN_ERR_SHAPE;
+    const attn_host::MaskSchedule sc = attn_host::build_mask_schedule(row_ptr, nrows, bh, num_ctas);
+    if (tasks_out != nullptr) std::copy(sc.tasks.begin(), sc.tasks.end(), tasks_out);
+    if (offsets_out != nullptr) std::copy(sc.offsets.begin(), sc.offsets.end(), offsets_out);
+    if (ctas_out != nullptr) *ctas_out = sc.ctas;
+    return ATTN_OK;
+}
+
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
                                  float* cos_out, float* sin_out, int* win_out) {
     if (S < 1 || S > kMaxS || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;

@@ -280,6 +280,29 @@ int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* 
                    int D, int causal, double rope_base, int window, int alibi, void* stream);
 
 /*
+ * attn_mask_schedule — the static task schedule attn_fwd_blocksparse and
+ * attn_fwd_local launch with, for inspection and tests (host only).
+ * A task is one 128-row query tile i of one (batch, head) x, encoded
+ * i * bh + x; its cost is the number of key tiles row i lists plus one.
+ * Each of `ctas` = min(num_ctas, ceil(nrows * bh / 2)) CTAs runs two task
+ * streams; stream s of CTA c runs tasks_out[offsets_out[2c+s] ..
+ * offsets_out[2c+s+1]).  Heaviest tasks go first into the least loaded
+ * stream ("AttnFuse", sec. 4.3 visits only the listed blocks; the balance is
+ * the prefill's longest-first rule, "Flash Attention: Causal Prefill D=128",
+ * Step 4).
+ *   row_ptr      host int32 [nrows + 1], a CSR block mask's row pointers
+ *                (non-decreasing, row_ptr[0] = 0)
+ *   bh           batch x heads, >= 1;  num_ctas >= 1
+ *   tasks_out    host int32 [nrows * bh], or NULL
+ *   offsets_out  host int32 [2 * ctas + 1], or NULL
+ *   ctas_out     host int32, or NULL: receives ctas
+ * Returns ATTN_ERR_NULL without row_ptr, ATTN_ERR_SHAPE for a bad argument
+ * or more than 2^31 - 1 tasks.  Pure host computation.
+ */
+int attn_mask_schedule(const int* row_ptr, int nrows, long long bh, int num_ctas, int* tasks_out, int* offsets_out,
+                       int* ctas_out);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -51,7 +52,8 @@ struct DevInfo {
     bool probed = false, ok = false;
     int sms = 0;
     int* status = nullptr;
-    unsigned configured = 0;  // kernel variants whose smem attribute was set (bit per variant)
+    std::atomic<unsigned> configured{0};  // kernel variants whose smem attribute was set (bit per variant);
+                                          // set by launches, which run outside the mutex
 };
 
 std::mutex g_mu;
@@ -206,10 +208,10 @@ int launch(const FwdParams& prm, int grid, cudaStream_t stream, DevInfo& di) {
     using Layout = attn::SmemLayout<D, WINDOW>;
     constexpr int smem = static_cast<int>(Layout::kAlloc) > 120 * 1024 ? static_cast<int>(Layout::kAlloc) : 120 * 1024;
     cudaError_t e;
-    if (!(di.configured & bit)) {
+    if (!(di.configured.load(std::memory_order_acquire) & bit)) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
             return cuda_fail("cudaFuncSetAttribute(max dynamic smem)", e);
-        di.configured |= bit;
+        di.configured.fetch_or(bit, std::memory_order_release);
     }
     kern<<<grid, attn::kNumThreads, smem, stream>>>(prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("kernel launch", e);
@@ -778,7 +780,7 @@ extern "C" int attn_decode(const void* q, const void* k, const void* v, void* o,
 // Backward ("AttnFuse", sec. 4.4 Backward Pass: row reduction, dK/dV, dQ).
 namespace {
 DecodeScratch g_bwd[kMaxDevices];  // Dlt rows, [B][Hq][S] floats
-unsigned g_bwd_configured[kMaxDevices];
+std::atomic<unsigned> g_bwd_configured[kMaxDevices];  // as DevInfo::configured, for the backward and block-sparse kernels
 
 template <int D, bool CAUSAL, bool ROPE>
 int launch_bwd(const attn::BwdParams& bp, int dev, int ntiles, cudaStream_t st) {
@@ -789,11 +791,11 @@ int launch_bwd(const attn::BwdParams& bp, int dev, int ntiles, cudaStream_t st) 
     auto kv = attn::bwd_dkdv_kernel<D, CAUSAL, ROPE>;
     auto kq = attn::bwd_dq_kernel<D, CAUSAL, ROPE>;
     cudaError_t e;
-    if (!(g_bwd_configured[dev] & bit)) {
+    if (!(g_bwd_configured[dev].load(std::memory_order_acquire) & bit)) {
         if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
             return cuda_fail("cudaFuncSetAttribute(backward)", e);
-        g_bwd_configured[dev] |= bit;
+        g_bwd_configured[dev].fetch_or(bit, std::memory_order_release);
     }
     const int B = bp.f.B, Hq = bp.f.Hq, Hkv = bp.f.Hkv;
     kv<<<static_cast<unsigned>(static_cast<long long>(B) * Hkv * ntiles), attn::kBwdThreads, smem, st>>>(bp);
@@ -1005,10 +1007,10 @@ int launch_bs(const attn::BsParams& bp, int dev, int ctas, cudaStream_t st) {
     constexpr unsigned bit = 1u << (8 + 8 * EXT + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0) + (ROPE ? 4 : 0));
     auto kern = attn::bs_fwd_kernel<D, CAUSAL, ROPE, EXT>;
     cudaError_t e;
-    if (!(g_bwd_configured[dev] & bit)) {
+    if (!(g_bwd_configured[dev].load(std::memory_order_acquire) & bit)) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
             return cuda_fail("cudaFuncSetAttribute(block-sparse)", e);
-        g_bwd_configured[dev] |= bit;
+        g_bwd_configured[dev].fetch_or(bit, std::memory_order_release);
     }
     kern<<<static_cast<unsigned>(ctas), attn::kBsThreads, smem, st>>>(bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("block-sparse kernel launch", e);

@@ -214,6 +214,12 @@ MaskSchedule build_mask_schedule(const int* row_ptr, int nrows, long long bh, in
             top.first += cost(i);
             heap.push(top);
         }
+    // each stream runs its tasks by (batch-head, descending query tile): all streams sweep the
+    // batch-heads in the same order, so the streams running at one time share K/V tiles in L2
+    for (auto& bin : bins)
+        std::stable_sort(bin.begin(), bin.end(), [&](int32_t a, int32_t b) {
+            return std::make_pair(a % bh, -(a / bh)) < std::make_pair(b % bh, -(b / bh));
+        });
     sc.offsets.push_back(0);
     for (auto& bin : bins) {
         sc.tasks.insert(sc.tasks.end(), bin.begin(), bin.end());

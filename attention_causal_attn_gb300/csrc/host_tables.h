@@ -68,9 +68,9 @@ long long schedule_units(int B, int Hq, int Hkv, int S);
 // tile i of one batch-head x, encoded i * bh + x.  Its cost is the number of
 // key tiles the mask lists for row i plus a fixed cost per task (the Q load
 // and rotation and the output stores).  Each CTA runs two task streams; the
-// heaviest tasks go first into the least loaded stream, and each stream runs
-// its tasks in that order, so streams that run at the same time work on the
-// same row of tiles.
+// heaviest tasks go first into the least loaded stream.  Each stream then runs
+// its tasks by (batch-head, descending query tile), so that all streams sweep
+// the batch-heads in the same order and share K/V tiles in L2.
 constexpr double kMaskTileFixedCost = 1.0;
 struct MaskSchedule {
     std::vector<int32_t> tasks;    // per-stream lists, concatenated: stream s of CTA c is list 2c + s

@@ -289,7 +289,8 @@ int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* 
  * offsets_out[2c+s+1]).  Heaviest tasks go first into the least loaded
  * stream ("AttnFuse", sec. 4.3 visits only the listed blocks; the balance is
  * the prefill's longest-first rule, "Flash Attention: Causal Prefill D=128",
- * Step 4).
+ * Step 4); each stream's list is then ordered by (batch-head, descending
+ * query tile).
  *   row_ptr      host int32 [nrows + 1], a CSR block mask's row pointers
  *                (non-decreasing, row_ptr[0] = 0)
  *   bh           batch x heads, >= 1;  num_ctas >= 1

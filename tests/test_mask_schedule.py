@@ -1,8 +1,8 @@
 """The block-sparse forward's static task schedule, through the C ABI (host logic, no GPU).
 
 Every (query tile, batch-head) task must appear exactly once, each CTA runs two streams, each stream
-runs its tasks heaviest first, and longest-first assignment leaves the streams' loads within one
-task's cost of each other.
+runs its tasks by (batch-head, descending query tile), and longest-first assignment leaves the
+streams' loads within one task's cost of each other.
 """
 import ctypes
 
@@ -33,11 +33,13 @@ def _check_schedule(rp, bh, num_ctas):
     tcost = cost[tasks // bh]
     loads = np.array([tcost[offsets[j]:offsets[j + 1]].sum() for j in range(2 * ctas)])
     # longest-first into the least loaded stream: the last task a stream received went to the lightest
-    # stream, so no stream ends more than one task's cost above the lightest
+    # stream, so no stream ends more than one task's cost above the lightest (run order does not
+    # change a stream's load)
     assert loads.max() - loads.min() <= tcost.max() + 1e-9
     for j in range(2 * ctas):
-        seg = tcost[offsets[j]:offsets[j + 1]]
-        assert np.all(np.diff(seg) <= 0), "a stream runs its tasks heaviest first"
+        seg = tasks[offsets[j]:offsets[j + 1]].astype(np.int64)
+        key = (seg % bh) * (nrows + 1) + (nrows - seg // bh)  # (batch-head, descending query tile)
+        assert np.all(np.diff(key) > 0), "a stream runs its tasks by batch-head, then descending query tile"
     return tasks, offsets, loads
 
 

@@ -241,8 +241,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *            ascending, in [0, ceil(S/128)); with causal, at most the row.
  *   q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base   as attn_fwd (no
  *            window).  A query row that sees no key gets O = 0, LSE = -inf.
- * The library keeps a device copy of each distinct mask until
- * attn_release_cache().  Asynchronous on `stream`.
+ * The library keeps a device copy of each distinct mask, and the task
+ * schedule of each (mask, B * Hq) (see attn_mask_schedule), until
+ * attn_release_cache(); the first call with a new mask or shape uploads them
+ * synchronously.  Asynchronous on `stream` after that.
  * Errors: as attn_fwd; ATTN_ERR_SHAPE for a malformed mask.
  */
 int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -104,10 +105,13 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    # where the raw samples go: $ATTN_CLOCK_LOG_DIR if set (to keep them), else a temporary folder
+    LOG_DIR = os.environ.get("ATTN_CLOCK_LOG_DIR") or os.path.join(tempfile.gettempdir(), "attn_bench_clocks")
+
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        self.path = os.path.join(self.LOG_DIR, f"clocks_gpu{index}.csv")
 
     def __enter__(self):
         try:

@@ -17,13 +17,13 @@ import numpy as np
 from ._build import INCLUDE, LIB, build
 
 __all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse",
-           "attn_fwd_local", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_mask_schedule", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+           "attn_fwd_local", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_mask_schedule", "attn_fwd_schedule", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
     "ATTN_OK": 0, "ATTN_ERR_NULL": -1, "ATTN_ERR_SHAPE": -2, "ATTN_ERR_ALIGN": -3,
     "ATTN_ERR_UNSUPPORTED": -4, "ATTN_ERR_CUDA": -5, "ATTN_ERR_TIMEOUT": -6, "ATTN_ERR_OOM": -7,
-    "ATTN_ERR_NO_DEVICE": -8, "ATTN_ERR_SCRATCH": -9,
+    "ATTN_ERR_NO_DEVICE": -8, "ATTN_ERR_SCRATCH": -9, "ATTN_ERR_NONFINITE": -10,
 }
 
 _lock = threading.Lock()
@@ -49,6 +49,8 @@ def load_library(path: str | None = None):
         vp, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
         lib.attn_fwd.restype = i
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
+        lib.attn_selftest_wait_timeout.restype = i
+        lib.attn_selftest_wait_timeout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, ctypes.c_ulonglong, vp]
         lib.attn_fwd_noalloc.restype = i
         lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, d, d, vp]
         lib.attn_fwd_host.restype = i
@@ -71,6 +73,8 @@ def load_library(path: str | None = None):
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_mask_schedule.restype = i
         lib.attn_mask_schedule.argtypes = [vp, i, ctypes.c_longlong, i, vp, vp, vp]
+        lib.attn_fwd_schedule.restype = i
+        lib.attn_fwd_schedule.argtypes = [i, i, i, i, i, i, i, d, vp, vp, vp]
         lib.attn_check.restype = i
         lib.attn_check.argtypes = [vp]
         lib.attn_error_string.restype = ctypes.c_char_p
@@ -372,6 +376,27 @@ def attn_mask_schedule(row_ptr, bh: int, num_ctas: int):
     return tasks[: nrows * int(bh)], offsets
 
 
+def attn_fwd_schedule(B: int, Hq: int, Hkv: int, S: int, D: int, causal: bool, num_ctas: int,
+                      kv_window_bytes: float = 64 * 2 ** 20):
+    """The forward's tile schedule: (words [units, 2] uint32, offsets [ctas + 1] int32); CTA c runs
+    units offsets[c]:offsets[c+1], word x = qtile0 | qtile1 << 16, y = h0 | h1 << 8 | b << 16."""
+    lib = load_library()
+    ctas = ctypes.c_int(0)
+    args = (int(B), int(Hq), int(Hkv), int(S), int(D), int(bool(causal)), int(num_ctas), float(kv_window_bytes))
+    rc = lib.attn_fwd_schedule(*args, None, None, ctypes.byref(ctas))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_schedule")
+    offsets = np.zeros(ctas.value + 1, dtype=np.int32)
+    rc = lib.attn_fwd_schedule(*args, None, offsets.ctypes.data, None)
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_schedule")
+    words = np.zeros((max(int(offsets[-1]), 1), 2), dtype=np.uint32)
+    rc = lib.attn_fwd_schedule(*args, words.ctypes.data, None, None)
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_schedule")
+    return words[: int(offsets[-1])], offsets
+
+
 def attn_build_tables(S: int, D: int, rope_base: float, window_k=None, pos_offset: int = 0):
     """Host RoPE tables cos/sin [S, D/2] (float32) and window widths W_r [D/2] (int32)."""
     cos = np.zeros((S, D // 2), dtype=np.float32)
@@ -385,7 +410,7 @@ def attn_build_tables(S: int, D: int, rope_base: float, window_k=None, pos_offse
 
 
 def attn_check(stream=None, device=None) -> None:
-    """Synchronise the stream and raise if a kernel reported a bounded-wait timeout."""
+    """Synchronise the stream and raise if a kernel reported a bounded-wait timeout or a non-finite forward row."""
     import torch
     dev = device if device is not None else torch.cuda.current_device()
     with torch.cuda.device(dev):

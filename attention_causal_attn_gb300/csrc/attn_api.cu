@@ -44,7 +44,7 @@ struct WinEntry {
     short2* table;
 };
 struct SchedEntry {
-    int dev, B, Hq, Hkv, S, causal, ctas;
+    int dev, B, Hq, Hkv, S, D, causal, ctas;
     uint2* tasks;
     int* offsets;
 };
@@ -69,6 +69,17 @@ bool verbose() {
 int cuda_fail(const char* what, cudaError_t e, int code = ATTN_ERR_CUDA) {
     if (verbose()) std::fprintf(stderr, "attn: %s failed: %s (%d)\n", what, cudaGetErrorString(e), static_cast<int>(e));
     return code;
+}
+// K/V bytes per scheduling window of the forward's tile schedule: the built-in
+// default, or ATTN_SCHEDULE_WINDOW_MB from the environment (read once; 0 turns
+// the windows off).
+double schedule_window_bytes() {
+    static const double b = [] {
+        const char* e = std::getenv("ATTN_SCHEDULE_WINDOW_MB");
+        if (e == nullptr || e[0] == '\0') return attn_host::kScheduleWindowBytes;
+        return std::max(0.0, std::atof(e)) * 1024.0 * 1024.0;
+    }();
+    return b;
 }
 std::vector<RopeEntry> g_rope;
 std::vector<SchedEntry> g_sched;
@@ -171,13 +182,14 @@ int get_wtab(int dev, int S, int D, double base, double k, short2** out) {
     return ATTN_OK;
 }
 
-int get_schedule(int dev, int B, int Hq, int Hkv, int S, int causal, int sms, const SchedEntry** out) {
+int get_schedule(int dev, int B, int Hq, int Hkv, int S, int D, int causal, int sms, const SchedEntry** out) {
     for (auto& e : g_sched)
-        if (e.dev == dev && e.B == B && e.Hq == Hq && e.Hkv == Hkv && e.S == S && e.causal == causal) {
+        if (e.dev == dev && e.B == B && e.Hq == Hq && e.Hkv == Hkv && e.S == S && e.D == D && e.causal == causal) {
             *out = &e;
             return ATTN_OK;
         }
-    const attn_host::Schedule sc = attn_host::build_schedule(B, Hq, Hkv, S, causal != 0, sms);
+    const attn_host::Schedule sc =
+        attn_host::build_schedule(B, Hq, Hkv, S, D, causal != 0, sms, schedule_window_bytes());
     uint2* tasks = nullptr;
     int* offs = nullptr;
     cudaError_t e;
@@ -195,7 +207,7 @@ int get_schedule(int dev, int B, int Hq, int Hkv, int S, int causal, int sms, co
         cudaFree(offs);
         return cuda_fail("cudaMemcpy(schedule)", e);
     }
-    g_sched.push_back({dev, B, Hq, Hkv, S, causal, sc.ctas, tasks, offs});
+    g_sched.push_back({dev, B, Hq, Hkv, S, D, causal, sc.ctas, tasks, offs});
     *out = &g_sched.back();
     return ATTN_OK;
 }
@@ -242,8 +254,11 @@ int check_args(const void* q, const void* k, const void* v, const void* o, int B
 
 namespace {
 // The forward; qk_f16: Q and K hold fp16 values (already rotated) rather than bf16.
+// test_no_loads: the bounded-wait test mode (the producer issues nothing), with
+// wait_limit_ns per wait.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S, int D,
-             int causal, double rope_base, double window_k, void* stream, bool qk_f16) {
+             int causal, double rope_base, double window_k, void* stream, bool qk_f16, bool test_no_loads = false,
+             unsigned long long wait_limit_ns = kWaitLimitNs) {
     int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, window_k);
     if (arc == ATTN_OK && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
                            (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
@@ -267,7 +282,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
         if (rope && (rc = get_rope(dev, S, D, rope_base, &rope_tab)) != ATTN_OK) return rc;
         if (window && (rc = get_wtab(dev, S, D, rope_base, window_k, &wtab)) != ATTN_OK) return rc;
         const SchedEntry* se = nullptr;
-        if ((rc = get_schedule(dev, B, Hq, Hkv, S, causal, g_dev[dev].sms, &se)) != ATTN_OK) return rc;
+        if ((rc = get_schedule(dev, B, Hq, Hkv, S, D, causal, g_dev[dev].sms, &se)) != ATTN_OK) return rc;
         sched = *se;
         prm.status = g_dev[dev].status;
     }
@@ -289,8 +304,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     prm.Hkv = Hkv;
     prm.S = S;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    prm.wait_limit_ns = kWaitLimitNs;
+    prm.wait_limit_ns = wait_limit_ns;
     prm.qk_f16 = qk_f16 ? 1 : 0;
+    prm.test_no_loads = test_no_loads ? 1 : 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     DevInfo& di = g_dev[dev];
@@ -309,6 +325,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int S, int D, int causal, double rope_base, double window_k, void* stream) {
     return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base, window_k, stream, false);
+}
+
+extern "C" int attn_selftest_wait_timeout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                          int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                                          unsigned long long wait_limit_ns, void* stream) {
+    if (wait_limit_ns < 100000ull || wait_limit_ns > kWaitLimitNs) return ATTN_ERR_UNSUPPORTED;
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base, 0.0, stream, false, true, wait_limit_ns);
 }
 
 extern "C" int attn_fwd_rotated(const void* q_rot, const void* k_rot, const void* v, void* o, float* lse, int B,
@@ -393,6 +416,11 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 struct NoAllocDev {
     bool ready = false;
     unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    // Recorded on the upload stream after the last upload; a launch on another
+    // stream waits for it until the upload has been seen complete.
+    cudaEvent_t uploaded = nullptr;
+    cudaStream_t upload_stream = nullptr;
+    bool upload_done = true;
     // what the scratch currently holds (re-uploaded only when the request differs)
     bool have = false;
     int S = 0, D = 0, B = 0, Hq = 0, Hkv = 0, causal = 0, rope = 0, ctas = 0;
@@ -426,13 +454,21 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     NoAllocDev& na = g_noalloc[dev];
     cudaError_t e;
     if (!na.ready) {
-        // once per device, with that device current
+        // once per device, with that device current (an event allocates no device memory)
         if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&na.scratch), g_noalloc_scratch)) != cudaSuccess)
             return cuda_fail("cudaGetSymbolAddress(no-alloc scratch)", e);
+        if ((e = cudaEventCreateWithFlags(&na.uploaded, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail("cudaEventCreateWithFlags(no-alloc upload)", e);
         na.ready = true;
     }
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(st, &capture)) != cudaSuccess) return cuda_fail("cudaStreamIsCapturing", e);
+    const bool capturing = capture != cudaStreamCaptureStatusNone;
     const bool same = na.have && na.S == S && na.D == D && na.B == B && na.Hq == Hq && na.Hkv == Hkv &&
                       na.causal == causal && na.rope == static_cast<int>(rope) && (!rope || na.base == rope_base);
+    // An upload enqueues copies from host vectors that end with this call: not
+    // while the stream is being captured.
+    if (!same && capturing) return ATTN_ERR_UNSUPPORTED;
     if (!same) {
         // size check first, from the shape alone
         const size_t rope_bytes = rope ? attn_host::rope_factor_table_floats(S, D) * sizeof(float) : 0;
@@ -444,7 +480,8 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
         if (units > static_cast<long long>(kNoAllocScratchBytes) ||
             off_offsets + static_cast<size_t>(ctas + 1) * sizeof(int32_t) > kNoAllocScratchBytes)
             return ATTN_ERR_SCRATCH;
-        const attn_host::Schedule sc = attn_host::build_schedule(B, Hq, Hkv, S, causal != 0, g_dev[dev].sms);
+        const attn_host::Schedule sc =
+            attn_host::build_schedule(B, Hq, Hkv, S, D, causal != 0, g_dev[dev].sms, schedule_window_bytes());
         na.have = false;  // contents are in flux until the copies below are enqueued
         // Pageable host sources: each copy returns once its source has been staged,
         // so the host vectors may go out of scope; the copies are ordered on `st`.
@@ -458,10 +495,27 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
             (e = cudaMemcpyAsync(na.scratch + off_offsets, sc.offsets.data(), sc.offsets.size() * sizeof(int32_t),
                                  cudaMemcpyHostToDevice, st)) != cudaSuccess)
             return cuda_fail("cudaMemcpyAsync(no-alloc schedule)", e);
+        if ((e = cudaEventRecord(na.uploaded, st)) != cudaSuccess) return cuda_fail("cudaEventRecord(no-alloc upload)", e);
+        na.upload_stream = st;
+        na.upload_done = false;
         na.have = true;
         na.S = S, na.D = D, na.B = B, na.Hq = Hq, na.Hkv = Hkv, na.causal = causal;
         na.rope = static_cast<int>(rope), na.base = rope_base, na.ctas = sc.ctas;
         na.off_tasks = off_tasks, na.off_offsets = off_offsets;
+    }
+
+    if (!na.upload_done && st != na.upload_stream) {
+        // The tables were enqueued on another stream: this launch must not start before they land.
+        if (capturing) return ATTN_ERR_UNSUPPORTED;
+        e = cudaEventQuery(na.uploaded);
+        if (e == cudaSuccess) {
+            na.upload_done = true;
+        } else if (e == cudaErrorNotReady) {
+            if ((e = cudaStreamWaitEvent(st, na.uploaded, 0)) != cudaSuccess)
+                return cuda_fail("cudaStreamWaitEvent(no-alloc upload)", e);
+        } else {
+            return cuda_fail("cudaEventQuery(no-alloc upload)", e);
+        }
     }
 
     FwdParams prm;
@@ -480,6 +534,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     prm.S = S;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     prm.qk_f16 = 0;
+    prm.test_no_loads = 0;
     prm.wait_limit_ns = kWaitLimitNs;
     DevInfo& di = g_dev[dev];
     const int grid = na.ctas;
@@ -1150,6 +1205,21 @@ extern "C" int attn_mask_schedule(const int* row_ptr, int nrows, long long bh, i
     return ATTN_OK;
 }
 
+extern "C" int attn_fwd_schedule(int B, int Hq, int Hkv, int S, int D, int causal, int num_ctas,
+                                 double kv_window_bytes, unsigned* words_out, int* offsets_out, int* ctas_out) {
+    if (B < 1 || B > 65535 || S < 1 || S > kMaxS || Hq < 1 || Hq > 255 || Hkv < 1 || Hkv > Hq || Hq % Hkv != 0 ||
+        (D != 64 && D != 128) || num_ctas < 1)
+        return ATTN_ERR_SHAPE;
+    if (causal != 0 && causal != 1) return ATTN_ERR_UNSUPPORTED;
+    if (attn_host::schedule_units(B, Hq, Hkv, S) > INT_MAX / 2) return ATTN_ERR_SHAPE;
+    if (std::isnan(kv_window_bytes)) return ATTN_ERR_UNSUPPORTED;
+    const attn_host::Schedule sc = attn_host::build_schedule(B, Hq, Hkv, S, D, causal != 0, num_ctas, kv_window_bytes);
+    if (words_out != nullptr) std::copy(sc.words.begin(), sc.words.end(), words_out);
+    if (offsets_out != nullptr) std::copy(sc.offsets.begin(), sc.offsets.end(), offsets_out);
+    if (ctas_out != nullptr) *ctas_out = sc.ctas;
+    return ATTN_OK;
+}
+
 extern "C" int attn_build_tables(int S, int D, double rope_base, double window_k, long long pos_offset,
                                  float* cos_out, float* sin_out, int* win_out) {
     if (S < 1 || S > kMaxS || (D != 64 && D != 128)) return ATTN_ERR_SHAPE;
@@ -1180,7 +1250,7 @@ extern "C" int attn_check(void* stream) {
     if (v != 0) {
         const int zero = 0;
         cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int));
-        return ATTN_ERR_TIMEOUT;
+        return (v & attn::kStatusTimeoutMask) != 0 ? ATTN_ERR_TIMEOUT : ATTN_ERR_NONFINITE;
     }
     return ATTN_OK;
 }
@@ -1196,6 +1266,8 @@ extern "C" const char* attn_error_string(int status) {
         case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a bounded in-kernel wait ran out";
         case ATTN_ERR_OOM: return "ATTN_ERR_OOM: table allocation failed";
         case ATTN_ERR_NO_DEVICE: return "ATTN_ERR_NO_DEVICE: no sm_103 device is current";
+        case ATTN_ERR_NONFINITE:
+            return "ATTN_ERR_NONFINITE: a result row came out non-finite (an input, or a rotated fp16 operand, out of range)";
         case ATTN_ERR_SCRATCH:
             return "ATTN_ERR_SCRATCH: the request needs more than the 16 MiB static scratch of attn_fwd_noalloc";
         default: return "unknown attn status";

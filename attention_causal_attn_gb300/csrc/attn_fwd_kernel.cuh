@@ -17,7 +17,8 @@
 //   warp 12     TMA producer: Q tiles, then K/V tiles from the diagonal down to
 //               tile 0 ("Flash Attention: Causal Prefill D=128", reverse
 //               traversal isolates the causal mask to the first tile)
-//   warp 13     tcgen05 issuer (one thread) and TMEM owner
+//   warp 13     tcgen05 issuer (the converged warp; one elected thread issues)
+//               and TMEM owner
 //   warps 14-15 idle (they complete the fourth warpgroup)
 //
 // TMEM (512 columns x 128 lanes x 32 bit): S0 [0,128), S1 [128,256), O0 [256,
@@ -72,6 +73,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // status word bits (OR-ed by the CTA whose wait ran out)
 constexpr int kStatusProducer = 1, kStatusRope = 2, kStatusMma = 4, kStatusSoftmax = 8, kStatusDrain = 16;
+constexpr int kStatusTimeoutMask = 255;
+// OR-ed by a row whose LSE came out non-finite: a score overflowed (with RoPE,
+// a rotated Q or K value past the fp16 range) or an input was not finite
+constexpr int kStatusNonFinite = 256;
 
 struct FwdParams {
     CUtensorMap tm_q;  // [B][S][Hq][D] bf16, box {64, 1, 128, 1}, 128B swizzle
@@ -92,6 +97,8 @@ struct FwdParams {
     int qk_f16;         // without in-kernel RoPE: Q and K hold fp16 (already rotated) rather than bf16
     const short2* wtab; // windowed variant, per tile distance: (first pair kept at the tile's smallest distance,
                         // first pair kept at its largest), see window_tile
+    int test_no_loads;  // test mode for the bounded waits: the producer issues nothing, so every
+                        // consumer's first wait runs out after wait_limit_ns (0 in every real launch)
 };
 
 // barrier slots
@@ -197,13 +204,12 @@ __device__ __forceinline__ WinTile window_tile(const FwdParams& p, const Unit& u
 }
 
 // ------------------------------------------------------------------ producer
+// Issues the CTA's Q, K and V loads; kit, vit, qit count the loads armed so far.
 template <int D, bool WINDOW>
-__device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, int t_begin, int t_end,
-                              const WaitCtl& ctl) {
+__device__ void producer_issue(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, int t_begin, int t_end,
+                               const WaitCtl& ctl, int& kit, int& vit, int (&qit)[2]) {
     constexpr int kKStages = k_stages<WINDOW>();
     using L = SmemLayout<D, WINDOW>;
-    int kit = 0, vit = 0;
-    int qit[2] = {0, 0};
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, causal);
 #pragma unroll
@@ -249,6 +255,20 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
             ++vit;
         }
     }
+}
+
+template <int D, bool WINDOW>
+__device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, int t_begin, int t_end,
+                              const WaitCtl& ctl) {
+    int kit = 0, vit = 0;
+    int qit[2] = {0, 0};
+    if (!p.test_no_loads) producer_issue<D, WINDOW>(p, causal, sm, bar0, t_begin, t_end, ctl, kit, vit, qit);
+    // On the way out, whether the loop ended or a wait gave up: the last load of
+    // every slot has landed before the CTA may exit (the earlier ones were consumed).
+#pragma unroll
+    for (int s = 0; s < 2; ++s) drain_ring(bar_at(bar0, BAR_Q_FULL + s), 1, qit[s], ctl, kStatusDrain);
+    drain_ring(bar_at(bar0, BAR_K_FULL), k_stages<WINDOW>(), kit, ctl, kStatusDrain);
+    drain_ring(bar_at(bar0, BAR_V_FULL), kVStages, vit, ctl, kStatusDrain);
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -459,15 +479,15 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                 const uint32_t tO = tmem + 256u + static_cast<uint32_t>(s * 128);
                 if (do_pv && n + 1 <= u.nhi[s]) {
                     if (!v_ready) {
-                        ok = mbar_wait(bar_at(bar0, BAR_V_FULL + vs), (vit / kVStages) & 1, ctl, kStatusMma);
+                        ok = mbar_wait_warp(bar_at(bar0, BAR_V_FULL + vs), (vit / kVStages) & 1, ctl, kStatusMma);
                         if (!ok) break;
                         v_ready = true;
                     }
-                    ok = mbar_wait(bar_at(bar0, BAR_P_FULL + s), pit[s] & 1, ctl, kStatusMma);
+                    ok = mbar_wait_warp(bar_at(bar0, BAR_P_FULL + s), pit[s] & 1, ctl, kStatusMma);
                     if (!ok) break;
                     ++pit[s];
                     if (first_pv[s]) {
-                        ok = mbar_wait(bar_at(bar0, BAR_O_FREE + s), (oit[s] & 1) ^ 1, ctl, kStatusMma);
+                        ok = mbar_wait_warp(bar_at(bar0, BAR_O_FREE + s), (oit[s] & 1) ^ 1, ctl, kStatusMma);
                         if (!ok) break;
                     }
                     tc_fence_after();
@@ -486,13 +506,13 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                 }
                 if (do_s && n <= u.nhi[s]) {
                     if (!k_ready) {
-                        ok = mbar_wait(bar_at(bar0, kbar_ready + ks), (kit / kKStages) & 1, ctl, kStatusMma);
+                        ok = mbar_wait_warp(bar_at(bar0, kbar_ready + ks), (kit / kKStages) & 1, ctl, kStatusMma);
                         if (!ok) break;
                         k_ready = true;
                         tc_fence_after();
                     }
                     if (n == u.nhi[s]) {
-                        ok = mbar_wait(bar_at(bar0, qbar_ready + s), qit[s] & 1, ctl, kStatusMma);
+                        ok = mbar_wait_warp(bar_at(bar0, qbar_ready + s), qit[s] & 1, ctl, kStatusMma);
                         if (!ok) break;
                         tc_fence_after();
                     }
@@ -803,9 +823,10 @@ __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32
         const float inv_l = 1.0f / l;
         const uint64_t il2 = f2_pack(inv_l, inv_l);
         const bool row_ok = row < p.S;
+        const float lse2 = m_used * c + log2f(l);  // every row sees at least one key: finite for finite scores
+        if (row_ok && !isfinite(lse2)) atomicOr(p.status, kStatusNonFinite);
         if (row_ok && p.lse != nullptr)
-            p.lse[(static_cast<size_t>(u.b) * p.Hq + head) * p.S + row] =
-                (m_used * c + log2f(l)) * 0.69314718055994531f;
+            p.lse[(static_cast<size_t>(u.b) * p.Hq + head) * p.S + row] = lse2 * 0.69314718055994531f;
         if constexpr (epi_tma<WINDOW>()) {
             // Each warp stages its 32 rows one 64-channel block at a time (128-byte
             // swizzle: chunk c of row r at chunk c ^ (r & 7)) and stores the block
@@ -951,8 +972,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_c
             if (lane == 0) producer_role<D, WINDOW>(p, CAUSAL, sm, bar0, t_begin, t_end, ctl);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            if (lane == 0) mma_role<D, ROPE, WINDOW>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);
-            __syncwarp();
+            mma_role<D, ROPE, WINDOW>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);  // the whole warp
         }
     }
 

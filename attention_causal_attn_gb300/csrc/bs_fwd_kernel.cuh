@@ -512,9 +512,15 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                 bs_swap(go0, go1);
                 s ^= 1;
             }
+            // On the way out, whether the lists ended or a wait gave up: the last load of every
+            // slot has landed before the CTA may exit (ql0 belongs to stream s, ql1 to the other).
+            drain_ring(bar_at(bar0, BS_Q_FULL + s), 1, ql0, ctl, kStatusDrain);
+            drain_ring(bar_at(bar0, BS_Q_FULL + (s ^ 1)), 1, ql1, ctl, kStatusDrain);
+            drain_ring(bar_at(bar0, BS_K_FULL), L::KS, kq, ctl, kStatusDrain);
+            drain_ring(bar_at(bar0, BS_V_FULL), L::VS, vq, ctl, kStatusDrain);
         }
         __syncwarp();
-    } else if (warp == kBsWarpMma && lane == 0) {
+    } else if (warp == kBsWarpMma) {  // the whole warp: one elected thread issues
         // ---- MMA issuer.  Per stream s: S_s = Q_s K^T (K-major, fp16 after RoPE), then, once the
         // stream's softmax has handed P back, O_s += P V (P from TMEM, V MN-major) followed at once
         // by the stream's next S, as the prefill issues its stages.  The streams alternate, so the
@@ -528,13 +534,13 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
         int kq = 0, vq = 0, qn0 = 0, qn1 = 0, pq0 = 0, pq1 = 0, dn0 = 0, dn1 = 0;
         auto issue_s = [&](const BsCursor& cu, int s, int& qn) -> bool {
             if (cu.first()) {
-                if (!mbar_wait(bar_at(bar0, BS_Q_FULL + s), qn & 1, ctl, kStatusMma)) return false;
-                if (ROPE && !mbar_wait(bar_at(bar0, BS_Q_ROT + s), qn & 1, ctl, kStatusMma)) return false;
+                if (!mbar_wait_warp(bar_at(bar0, BS_Q_FULL + s), qn & 1, ctl, kStatusMma)) return false;
+                if (ROPE && !mbar_wait_warp(bar_at(bar0, BS_Q_ROT + s), qn & 1, ctl, kStatusMma)) return false;
                 ++qn;
             }
             const int r = kq % L::KS, n = kq / L::KS;
-            if (!mbar_wait(bar_at(bar0, BS_K_FULL + r), n & 1, ctl, kStatusMma)) return false;
-            if (ROPE && !mbar_wait(bar_at(bar0, BS_K_ROT + r), n & 1, ctl, kStatusMma)) return false;
+            if (!mbar_wait_warp(bar_at(bar0, BS_K_FULL + r), n & 1, ctl, kStatusMma)) return false;
+            if (ROPE && !mbar_wait_warp(bar_at(bar0, BS_K_ROT + r), n & 1, ctl, kStatusMma)) return false;
             ++kq;
             tc_fence_after();
             const uint64_t qdesc = sw128_desc(sm + L::kQ0 + s * L::kTile, 16u, 1024u);
@@ -550,11 +556,11 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             return true;
         };
         auto issue_pv = [&](const BsCursor& cu, int s, int& pq, int& dn) -> bool {
-            if (!mbar_wait(bar_at(bar0, BS_P_FULL + s), pq & 1, ctl, kStatusMma)) return false;
+            if (!mbar_wait_warp(bar_at(bar0, BS_P_FULL + s), pq & 1, ctl, kStatusMma)) return false;
             ++pq;
             const int r = vq % L::VS, n = vq / L::VS;
-            if (!mbar_wait(bar_at(bar0, BS_V_FULL + r), n & 1, ctl, kStatusMma)) return false;
-            if (cu.first() && dn >= 1 && !mbar_wait(bar_at(bar0, BS_O_FREE + s), (dn - 1) & 1, ctl, kStatusMma))
+            if (!mbar_wait_warp(bar_at(bar0, BS_V_FULL + r), n & 1, ctl, kStatusMma)) return false;
+            if (cu.first() && dn >= 1 && !mbar_wait_warp(bar_at(bar0, BS_O_FREE + s), (dn - 1) & 1, ctl, kStatusMma))
                 return false;
             ++vq;
             tc_fence_after();

@@ -404,6 +404,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                 tma_load_4d(sm + L::kRes1 + sub * kSubTileBytes, &f.tm_v, rb, sub * 64, g, kv0, b);
             }
         }
+        int armed = 0;  // streamed loads armed so far
         for (int it = 0; it < iters; ++it) {
             const int s = it & 1, n = it >> 1;
             const int h = g * G + it / per_head;
@@ -437,9 +438,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                     tma_load_4d(dq + L::kTile + sub * kSubTileBytes, &p.tm_do, fb, sub * 64, h, q0, b);
                 }
             }
+            ++armed;
             __syncwarp();
         }
-    } else if (warp == kBwdWarpMma && lane == 0) {
+        // on the way out (loop ended or a wait gave up): every load has landed before the CTA may exit
+        if (lane == 0) {
+            mbar_drain(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusDrain);
+            drain_ring(bar_at(bar0, BB_STR_FULL), 2, armed, ctl, kStatusDrain);
+        }
+        __syncwarp();
+    } else if (warp == kBwdWarpMma) {  // the whole warp: one elected thread issues
         // ---- MMA issuer
         // S^T = K Q^T (A = K tile, B = Q tile, both K-major; fp16 after RoPE) and dP^T = V dO^T (bf16)
         const uint32_t kIdescS = umma_idesc_f16(ROPE ? 0u : 1u, 0u, 128, 128);
@@ -450,10 +458,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         const uint32_t tS = tmem, tdP = tmem + 128u, tdV = tmem + 256u, tdK = tmem + 256u + D;
         const uint64_t kdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
         const uint64_t vdesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
-        bool ok = mbar_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
+        bool ok = mbar_wait_warp(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
         for (int it = 0; it < iters && ok; ++it) {
             const int s = it & 1, n = it >> 1;
-            ok = mbar_wait(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
+            ok = mbar_wait_warp(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
             if (!ok) break;
             tc_fence_after();
             const uint32_t qa = sm + L::kStr0 + s * 2 * L::kTile, da = qa + L::kTile;
@@ -464,8 +472,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                 umma_ss(tdP, desc_advance(vdesc, kmajor_units(kk)), desc_advance(ddesc, kmajor_units(kk)), kIdescDP,
                         kk > 0 ? 1u : 0u);
             if (ROPE) {
-                if (it == 0) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
-                if (ok) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
+                if (it == 0) ok = mbar_wait_warp(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
+                if (ok) ok = mbar_wait_warp(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -474,7 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                 umma_ss(tS, desc_advance(kdesc, kmajor_units(kk)), desc_advance(qdesc, kmajor_units(kk)), kIdescS,
                         kk > 0 ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_S_FULL));
-            ok = mbar_wait(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
+            ok = mbar_wait_warp(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
             if (!ok) break;
             tc_fence_after();
             const uint64_t dmn = sw128_desc(da, kSubTileBytes, 1024u), qmn = sw128_desc(qa, kSubTileBytes, 1024u);
@@ -614,6 +622,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                 tma_load_4d(sm + L::kRes0 + sub * kSubTileBytes, &f.tm_q, rb, sub * 64, h, q0, b);
                 tma_load_4d(sm + L::kRes1 + sub * kSubTileBytes, &p.tm_do, rb, sub * 64, h, q0, b);
             }
+            int armed = 0;  // streamed loads armed so far
             for (int it = 0; it < iters; ++it) {
                 const int s = it & 1, n = it >> 1;
                 if (n >= 1 && !mbar_wait(bar_at(bar0, BB_STR_EMPTY + s), (n - 1) & 1, ctl, kStatusProducer)) break;
@@ -625,10 +634,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                     tma_load_4d(ka + sub * kSubTileBytes, &f.tm_k, fb, sub * 64, g, ktile(it) * 128, b);
                     tma_load_4d(ka + L::kTile + sub * kSubTileBytes, &f.tm_v, fb, sub * 64, g, ktile(it) * 128, b);
                 }
+                ++armed;
             }
+            // on the way out (loop ended or a wait gave up): every load has landed before the CTA may exit
+            mbar_drain(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusDrain);
+            drain_ring(bar_at(bar0, BB_STR_FULL), 2, armed, ctl, kStatusDrain);
         }
         __syncwarp();
-    } else if (warp == kBwdWarpMma && lane == 0) {
+    } else if (warp == kBwdWarpMma) {  // the whole warp: one elected thread issues
         // ---- MMA issuer: S = Q K^T, dP = dO V^T (K-major operands), then dQ += dS K (K tile MN-major)
         const uint32_t kIdescS = umma_idesc_f16(ROPE ? 0u : 1u, 0u, 128, 128);
         constexpr uint32_t kIdescDP = umma_idesc_f16(1u, 0u, 128, 128);
@@ -636,10 +649,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         const uint32_t tS = tmem, tdP = tmem + 128u, tdQ = tmem + 256u;
         const uint64_t qdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
         const uint64_t ddesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
-        bool ok = mbar_wait(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
+        bool ok = mbar_wait_warp(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
         for (int it = 0; it < iters && ok; ++it) {
             const int s = it & 1, n = it >> 1;
-            ok = mbar_wait(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
+            ok = mbar_wait_warp(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
             if (!ok) break;
             tc_fence_after();
             const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile, va = ka + L::kTile;
@@ -650,8 +663,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                 umma_ss(tdP, desc_advance(ddesc, kmajor_units(kk)), desc_advance(vdesc, kmajor_units(kk)), kIdescDP,
                         kk > 0 ? 1u : 0u);
             if (ROPE) {
-                if (it == 0) ok = mbar_wait(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
-                if (ok) ok = mbar_wait(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
+                if (it == 0) ok = mbar_wait_warp(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
+                if (ok) ok = mbar_wait_warp(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -660,7 +673,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                 umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
                         kk > 0 ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_S_FULL));
-            ok = mbar_wait(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
+            ok = mbar_wait_warp(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
             if (!ok) break;
             tc_fence_after();
             const uint64_t kmn = sw128_desc(ka, kSubTileBytes, 1024u);

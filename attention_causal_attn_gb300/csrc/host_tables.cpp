@@ -114,11 +114,11 @@ long long schedule_units(int B, int Hq, int Hkv, int S) {
     return static_cast<long long>(B) * Hq * ((nqt + 1) / 2);
 }
 
-Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas) {
+Schedule build_schedule(int B, int Hq, int Hkv, int S, int D, bool causal, int num_ctas, double kv_window_bytes) {
     struct U {
         uint32_t x, y;
         double cost;
-        int b, kvh, h, qt;
+        int kv;  // b * Hkv + KV head: the window key
     };
     const int nqt = (S + kTile - 1) / kTile;
     const int G = Hq / Hkv;
@@ -136,7 +136,7 @@ Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas
                         u.y = static_cast<uint32_t>(h) | (static_cast<uint32_t>(pair ? h + 1 : h) << 8) |
                               (static_cast<uint32_t>(b) << 16);
                         u.cost = tile_cost(qt) * (pair ? 2 : 1) + 4.0;
-                        u.b = b, u.kvh = g, u.h = h, u.qt = qt;
+                        u.kv = b * Hkv + g;
                         units.push_back(u);
                     }
     } else {
@@ -150,17 +150,39 @@ Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas
                     u.x = static_cast<uint32_t>(q0) | ((pair ? static_cast<uint32_t>(q1) : kNoTile) << 16);
                     u.y = static_cast<uint32_t>(h) | (static_cast<uint32_t>(h) << 8) | (static_cast<uint32_t>(b) << 16);
                     u.cost = tile_cost(q0) + (pair ? tile_cost(q1) : 0.0) + 4.0;
-                    u.b = b, u.kvh = h, u.h = h, u.qt = q0;
+                    u.kv = b * Hkv + h;
                     units.push_back(u);
                 }
     }
     Schedule sc;
     const int n = static_cast<int>(units.size());
     sc.ctas = std::max(1, std::min(num_ctas, n));
-    // longest-processing-time-first into the least loaded CTA
+    // KV heads per window: K and V of one KV head take 2 * 2 * S * D bytes (bf16)
+    const double kv_head_bytes = 4.0 * static_cast<double>(S) * static_cast<double>(D);
+    const long long kv_heads = static_cast<long long>(B) * Hkv;
+    // KV heads per window (all of them without a window size).  The last window evens out the loads
+    // that the earlier ones leave, so it takes at least three units per CTA; the heads before it are
+    // split into windows whose sizes differ by at most one head.
+    long long cap = kv_heads;
+    if (kv_window_bytes > 0.0)
+        cap = std::max<long long>(1, std::min<long long>(kv_heads, static_cast<long long>(kv_window_bytes / kv_head_bytes)));
+    const long long units_per_kv = (n + kv_heads - 1) / kv_heads;
+    const long long tail_heads =
+        std::min<long long>(kv_heads, std::max<long long>(cap, (3LL * sc.ctas + units_per_kv - 1) / units_per_kv));
+    const long long front_heads = kv_heads - tail_heads;
+    const long long front_windows = (front_heads + cap - 1) / cap;
+    auto window_of = [&](int kv) -> long long {
+        if (kv >= front_heads) return front_windows;
+        return static_cast<long long>(kv) * front_windows / front_heads;
+    };
+    // window by window; inside a window, heaviest first (stable: ties keep the (batch, head, tile) order)
     std::vector<int> order(n);
     std::iota(order.begin(), order.end(), 0);
-    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return units[a].cost > units[b].cost; });
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        const long long wa = window_of(units[a].kv), wb = window_of(units[b].kv);
+        if (wa != wb) return wa < wb;
+        return units[a].cost > units[b].cost;
+    });
     using Load = std::pair<double, int>;
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
     for (int c = 0; c < sc.ctas; ++c) heap.push({0.0, c});
@@ -176,12 +198,7 @@ Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas
     }
     sc.offsets.push_back(0);
     for (int c = 0; c < sc.ctas; ++c) {
-        auto& bin = bins[c];
-        std::stable_sort(bin.begin(), bin.end(), [&](int a, int b) {
-            const U &ua = units[a], &ub = units[b];
-            return std::make_tuple(ua.b, ua.kvh, ua.h, -ua.qt) < std::make_tuple(ub.b, ub.kvh, ub.h, -ub.qt);
-        });
-        for (int i : bin) {
+        for (int i : bins[c]) {
             sc.words.push_back(units[i].x);
             sc.words.push_back(units[i].y);
         }

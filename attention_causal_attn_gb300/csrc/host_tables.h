@@ -58,8 +58,22 @@ struct Schedule {
 
 // Cost-guided static schedule ("Flash Attention: Causal Prefill D=128", Step 4:
 // estimated cost 2(bm+1) + 4 per query tile, heaviest units first into the
-// lightest CTA, then each CTA's list ordered by batch/head for K/V locality).
-Schedule build_schedule(int B, int Hq, int Hkv, int S, bool causal, int num_ctas);
+// lightest CTA).
+//
+// K/V locality in L2: the KV heads, in (batch, KV head) order, are cut into
+// windows whose K and V together take at most kv_window_bytes (at least one
+// KV head per window).  Windows are scheduled one after another: the units of
+// a window go heaviest first into the CTA with the least load accumulated over
+// all earlier windows, and each CTA runs its units in that order.  The loads
+// stay balanced at every window boundary (to within one unit), so the CTAs
+// move through the windows together and the K/V tiles that the units running
+// at one time read from L2 belong to one or two windows.  The last window,
+// which has to even out what the earlier ones leave, is widened to at least
+// three units per CTA.  kv_window_bytes <= 0 puts every KV head into one
+// window (plain longest-first).
+constexpr double kScheduleWindowBytes = 64.0 * 1024.0 * 1024.0;
+Schedule build_schedule(int B, int Hq, int Hkv, int S, int D, bool causal, int num_ctas,
+                        double kv_window_bytes = kScheduleWindowBytes);
 
 // Number of work units build_schedule makes for a shape, without building it.
 long long schedule_units(int B, int Hq, int Hkv, int S);

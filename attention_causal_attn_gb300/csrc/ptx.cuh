@@ -72,6 +72,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// Wait, ignoring the abort flag but still within ctl.limit_ns (after which it
+// ORs `code` into the status word and gives up), until the phase with the
+// given parity has completed.  For the way out of a role: a TMA load, once
+// issued, lands whether or not anyone consumes it, so its producer waits for
+// it before the CTA may exit and its shared memory be reused.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int code) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > ctl.limit_ns) {
+            atomicOr(ctl.status, code);
+            return;
+        }
+    }
+}
+
+// mbar_drain for a ring of `stages` slot barriers (8 bytes apart from
+// `bar_first`) that has had `armed` loads so far, load i in slot i % stages
+// and phase i / stages: waits for the last load of every slot.  Each earlier
+// load of a slot was consumed before the slot was refilled.
+__device__ __forceinline__ void drain_ring(uint32_t bar_first, int stages, int armed, const WaitCtl& ctl, int code) {
+    for (int i = armed > stages ? armed - stages : 0; i < armed; ++i)
+        mbar_drain(bar_first + 8u * static_cast<uint32_t>(i % stages), static_cast<uint32_t>(i / stages) & 1u, ctl, code);
+}
+
+// mbar_wait for all 32 threads of a warp, with one result for the whole warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl, int code) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, code));
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -145,32 +174,41 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// The tensor-core issue primitives below (tc_commit, umma_ss, umma_ts) are
+// warp-collective: all 32 threads of a converged warp call them with the same
+// arguments, and one thread chosen by elect.sync issues the instruction.  An
+// issuer written this way keeps its warp converged, so its descriptors and
+// addresses stay warp-uniform values; an issuer running in a one-thread
+// branch measured about 1.5x slower per MMA and per barrier wait.
+
 // The mbarrier gets one arrive once every tcgen05 async op issued so far by
-// this thread has completed.
+// the issuing thread has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void tmem_store_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16 (fp16 or bf16 in, fp32 acc).
+// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16 (fp16 or bf16 in, fp32 acc).  Warp-collective.
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// D(tmem) (+)= A(tmem) * B(smem desc), kind::f16.
+// D(tmem) (+)= A(tmem) * B(smem desc), kind::f16.  Warp-collective.
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

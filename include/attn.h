@@ -46,7 +46,8 @@ typedef enum {
     ATTN_ERR_TIMEOUT = -6,     /* a bounded in-kernel wait ran out (see attn_check) */
     ATTN_ERR_OOM = -7,         /* the library could not allocate its cached tables */
     ATTN_ERR_NO_DEVICE = -8,   /* no sm_103 device is current */
-    ATTN_ERR_SCRATCH = -9      /* attn_fwd_noalloc: tables exceed its static scratch */
+    ATTN_ERR_SCRATCH = -9,     /* attn_fwd_noalloc: tables exceed its static scratch */
+    ATTN_ERR_NONFINITE = -10   /* a forward row's result was not finite (see attn_check) */
 } attn_status;
 
 /*
@@ -71,8 +72,11 @@ typedef enum {
  * S, D, rope_base, window_k, B, Hq, Hkv) builds and uploads tables
  * synchronously; later calls only launch.  Precision: with RoPE on, the
  * rotated Q and K are rounded to fp16 for the QK^T product (inputs must keep
- * |x| < 46000 so the rotated values stay finite); with RoPE off, Q and K go
- * to the tensor cores as the given bf16 values.
+ * |x| < 46000 so the rotated values stay finite: a rotation keeps each pair's
+ * norm, and sqrt(2) * 46000 < 65504); with RoPE off, Q and K go to the tensor
+ * cores as the given bf16 values.  A row whose LSE comes out non-finite (an
+ * input past that bound or not finite) raises a bit in the device status
+ * word, and the next attn_check reports ATTN_ERR_NONFINITE.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int Hq, int Hkv, int S, int D, int causal,
@@ -98,14 +102,22 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *     units (B * Hq * S up to roughly 5e8); larger requests return
  *     ATTN_ERR_SCRATCH before anything is enqueued.  The window must be off.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and creates one event
+ *     (no device memory); make that first call before any stream capture.
  *   - The array keeps the last call's contents.  A call whose shape, RoPE base
  *     and causal flag differ from the previous call on the device re-uploads
  *     the tables with cudaMemcpyAsync on `stream` (from pageable host memory,
- *     so the host waits for the staging); otherwise it only launches.
- *   - All calls share the one array: calls on different streams that overlap
- *     on the GPU race on it unless they use the same shape and options.
+ *     so the host waits for the staging) and records the event there;
+ *     otherwise it only launches.  A call of the same shape on another stream
+ *     waits for that event (cudaStreamWaitEvent) until the upload has been
+ *     seen complete, so it never reads tables still in flight.
+ *   - While `stream` is being captured, a call that would upload, or that
+ *     would have to wait for an upload enqueued on another stream, returns
+ *     ATTN_ERR_UNSUPPORTED and enqueues nothing.
+ *   - All calls share the one array: a call whose shape or options differ
+ *     overwrites the tables that a call still running on another stream
+ *     reads (a race).  Keep such calls on one stream, or synchronise between
+ *     them.
  */
 int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int Hq, int Hkv, int S, int D, int causal,
@@ -306,6 +318,34 @@ int attn_mask_schedule(const int* row_ptr, int nrows, long long bh, int num_ctas
                        int* ctas_out);
 
 /*
+ * attn_fwd_schedule — the static tile schedule attn_fwd launches with, for
+ * inspection and tests (host only).
+ * A work unit is two 128-row query tiles that share one KV head: two
+ * consecutive tiles of one head (Hq == Hkv), or two query heads of one KV
+ * group at the same tile (Hq > Hkv; a group of odd size ends with a unit of
+ * one head).  Unit word pair: x = qtile0 | qtile1 << 16 (0xFFFF: no second
+ * tile), y = h0 | h1 << 8 | b << 16.  Its estimated cost is 2(bm + 1) + 4 per
+ * query tile bm ("Flash Attention: Causal Prefill D=128", Step 4).
+ * The KV heads, in (batch, KV head) order, are cut into windows whose K and
+ * V take at most kv_window_bytes (at least one KV head each; <= 0: one
+ * window); window by window, the heaviest units go first into the CTA with
+ * the least load accumulated so far, and each CTA runs its units in that
+ * order, so the CTAs move through the windows together and share K/V tiles
+ * in L2.  attn_fwd uses 64 MiB, or ATTN_SCHEDULE_WINDOW_MB from the
+ * environment when it is set.
+ *   num_ctas     >= 1 (attn_fwd passes the device's SM count);
+ *                ctas = min(num_ctas, units)
+ *   words_out    host uint32 [2 * units], or NULL
+ *   offsets_out  host int32 [ctas + 1], or NULL: CTA c runs units
+ *                offsets_out[c] .. offsets_out[c+1]
+ *   ctas_out     host int32, or NULL: receives ctas
+ * Returns ATTN_ERR_SHAPE / ATTN_ERR_UNSUPPORTED on bad arguments.  Pure host
+ * computation.
+ */
+int attn_fwd_schedule(int B, int Hq, int Hkv, int S, int D, int causal, int num_ctas, double kv_window_bytes,
+                      unsigned* words_out, int* offsets_out, int* ctas_out);
+
+/*
  * attn_build_tables — the host-side RoPE angles and window widths.
  *
  * The kernel derives the same angles on the device by complex multiplication
@@ -324,9 +364,28 @@ int attn_build_tables(int S, int D, double rope_base, double window_k, long long
                       float* cos_out, float* sin_out, int* win_out);
 
 /*
+ * attn_selftest_wait_timeout — a check of the kernels' bounded waits, for tests.
+ *
+ * The source pages have no counterpart: this is failure detection.  It
+ * enqueues the attn_fwd kernel for the given arguments (as attn_fwd, window
+ * off) in a mode in which its TMA producer issues no load at all, with each
+ * in-kernel wait limited to wait_limit_ns.  Every role's first wait then runs
+ * out: the CTAs raise the status word and leave (no load or tensor-core work
+ * is in flight), and attn_check(stream) returns ATTN_ERR_TIMEOUT.  Nothing is
+ * read from q, k, v or written to o and lse; the device stays usable.
+ *   wait_limit_ns  100000 (0.1 ms) .. 2000000000 (the limit of real launches),
+ *                  else ATTN_ERR_UNSUPPORTED.
+ */
+int attn_selftest_wait_timeout(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int Hq, int Hkv, int S, int D, int causal,
+                               double rope_base, unsigned long long wait_limit_ns, void* stream);
+
+/*
  * attn_check — synchronise `stream`, then read and clear the device status
- * word that the kernels raise when a bounded wait inside them runs out.
- * Returns ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA if the stream failed.
+ * word that the kernels raise when a bounded wait inside them runs out, or
+ * when a row of the forward (attn_fwd and the entries built on it) came out
+ * non-finite.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (which takes precedence),
+ * ATTN_ERR_NONFINITE, or ATTN_ERR_CUDA if the stream failed.
  */
 int attn_check(void* stream);
 

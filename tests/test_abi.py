@@ -19,7 +19,8 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
     assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated",
-                          "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "attn_fwd_local", "attn_mask_schedule", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
+                          "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "attn_fwd_local", "attn_mask_schedule", "attn_fwd_schedule", "attn_selftest_wait_timeout",
+                          "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for n in names:

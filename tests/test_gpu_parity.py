@@ -36,8 +36,12 @@ def _check(o, lse, o_ref, lse_ref, tag=""):
     assert err.max() <= O_MAX, f"{tag}: max|dO| {err.max():.3e}"
     assert err.mean() <= O_MEAN, f"{tag}: mean|dO| {err.mean():.3e}"
     if lse is not None:
-        lerr = np.abs(np.asarray(lse, np.float64) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
-        assert lerr.max() <= LSE_REL, f"{tag}: max rel dLSE {lerr.max():.3e}"
+        # the gate: |dLSE| <= 1e-3 * max(1, |LSE|) (a row's LSE can be near 0, e.g. row 0's is one
+        # score); the plain relative error is reported beside it
+        d = np.abs(np.asarray(lse, np.float64) - lse_ref)
+        lerr = d / np.maximum(1.0, np.abs(lse_ref))
+        rel = d / np.maximum(1e-6, np.abs(lse_ref))
+        assert lerr.max() <= LSE_REL, f"{tag}: max dLSE/max(1,|LSE|) {lerr.max():.3e} (plain relative {rel.max():.3e})"
     return err.max()
 
 
@@ -180,7 +184,7 @@ def test_window_small_all_rows(B, Hq, Hkv, S, D, base, k):
 
 
 def _sampled_window(k):
-    return _sampled(1, 32, 8, 131072, 128, True, 500000.0, nrows=128, window_k=k)
+    return _sampled(1, 32, 8, 131072, 128, True, 500000.0, window_k=k)
 
 
 @pytest.mark.parametrize("k", [1.0, 4.0, None])

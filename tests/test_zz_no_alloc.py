@@ -59,6 +59,54 @@ def test_noalloc_matches_attn_fwd_on_two_calls(B, Hq, Hkv, S, D, causal, base):
         assert lerr.max() <= LSE_REL
 
 
+def test_noalloc_waits_for_an_upload_enqueued_on_another_stream():
+    """A call whose tables were uploaded on stream A, repeated with the same shape on stream B
+    before A has run, must wait for the upload rather than read the array's previous contents.
+
+    Stream A is held back by a sleep kernel, so B would otherwise launch first.  The previous
+    contents come from a smaller RoPE shape whose upload covers only the start of the array
+    (below the larger shape's schedule), so a launch that did not wait would read wrong RoPE
+    factors but nothing outside its tensors."""
+    lib = attn.load_library()
+    big = (2, 4, 2, 700, 128)     # its RoPE table ends below its schedule's offset in the array
+    small = (1, 2, 2, 128, 128)   # its whole upload lies below the larger shape's schedule
+    base = 10000.0
+
+    def inputs(shape, seed):
+        B, Hq, Hkv, S, D = shape
+        return [_dev(x) for x in si.make_qkv(B, Hq, Hkv, S, D, seed=seed)]
+
+    qb, kb, vb = inputs(big, 91)
+    qs, ks, vs = inputs(small, 92)
+    o_ref, lse_ref = attn.attn_fwd(qb, kb, vb, causal=True, rope_base=base)
+    attn.attn_check()
+    o_ref, lse_ref = o_ref.float().cpu().numpy(), lse_ref.cpu().numpy()
+
+    def outputs(q):
+        B, S, Hq, D = q.shape
+        return (torch.full_like(q, float("nan")),
+                torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device=q.device))
+
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    o1, l1 = outputs(qb)
+    assert _noalloc(lib, qb, kb, vb, o1, l1, True, base, sa) == 0   # the larger shape's tables
+    o2, l2 = outputs(qs)
+    assert _noalloc(lib, qs, ks, vs, o2, l2, True, base, sa) == 0   # overwritten at the start
+    torch.cuda.synchronize()
+    o3, l3 = outputs(qb)
+    with torch.cuda.stream(sa):
+        torch.cuda._sleep(200_000_000)  # holds stream A back by tens of milliseconds
+    assert _noalloc(lib, qb, kb, vb, o3, l3, True, base, sa) == 0   # re-upload, enqueued behind the sleep
+    assert _noalloc(lib, qb, kb, vb, o3, l3, True, base, sb) == 0   # same shape on stream B: must wait
+    torch.cuda.synchronize()
+    attn.attn_check()
+    err = np.abs(o3.float().cpu().numpy() - o_ref)
+    assert np.isfinite(err).all()
+    assert err.max() <= O_MAX and err.mean() <= O_MEAN
+    lerr = np.abs(l3.cpu().numpy() - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+    assert lerr.max() <= LSE_REL
+
+
 def test_noalloc_rejects_requests_beyond_its_scratch():
     lib = attn.load_library()
     q = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: the size check comes first

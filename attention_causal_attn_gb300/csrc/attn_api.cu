@@ -217,7 +217,7 @@ int launch(const FwdParams& prm, int grid, cudaStream_t stream, DevInfo& di) {
     constexpr unsigned bit = 1u << ((WINDOW ? 8 : 0) | (D == 128 ? 4 : 0) | (CAUSAL ? 2 : 0) | (ROPE ? 1 : 0));
     auto kern = attn::attn_fwd_kernel<D, CAUSAL, ROPE, WINDOW>;
     // At least 120 KB so that only one CTA fits on an SM: each CTA takes all 512 TMEM columns.
-    using Layout = attn::SmemLayout<D, WINDOW>;
+    using Layout = attn::SmemLayout<D>;
     constexpr int smem = static_cast<int>(Layout::kAlloc) > 120 * 1024 ? static_cast<int>(Layout::kAlloc) : 120 * 1024;
     cudaError_t e;
     if (!(di.configured.load(std::memory_order_acquire) & bit)) {
@@ -286,8 +286,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
         sched = *se;
         prm.status = g_dev[dev].status;
     }
-    if (!encode_operands(&prm, q, k, v, o, B, S, Hq, Hkv, D) ||
-        (window && !encode_bshd(&prm.tm_k16, k, B, S, Hkv, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)))
+    if (!encode_operands(&prm, q, k, v, o, B, S, Hq, Hkv, D))
         return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
     {
         const std::vector<int32_t> w = attn_host::window_widths(D, rope ? rope_base : 10000.0, window ? window_k : 0.0);

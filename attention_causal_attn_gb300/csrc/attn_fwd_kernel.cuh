@@ -17,8 +17,8 @@
 //   warp 12     TMA producer: Q tiles, then K/V tiles from the diagonal down to
 //               tile 0 ("Flash Attention: Causal Prefill D=128", reverse
 //               traversal isolates the causal mask to the first tile)
-//   warp 13     tcgen05 issuer (the converged warp; one elected thread issues)
-//               and TMEM owner
+//   warp 13     tcgen05 issuer (the converged warp, one elected thread issues;
+//               one thread in the windowed variant) and TMEM owner
 //   warps 14-15 idle (they complete the fourth warpgroup)
 //
 // TMEM (512 columns x 128 lanes x 32 bit): S0 [0,128), S1 [128,256), O0 [256,
@@ -53,11 +53,7 @@ namespace attn {
 
 constexpr int kBlockM = 128;  // query rows per stage
 constexpr int kBlockN = 128;  // keys per KV tile
-constexpr int kMaxKStages = 3;
-// K ring depth: the windowed variant holds each K tile until its PV is issued
-// (the softmax reads boundary pairs from it), so it keeps one more tile in flight.
-template <bool WINDOW>
-__host__ __device__ constexpr int k_stages() { return WINDOW ? 3 : 2; }
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kNumThreads = 512;  // four warpgroups; launched at 128 registers per thread
 constexpr int kWarpRope = 8;
@@ -82,7 +78,6 @@ struct FwdParams {
     CUtensorMap tm_q;  // [B][S][Hq][D] bf16, box {64, 1, 128, 1}, 128B swizzle
     CUtensorMap tm_k;  // [B][S][Hkv][D]
     CUtensorMap tm_v;
-    CUtensorMap tm_k16; // K again, box {16, 1, 128, 1}, 32-byte swizzle (windowed variant: one 16-channel group per load)
     CUtensorMap tm_o;   // O [B][S][Hq][D] bf16, box {64, 1, 32, 1}, 128B swizzle: one warp's rows of one 64-channel block
     __nv_bfloat16* o;   // [B][S][Hq][D]
     float* lse;         // [B][Hq][S] or null
@@ -107,9 +102,9 @@ enum : int {
     BAR_Q_ROT = 2,    // [2] Q_s rotated (RoPE)
     BAR_Q_EMPTY = 4,  // [2] last QK^T of the unit read Q_s
     BAR_K_FULL = 6,   // [kKStages]
-    BAR_K_ROT = BAR_K_FULL + kMaxKStages,
-    BAR_K_EMPTY = BAR_K_ROT + kMaxKStages,
-    BAR_V_FULL = BAR_K_EMPTY + kMaxKStages,  // [kVStages]
+    BAR_K_ROT = BAR_K_FULL + kKStages,
+    BAR_K_EMPTY = BAR_K_ROT + kKStages,
+    BAR_V_FULL = BAR_K_EMPTY + kKStages,  // [kVStages]
     BAR_V_EMPTY = BAR_V_FULL + kVStages,
     BAR_S_FULL = BAR_V_EMPTY + kVStages,  // [2] S_s(n) in TMEM (and PV_s(n+1) done)
     BAR_P_FULL = BAR_S_FULL + 2,          // [2] P_s(n) in TMEM, O_s rescaled
@@ -121,22 +116,17 @@ enum : int {
 
 // Output staging for the TMA-store epilogue: per stage, one [32 rows][128 B]
 // block (64 channels, 128-byte swizzle) per warp of the softmax warpgroup.
-// The windowed variant's third K stage leaves no room for it; it stores O
-// with plain per-row stores.
-template <bool WINDOW>
-__host__ __device__ constexpr bool epi_tma() { return !WINDOW; }
 constexpr uint32_t kEpiWarpBytes = 32u * 128u;
 constexpr uint32_t kEpiStageBytes = 4u * kEpiWarpBytes;
 
-template <int D, bool WINDOW>
+template <int D>
 struct SmemLayout {
-    static constexpr int KS = k_stages<WINDOW>();
     static constexpr uint32_t kTileBytes = 128u * D * 2u;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kK = kQ + 2 * kTileBytes;
-    static constexpr uint32_t kV = kK + KS * kTileBytes;
+    static constexpr uint32_t kV = kK + kKStages * kTileBytes;
     static constexpr uint32_t kO = kV + kVStages * kTileBytes;  // 1024-byte aligned (tiles are multiples of 16 KB)
-    static constexpr uint32_t kBars = kO + (epi_tma<WINDOW>() ? 2 * kEpiStageBytes : 0u);
+    static constexpr uint32_t kBars = kO + 2 * kEpiStageBytes;
     static constexpr uint32_t kMisc = kBars + 8 * NUM_BARS;
     static constexpr uint32_t kBytes = kMisc + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -183,10 +173,10 @@ __device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int i) { return bar0 +
 //        for every cell); pairs in [.x, .y) are the tile's boundary pairs.
 //
 // Pairs below z are dropped for every cell of the KV tile against every query
-// tile of the unit.  K is held as D/16 groups of 16 channels (one K=16 MMA
-// step each); the 16-pair blocks below m0 = z / 16 are never loaded nor
-// multiplied (for block m: channel groups m and m + D/32), and the pairs of
-// block m0 below z are zeroed in shared memory.
+// tile of the unit.  A K=16 MMA step multiplies 16 channels, so the 16-pair
+// blocks below m0 = z / 16 are neither rotated nor multiplied (block m is
+// k-steps m and m + D/32: the pairs' first and second members), and the pairs
+// of block m0 below z are zeroed in shared memory by the rotation.
 struct WinTile {
     int z, m0;
 };
@@ -208,8 +198,7 @@ __device__ __forceinline__ WinTile window_tile(const FwdParams& p, const Unit& u
 template <int D, bool WINDOW>
 __device__ void producer_issue(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, int t_begin, int t_end,
                                const WaitCtl& ctl, int& kit, int& vit, int (&qit)[2]) {
-    constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, WINDOW>;
+    using L = SmemLayout<D>;
     for (int ti = t_begin; ti < t_end; ++ti) {
         const Unit u = decode_unit(p.tasks[ti], p, causal);
 #pragma unroll
@@ -225,25 +214,12 @@ __device__ void producer_issue(const FwdParams& p, bool causal, uint32_t sm, uin
         }
         for (int n = u.nmax; n >= 0; --n) {
             const int ks = kit % kKStages;
-            const WinTile w = WINDOW ? window_tile<D>(p, u, n) : WinTile{0, 0};  // before the wait: load in flight
             if (!mbar_wait(bar_at(bar0, BAR_K_EMPTY + ks), ((kit / kKStages) & 1) ^ 1, ctl, kStatusProducer)) return;
             const uint32_t kb = bar_at(bar0, BAR_K_FULL + ks);
-            if (WINDOW) {
-                // only the 16-pair blocks with a kept pair: 16 channels x 128 rows = 4 KB per group, two per block
-                constexpr int kBlocks = D / 32;
-                mbar_arrive_expect_tx(kb, static_cast<uint32_t>(2 * (kBlocks - w.m0)) * 4096u);
-                for (int m = w.m0; m < kBlocks; ++m) {
-                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + m * 4096u, &p.tm_k16, kb, 16 * m, u.kvh,
-                                n * kBlockN, u.b);
-                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + (m + kBlocks) * 4096u, &p.tm_k16, kb,
-                                D / 2 + 16 * m, u.kvh, n * kBlockN, u.b);
-                }
-            } else {
-                mbar_arrive_expect_tx(kb, L::kTileBytes);
-                for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + sub * kSubTileBytes, &p.tm_k, kb, sub * 64, u.kvh,
-                                n * kBlockN, u.b);
-            }
+            mbar_arrive_expect_tx(kb, L::kTileBytes);
+            for (int sub = 0; sub < D / 64; ++sub)
+                tma_load_4d(sm + L::kK + ks * L::kTileBytes + sub * kSubTileBytes, &p.tm_k, kb, sub * 64, u.kvh,
+                            n * kBlockN, u.b);
             ++kit;
             const int vs = vit % kVStages;
             if (!mbar_wait(bar_at(bar0, BAR_V_EMPTY + vs), ((vit / kVStages) & 1) ^ 1, ctl, kStatusProducer)) return;
@@ -267,7 +243,7 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
     // every slot has landed before the CTA may exit (the earlier ones were consumed).
 #pragma unroll
     for (int s = 0; s < 2; ++s) drain_ring(bar_at(bar0, BAR_Q_FULL + s), 1, qit[s], ctl, kStatusDrain);
-    drain_ring(bar_at(bar0, BAR_K_FULL), k_stages<WINDOW>(), kit, ctl, kStatusDrain);
+    drain_ring(bar_at(bar0, BAR_K_FULL), kKStages, kit, ctl, kStatusDrain);
     drain_ring(bar_at(bar0, BAR_V_FULL), kVStages, vit, ctl, kStatusDrain);
 }
 
@@ -277,10 +253,7 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
 // c of row r sits at chunk c ^ (r & 7)).  Pair (r, r + D/2) has both members
 // at the same swizzled offset in column blocks 0 and 1 for D = 128, and in
 // chunks c and c + 4 of the single block for D = 64, so each thread rotates
-// whole pairs from two 16-byte loads.  The windowed variant stores K as D/16
-// channel groups of [128 rows][32 B] with the 32-byte swizzle (group g at
-// g * 4 KB; the 16-byte half h of row r sits at half h ^ ((r >> 2) & 1)), so
-// that dropped groups are never loaded.  Input bf16, math fp32, output fp16.
+// whole pairs from two 16-byte loads.  Input bf16, math fp32, output fp16.
 //
 // Thread t owns chunk c = t / kRows (pairs 8c..8c+7) of rows rr + kRows*i,
 // rr = t % kRows: eight consecutive threads touch eight rows of one chunk,
@@ -340,8 +313,8 @@ __device__ __forceinline__ void cmul2(uint64_t& c, uint64_t& s, uint64_t fc, uin
     c = nc;
 }
 
-// LAYOUT_GROUPS: the windowed K layout; pairs below `zero_below` come out as 0.
-template <int D, bool LAYOUT_GROUPS>
+// ZERO (windowed variant): pairs below `zero_below` come out as 0.
+template <int D, bool ZERO>
 __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts& k, uint64_t (&cb)[4],
                                                  uint64_t (&sb)[4], int t, int zero_below = 0) {
     using G = RopeGeom<D>;
@@ -353,11 +326,7 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
     for (int i = 0; i < G::kIters; ++i) {
         const int row = rr + G::kRows * i;
         uint32_t lo_off, hi_off;
-        if (LAYOUT_GROUPS) {
-            const uint32_t half = static_cast<uint32_t>(((c & 1) ^ ((row >> 2) & 1)) << 4);
-            lo_off = static_cast<uint32_t>((c >> 1) * 4096 + row * 32) + half;
-            hi_off = lo_off + static_cast<uint32_t>(G::kChunks / 2 * 4096);
-        } else if (D == 128) {
+        if (D == 128) {
             lo_off = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
             hi_off = lo_off + kSubTileBytes;
         } else {
@@ -378,7 +347,7 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
             f2_unpack(f2_fma(y, cb[q], f2_mul(x, sb[q])), b0, b1);           // y cos + x sin
             lo_out[q] = pack_f16x2(a0, a1);
             hi_out[q] = pack_f16x2(b0, b1);
-            if (LAYOUT_GROUPS) {  // pairs 8c+2q, 8c+2q+1 below zero_below are dropped
+            if (ZERO) {  // pairs 8c+2q, 8c+2q+1 below zero_below are dropped
                 const int pr = 8 * c + 2 * q;
                 const uint32_t keep = (pr >= zero_below ? 0x0000FFFFu : 0u) | (pr + 1 >= zero_below ? 0xFFFF0000u : 0u);
                 lo_out[q] &= keep;
@@ -395,8 +364,7 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
 template <int D, bool WINDOW>
 __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_t bar0, int t_begin, int t_end,
                           const WaitCtl& ctl, int t) {
-    constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, WINDOW>;
+    using L = SmemLayout<D>;
     RopeConsts k;
     rope_load_consts<D>(p, t, k);
     int kit = 0;
@@ -425,7 +393,8 @@ __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_
             if (WINDOW) {
                 using G = RopeGeom<D>;
                 const int c = t / G::kRows;
-                // chunk c is in block c / 2; blocks below m0 were not loaded and are not multiplied
+                // chunk c (pairs 8c..8c+7) is in 16-pair block c / 2; the blocks below m0 are not
+                // multiplied, and the pairs of block m0 below z are zeroed
                 if (c / 2 >= w.m0) rope_rotate_tile<D, true>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t, w.z);
             } else {
                 rope_rotate_tile<D, false>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t);
@@ -438,11 +407,35 @@ __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// Issuer form: the whole warp runs the loop and one elected thread issues,
+// so the warp stays converged; the alternative runs the loop on one thread.
+// Each is the faster one measured for its variant: converged without the
+// window (1215 against 1130 TFLOP/s on the RoPE + causal S=8192 prefill), one
+// thread with it (141 against 153 ms on the windowed S=131072 prefill, k=1).
+template <bool WINDOW>
+__host__ __device__ constexpr bool issue_one_thread() { return WINDOW; }
+
 template <int D, bool ROPE, bool WINDOW>
 __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t bar0, uint32_t tmem, int t_begin,
                          int t_end, const WaitCtl& ctl) {
-    constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, WINDOW>;
+    constexpr bool kWarp = !issue_one_thread<WINDOW>();
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if constexpr (kWarp) return mbar_wait_warp(bar, parity, ctl, kStatusMma);
+        else return mbar_wait(bar, parity, ctl, kStatusMma);
+    };
+    auto commit = [&](uint32_t bar) {
+        if constexpr (kWarp) tc_commit(bar);
+        else tc_commit_one(bar);
+    };
+    auto mma_ss = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+        if constexpr (kWarp) umma_ss(d, a, b, idesc, acc);
+        else umma_ss_one(d, a, b, idesc, acc);
+    };
+    auto mma_ts = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+        if constexpr (kWarp) umma_ts(d, a, b, idesc, acc);
+        else umma_ts_one(d, a, b, idesc, acc);
+    };
+    using L = SmemLayout<D>;
     // QK^T: A = Q tile, B = K tile, both K-major; fp16 after rotation, bf16 otherwise.
     const uint32_t kIdescQK = umma_idesc_f16((ROPE || p.qk_f16) ? 0u : 1u, 0u, kBlockM, kBlockN);
     // PV: A = P (bf16, TMEM), B = V tile [keys][D] with D contiguous: MN-major.
@@ -454,11 +447,10 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
     // operand descriptors, built once; each MMA step only advances the start address
     const uint64_t qdesc0 = sw128_desc(sm + L::kQ, 16u, 1024u);
     const uint64_t qdesc1 = sw128_desc(sm + L::kQ + L::kTileBytes, 16u, 1024u);
-    // windowed K: one 16-channel group of [128 rows][32 B] per K=16 step, 32-byte swizzle, 8-row atoms 256 B apart
-    const uint64_t kdesc0 = WINDOW ? sw32_desc(sm + L::kK, 256u) : sw128_desc(sm + L::kK, 16u, 1024u);
+    const uint64_t kdesc0 = sw128_desc(sm + L::kK, 16u, 1024u);
     const uint64_t vdesc0 = sw128_desc(sm + L::kV, kSubTileBytes, 1024u);
     const uint64_t vdesc1 = sw128_desc(sm + L::kV + L::kTileBytes, kSubTileBytes, 1024u);
-    int kit = 0, vit = 0, krel = 0;
+    int kit = 0, vit = 0;
     int qit[2] = {0, 0}, pit[2] = {0, 0}, oit[2] = {0, 0};
     bool ok = true;
     for (int ti = t_begin; ti < t_end && ok; ++ti) {
@@ -479,40 +471,35 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
                 const uint32_t tO = tmem + 256u + static_cast<uint32_t>(s * 128);
                 if (do_pv && n + 1 <= u.nhi[s]) {
                     if (!v_ready) {
-                        ok = mbar_wait_warp(bar_at(bar0, BAR_V_FULL + vs), (vit / kVStages) & 1, ctl, kStatusMma);
+                        ok = wait(bar_at(bar0, BAR_V_FULL + vs), (vit / kVStages) & 1);
                         if (!ok) break;
                         v_ready = true;
                     }
-                    ok = mbar_wait_warp(bar_at(bar0, BAR_P_FULL + s), pit[s] & 1, ctl, kStatusMma);
+                    ok = wait(bar_at(bar0, BAR_P_FULL + s), pit[s] & 1);
                     if (!ok) break;
                     ++pit[s];
                     if (first_pv[s]) {
-                        ok = mbar_wait_warp(bar_at(bar0, BAR_O_FREE + s), (oit[s] & 1) ^ 1, ctl, kStatusMma);
+                        ok = wait(bar_at(bar0, BAR_O_FREE + s), (oit[s] & 1) ^ 1);
                         if (!ok) break;
                     }
                     tc_fence_after();
                     const uint64_t vdesc = vs ? vdesc1 : vdesc0;
                     // 16 keys per step: 2048 bytes of V, 8 TMEM columns of P
-                    umma_ts(tO, tS, vdesc, kIdescPV, first_pv[s] ? 0u : 1u);
+                    mma_ts(tO, tS, vdesc, kIdescPV, first_pv[s] ? 0u : 1u);
 #pragma unroll
                     for (int kk = 1; kk < kBlockN / 16; ++kk)
-                        umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, 1u);
+                        mma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, 1u);
                     first_pv[s] = false;
-                    if (WINDOW && n + 1 == 0) {
-                        // windowed: the softmax reads Q_s until it hands over the unit's last P
-                        tc_commit(bar_at(bar0, BAR_Q_EMPTY + s));
-                        ++qit[s];
-                    }
                 }
                 if (do_s && n <= u.nhi[s]) {
                     if (!k_ready) {
-                        ok = mbar_wait_warp(bar_at(bar0, kbar_ready + ks), (kit / kKStages) & 1, ctl, kStatusMma);
+                        ok = wait(bar_at(bar0, kbar_ready + ks), (kit / kKStages) & 1);
                         if (!ok) break;
                         k_ready = true;
                         tc_fence_after();
                     }
                     if (n == u.nhi[s]) {
-                        ok = mbar_wait_warp(bar_at(bar0, qbar_ready + s), qit[s] & 1, ctl, kStatusMma);
+                        ok = wait(bar_at(bar0, qbar_ready + s), qit[s] & 1);
                         if (!ok) break;
                         tc_fence_after();
                     }
@@ -525,49 +512,41 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             if (kk % (D / 32) < m0) continue;
-                            const uint32_t qunits = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
-                            umma_ss(tS, desc_advance(qdesc, qunits), desc_advance(kdesc, kk * 256u), kIdescQK, acc);
+                            const uint32_t units = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
+                            mma_ss(tS, desc_advance(qdesc, units), desc_advance(kdesc, units), kIdescQK, acc);
                             acc = 1u;
                         }
                     } else {
                         // 16 channels per step: 32 bytes inside a 128-byte row, next column block every 4 steps
-                        umma_ss(tS, qdesc, kdesc, kIdescQK, 0u);
+                        mma_ss(tS, qdesc, kdesc, kIdescQK, 0u);
 #pragma unroll
                         for (int kk = 1; kk < D / 16; ++kk) {
                             const uint32_t units = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
-                            umma_ss(tS, desc_advance(qdesc, units), desc_advance(kdesc, units), kIdescQK, 1u);
+                            mma_ss(tS, desc_advance(qdesc, units), desc_advance(kdesc, units), kIdescQK, 1u);
                         }
                     }
-                    tc_commit(bar_at(bar0, BAR_S_FULL + s));
-                    if (!WINDOW && n == 0) ++qit[s];  // Q_s is released by its softmax once S_s(0) has landed
+                    commit(bar_at(bar0, BAR_S_FULL + s));
+                    if (n == 0) ++qit[s];  // Q_s is released by its softmax (see softmax_loop)
                 }
             }
             if (!ok) break;
-            // Without the window the K/V slots are released by the softmax (see
-            // softmax_loop): each commit here would take a slot of the tensor
-            // core's short instruction queue between two groups of MMAs.
+            // The K/V slots are released by the softmax (see softmax_loop): each
+            // commit here would take a slot of the tensor core's short
+            // instruction queue between two groups of MMAs.
             if (do_s) ++kit;
-            if (WINDOW && do_pv) {
-                // windowed: the softmax reads K(n+1) until it hands over P(n+1), which the PVs above waited for
-                tc_commit(bar_at(bar0, BAR_K_EMPTY + krel % kKStages));
-                ++krel;
-            }
-            if (do_pv) {
-                if (WINDOW) tc_commit(bar_at(bar0, BAR_V_EMPTY + vs));
-                ++vit;
-            }
+            if (do_pv) ++vit;
         }
         if (!ok) break;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             if (!u.valid[s]) continue;
-            tc_commit(bar_at(bar0, BAR_O_FULL + s));
+            commit(bar_at(bar0, BAR_O_FULL + s));
             ++oit[s];
         }
     }
     // Drain: every issued MMA must finish before TMEM is released.  This wait
     // ignores the abort flag but keeps its own time limit.
-    tc_commit(bar_at(bar0, BAR_DRAIN));
+    commit(bar_at(bar0, BAR_DRAIN));
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar_at(bar0, BAR_DRAIN), 0)) {
         if (global_timer_ns() - t0 > ctl.limit_ns) {
@@ -687,18 +666,16 @@ __device__ __noinline__ void window_correct(uint32_t tS, const uint8_t* qtile, c
                                     (dx % 8) * 2);
             const float qy = f16_at(qtile + (dy / 64) * kSubTileBytes + t * 128 + ((((dy % 64) / 8) ^ (t & 7)) << 4) +
                                     (dy % 8) * 2);
-            // K in 16-channel groups with the 32-byte swizzle: channel d of key row j at
-            // (d/16)*4096 + j*32 + ((((d%16)/8) ^ ((j>>2)&1)) << 4) + (d%8)*2; cc is a multiple of 8,
-            // so the swizzle bit of key cc + j is (j >> 2) & 1
-            const uint8_t* kx = ktile + (dx / 16) * 4096 + (dx % 8) * 2 + cc * 32;
-            const uint8_t* ky = ktile + (dy / 16) * 4096 + (dy % 8) * 2 + cc * 32;
-            const int hx = ((dx % 16) / 8) << 4, hy = ((dy % 16) / 8) << 4;
+            // K as Q: channel d of key row j at (d/64)*kSubTileBytes + j*128 + ((((d%64)/8) ^ (j&7)) << 4)
+            // + (d%8)*2; cc is a multiple of 8, so the swizzle of key cc + j is j & 7
+            const uint8_t* kx = ktile + (dx / 64) * kSubTileBytes + (dx % 8) * 2 + cc * 128;
+            const uint8_t* ky = ktile + (dy / 64) * kSubTileBytes + (dy % 8) * 2 + cc * 128;
+            const int hx = (dx % 64) / 8, hy = (dy % 64) / 8;
             float kxv[32], kyv[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const int sw = ((j >> 2) & 1) << 4;
-                kxv[j] = f16_at(kx + j * 32 + (hx ^ sw));
-                kyv[j] = f16_at(ky + j * 32 + (hy ^ sw));
+                kxv[j] = f16_at(kx + j * 128 + ((hx ^ (j & 7)) << 4));
+                kyv[j] = f16_at(ky + j * 128 + ((hy ^ (j & 7)) << 4));
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -718,9 +695,8 @@ __device__ __noinline__ void window_correct(uint32_t tS, const uint8_t* qtile, c
 template <int D, bool CAUSAL, bool WINDOW>
 __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32_t bar0, uint32_t tmem, int t_begin,
                              int t_end, const WaitCtl& ctl, int t) {
-    constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, WINDOW>;
-    int kit = 0;  // K tiles seen by the unit loop (which K stage holds tile n), windowed variant
+    using L = SmemLayout<D>;
+    int kit = 0;  // K tiles seen by the unit loop (which K stage holds tile n)
     const uint32_t lane_base = static_cast<uint32_t>(t & ~31);  // this warp's TMEM lane quarter
     const uint32_t trow = tmem + (lane_base << 16);
     const uint32_t tS = trow + static_cast<uint32_t>(stage * 128);
@@ -750,15 +726,15 @@ __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32
                 return;
             ++sit;
             tc_fence_after();
+            const int it = kit_unit + u.nmax - n;  // load index of K(n) and V(n)
+            if (releaser && t == 0) {
+                // S_s(n) landed, and the issue order puts it after every other
+                // product that reads V(n+1) (and K(n)): the slots are free again
+                if (n + 1 <= u.nmax) mbar_arrive(bar_at(bar0, BAR_V_EMPTY + (it - 1) % kVStages));
+                if (!WINDOW) mbar_arrive(bar_at(bar0, BAR_K_EMPTY + it % kKStages));
+            }
             if (!WINDOW && n == 0 && t == 0)  // the unit's last product reading Q_s has landed
                 mbar_arrive(bar_at(bar0, BAR_Q_EMPTY + stage));
-            if (!WINDOW && releaser && t == 0) {
-                // S_s(n) landed, and the issue order puts it after every other
-                // product that reads K(n) or V(n+1): both slots are free again
-                const int it = kit_unit + u.nmax - n;
-                mbar_arrive(bar_at(bar0, BAR_K_EMPTY + it % kKStages));
-                if (n + 1 <= u.nmax) mbar_arrive(bar_at(bar0, BAR_V_EMPTY + (it - 1) % kVStages));
-            }
             if (WINDOW) {
                 // boundary pairs: kept for the tile by the MMA, dropped beyond W_r for some of its cells
                 const int z = window_tile<D>(p, u, n).z;
@@ -766,8 +742,15 @@ __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32
                 const int r_end = p.wtab[rel0 / kBlockM].y;                       // kept everywhere from here on
                 if (z < r_end)
                     window_correct<D>(tS, smg + L::kQ + stage * L::kTileBytes,
-                                      smg + L::kK + ((kit_unit + u.nmax - n) % kKStages) * L::kTileBytes, p, z, r_end,
-                                      rel0 + t, t);
+                                      smg + L::kK + (it % kKStages) * L::kTileBytes, p, z, r_end, rel0 + t, t);
+                // K(n), and Q_s after tile 0, are free once both stages' corrections have read them:
+                // one arrival per warp and stage, doubled when the other stage does not visit tile n
+                __syncwarp();
+                if ((t & 31) == 0) {
+                    const bool other = stage ? (u.valid[0] && n <= u.nhi[0]) : (u.valid[1] && n <= u.nhi[1]);
+                    mbar_arrive_cnt(bar_at(bar0, BAR_K_EMPTY + it % kKStages), other ? 1u : 2u);
+                    if (n == 0) mbar_arrive(bar_at(bar0, BAR_Q_EMPTY + stage));
+                }
             }
             // keys [0, limit) of this tile are visible to this row; only the
             // diagonal tile (causal) and the ragged last tile have a limit < 128
@@ -818,7 +801,7 @@ __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32
             return;
         ++oit;
         tc_fence_after();
-        if (!WINDOW && releaser && t == 0)  // the unit's last products (PV of tile 0) are done: V(0) is free
+        if (releaser && t == 0)  // the unit's last products (PV of tile 0) are done: V(0) is free
             mbar_arrive(bar_at(bar0, BAR_V_EMPTY + (kit_unit + u.nmax) % kVStages));
         const float inv_l = 1.0f / l;
         const uint64_t il2 = f2_pack(inv_l, inv_l);
@@ -827,53 +810,25 @@ __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32
         if (row_ok && !isfinite(lse2)) atomicOr(p.status, kStatusNonFinite);
         if (row_ok && p.lse != nullptr)
             p.lse[(static_cast<size_t>(u.b) * p.Hq + head) * p.S + row] = lse2 * 0.69314718055994531f;
-        if constexpr (epi_tma<WINDOW>()) {
-            // Each warp stages its 32 rows one 64-channel block at a time (128-byte
-            // swizzle: chunk c of row r at chunk c ^ (r & 7)) and stores the block
-            // with one TMA copy; rows past S are clipped by the copy.  O_s is
-            // handed back as soon as its last columns are in registers.
-            const int lane = t & 31, wq = t >> 5;
-            uint8_t* blk = smg + L::kO + static_cast<uint32_t>(stage) * kEpiStageBytes + static_cast<uint32_t>(wq) * kEpiWarpBytes;
-            const int row0 = (stage ? u.row0[1] : u.row0[0]) + 32 * wq;
+        // Each warp stages its 32 rows one 64-channel block at a time (128-byte
+        // swizzle: chunk c of row r at chunk c ^ (r & 7)) and stores the block
+        // with one TMA copy; rows past S are clipped by the copy.  O_s is
+        // handed back as soon as its last columns are in registers.
+        const int lane = t & 31, wq = t >> 5;
+        uint8_t* blk = smg + L::kO + static_cast<uint32_t>(stage) * kEpiStageBytes + static_cast<uint32_t>(wq) * kEpiWarpBytes;
+        const int row0 = (stage ? u.row0[1] : u.row0[0]) + 32 * wq;
 #pragma unroll
-            for (int sub = 0; sub < D / 64; ++sub) {
-                if (lane == 0) bulk_wait_group_read<0>();  // the previous copy has read the block
-                __syncwarp();
+        for (int sub = 0; sub < D / 64; ++sub) {
+            if (lane == 0) bulk_wait_group_read<0>();  // the previous copy has read the block
+            __syncwarp();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {  // 32 channels (four 16-byte chunks) at a time
-                    uint32_t r[32];
-                    tmem_load_32(tO + 64 * sub + 32 * h, r);
-                    if (sub == D / 64 - 1 && h == 1) {
-                        tc_fence_before();
-                        mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
-                    }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float x0, x1;
-                        f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il2), x0, x1);
-                        pk[j] = pack_bf16x2(x0, x1);
-                    }
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int c8 = 4 * h + c4;
-                        *reinterpret_cast<uint4*>(blk + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
-                            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_4d(&p.tm_o, smem_addr(blk), 64 * sub, head, row0, u.b);
-                    bulk_commit_group();
-                }
-            }
-        } else {
-            __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.S + row) * p.Hq + head) * D;
-#pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
+            for (int h = 0; h < 2; ++h) {  // 32 channels (four 16-byte chunks) at a time
                 uint32_t r[32];
-                tmem_load_32(tO + cc, r);
+                tmem_load_32(tO + 64 * sub + 32 * h, r);
+                if (sub == D / 64 - 1 && h == 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -881,15 +836,19 @@ __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32
                     f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), il2), x0, x1);
                     pk[j] = pack_bf16x2(x0, x1);
                 }
-                if (row_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + cc);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int c8 = 4 * h + c4;
+                    *reinterpret_cast<uint4*>(blk + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
+                        make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar_at(bar0, BAR_O_FREE + stage));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_4d(&p.tm_o, smem_addr(blk), 64 * sub, head, row0, u.b);
+                bulk_commit_group();
+            }
         }
     }
 }
@@ -900,15 +859,14 @@ template <int D, bool CAUSAL, bool WINDOW>
 __device__ void softmax_role(const FwdParams& p, int stage, uint8_t* smg, uint32_t bar0, uint32_t tmem, int t_begin,
                              int t_end, const WaitCtl& ctl, int t) {
     softmax_loop<D, CAUSAL, WINDOW>(p, stage, smg, bar0, tmem, t_begin, t_end, ctl, t);
-    if (epi_tma<WINDOW>() && (t & 31) == 0) bulk_wait_group<0>();
+    if ((t & 31) == 0) bulk_wait_group<0>();
 }
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool CAUSAL, bool ROPE, bool WINDOW>
 __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     static_assert(!WINDOW || (CAUSAL && ROPE), "the window is defined with RoPE and causal masking");
-    constexpr int kKStages = k_stages<WINDOW>();
-    using L = SmemLayout<D, WINDOW>;
+    using L = SmemLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smg = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sm = smem_addr(smg);
@@ -924,7 +882,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_c
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_at(bar0, BAR_Q_FULL + s), 1);
             mbar_init(bar_at(bar0, BAR_Q_ROT + s), 128);
-            mbar_init(bar_at(bar0, BAR_Q_EMPTY + s), 1);
+            mbar_init(bar_at(bar0, BAR_Q_EMPTY + s), WINDOW ? 4 : 1);  // windowed: one arrival per warp
             mbar_init(bar_at(bar0, BAR_S_FULL + s), 1);
             mbar_init(bar_at(bar0, BAR_P_FULL + s), 128);
             mbar_init(bar_at(bar0, BAR_O_FULL + s), 1);
@@ -933,7 +891,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_c
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(bar_at(bar0, BAR_K_FULL + i), 1);
             mbar_init(bar_at(bar0, BAR_K_ROT + i), 128);
-            mbar_init(bar_at(bar0, BAR_K_EMPTY + i), 1);
+            mbar_init(bar_at(bar0, BAR_K_EMPTY + i), WINDOW ? 8 : 1);  // windowed: per warp of both stages
         }
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(bar_at(bar0, BAR_V_FULL + i), 1);
@@ -972,7 +930,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) attn_fwd_kernel(const __grid_c
             if (lane == 0) producer_role<D, WINDOW>(p, CAUSAL, sm, bar0, t_begin, t_end, ctl);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            mma_role<D, ROPE, WINDOW>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);  // the whole warp
+            if constexpr (issue_one_thread<WINDOW>()) {
+                if (lane == 0) mma_role<D, ROPE, WINDOW>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);
+                __syncwarp();
+            } else {
+                mma_role<D, ROPE, WINDOW>(p, CAUSAL, sm, bar0, tmem, t_begin, t_end, ctl);  // the whole warp
+            }
         }
     }
 

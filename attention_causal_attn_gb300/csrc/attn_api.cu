@@ -286,7 +286,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
         sched = *se;
         prm.status = g_dev[dev].status;
     }
-    if (!encode_operands(&prm, q, k, v, o, B, S, Hq, Hkv, D))
+    if (!encode_operands(&prm, q, k, v, o, B, S, Hq, Hkv, D) ||
+        (window && !encode_bshd(&prm.tm_k16, k, B, S, Hkv, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)))
         return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
     {
         const std::vector<int32_t> w = attn_host::window_widths(D, rope ? rope_base : 10000.0, window ? window_k : 0.0);

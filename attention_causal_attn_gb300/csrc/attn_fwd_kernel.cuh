@@ -78,6 +78,7 @@ struct FwdParams {
     CUtensorMap tm_q;  // [B][S][Hq][D] bf16, box {64, 1, 128, 1}, 128B swizzle
     CUtensorMap tm_k;  // [B][S][Hkv][D]
     CUtensorMap tm_v;
+    CUtensorMap tm_k16; // K again, box {16, 1, 128, 1}, 32-byte swizzle (windowed variant: one 16-channel group per load)
     CUtensorMap tm_o;   // O [B][S][Hq][D] bf16, box {64, 1, 32, 1}, 128B swizzle: one warp's rows of one 64-channel block
     __nv_bfloat16* o;   // [B][S][Hq][D]
     float* lse;         // [B][Hq][S] or null
@@ -173,9 +174,10 @@ __device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int i) { return bar0 +
 //        for every cell); pairs in [.x, .y) are the tile's boundary pairs.
 //
 // Pairs below z are dropped for every cell of the KV tile against every query
-// tile of the unit.  A K=16 MMA step multiplies 16 channels, so the 16-pair
-// blocks below m0 = z / 16 are neither rotated nor multiplied (block m is
-// k-steps m and m + D/32: the pairs' first and second members), and the pairs
+// tile of the unit.  The windowed variant holds K as D/16 groups of 16
+// channels (one K=16 MMA step each, 32-byte swizzle); the 16-pair blocks below
+// m0 = z / 16 are never loaded, rotated nor multiplied (block m is channel
+// groups m and m + D/32: the pairs' first and second members), and the pairs
 // of block m0 below z are zeroed in shared memory by the rotation.
 struct WinTile {
     int z, m0;
@@ -214,12 +216,25 @@ __device__ void producer_issue(const FwdParams& p, bool causal, uint32_t sm, uin
         }
         for (int n = u.nmax; n >= 0; --n) {
             const int ks = kit % kKStages;
+            const WinTile w = WINDOW ? window_tile<D>(p, u, n) : WinTile{0, 0};  // before the wait: load in flight
             if (!mbar_wait(bar_at(bar0, BAR_K_EMPTY + ks), ((kit / kKStages) & 1) ^ 1, ctl, kStatusProducer)) return;
             const uint32_t kb = bar_at(bar0, BAR_K_FULL + ks);
-            mbar_arrive_expect_tx(kb, L::kTileBytes);
-            for (int sub = 0; sub < D / 64; ++sub)
-                tma_load_4d(sm + L::kK + ks * L::kTileBytes + sub * kSubTileBytes, &p.tm_k, kb, sub * 64, u.kvh,
-                            n * kBlockN, u.b);
+            if (WINDOW) {
+                // only the 16-pair blocks with a kept pair: 16 channels x 128 rows = 4 KB per group, two per block
+                constexpr int kBlocks = D / 32;
+                mbar_arrive_expect_tx(kb, static_cast<uint32_t>(2 * (kBlocks - w.m0)) * 4096u);
+                for (int m = w.m0; m < kBlocks; ++m) {
+                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + m * 4096u, &p.tm_k16, kb, 16 * m, u.kvh,
+                                n * kBlockN, u.b);
+                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + (m + kBlocks) * 4096u, &p.tm_k16, kb,
+                                D / 2 + 16 * m, u.kvh, n * kBlockN, u.b);
+                }
+            } else {
+                mbar_arrive_expect_tx(kb, L::kTileBytes);
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_4d(sm + L::kK + ks * L::kTileBytes + sub * kSubTileBytes, &p.tm_k, kb, sub * 64, u.kvh,
+                                n * kBlockN, u.b);
+            }
             ++kit;
             const int vs = vit % kVStages;
             if (!mbar_wait(bar_at(bar0, BAR_V_EMPTY + vs), ((vit / kVStages) & 1) ^ 1, ctl, kStatusProducer)) return;
@@ -253,7 +268,10 @@ __device__ void producer_role(const FwdParams& p, bool causal, uint32_t sm, uint
 // c of row r sits at chunk c ^ (r & 7)).  Pair (r, r + D/2) has both members
 // at the same swizzled offset in column blocks 0 and 1 for D = 128, and in
 // chunks c and c + 4 of the single block for D = 64, so each thread rotates
-// whole pairs from two 16-byte loads.  Input bf16, math fp32, output fp16.
+// whole pairs from two 16-byte loads.  The windowed variant stores K as D/16
+// channel groups of [128 rows][32 B] with the 32-byte swizzle (group g at
+// g * 4 KB; the 16-byte half h of row r sits at half h ^ ((r >> 2) & 1)), so
+// that dropped groups are never loaded.  Input bf16, math fp32, output fp16.
 //
 // Thread t owns chunk c = t / kRows (pairs 8c..8c+7) of rows rr + kRows*i,
 // rr = t % kRows: eight consecutive threads touch eight rows of one chunk,
@@ -313,8 +331,8 @@ __device__ __forceinline__ void cmul2(uint64_t& c, uint64_t& s, uint64_t fc, uin
     c = nc;
 }
 
-// ZERO (windowed variant): pairs below `zero_below` come out as 0.
-template <int D, bool ZERO>
+// LAYOUT_GROUPS: the windowed K layout; pairs below `zero_below` come out as 0.
+template <int D, bool LAYOUT_GROUPS>
 __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts& k, uint64_t (&cb)[4],
                                                  uint64_t (&sb)[4], int t, int zero_below = 0) {
     using G = RopeGeom<D>;
@@ -326,7 +344,11 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
     for (int i = 0; i < G::kIters; ++i) {
         const int row = rr + G::kRows * i;
         uint32_t lo_off, hi_off;
-        if (D == 128) {
+        if (LAYOUT_GROUPS) {
+            const uint32_t half = static_cast<uint32_t>(((c & 1) ^ ((row >> 2) & 1)) << 4);
+            lo_off = static_cast<uint32_t>((c >> 1) * 4096 + row * 32) + half;
+            hi_off = lo_off + static_cast<uint32_t>(G::kChunks / 2 * 4096);
+        } else if (D == 128) {
             lo_off = static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
             hi_off = lo_off + kSubTileBytes;
         } else {
@@ -347,7 +369,7 @@ __device__ __forceinline__ void rope_rotate_tile(uint8_t* tile, const RopeConsts
             f2_unpack(f2_fma(y, cb[q], f2_mul(x, sb[q])), b0, b1);           // y cos + x sin
             lo_out[q] = pack_f16x2(a0, a1);
             hi_out[q] = pack_f16x2(b0, b1);
-            if (ZERO) {  // pairs 8c+2q, 8c+2q+1 below zero_below are dropped
+            if (LAYOUT_GROUPS) {  // pairs 8c+2q, 8c+2q+1 below zero_below are dropped
                 const int pr = 8 * c + 2 * q;
                 const uint32_t keep = (pr >= zero_below ? 0x0000FFFFu : 0u) | (pr + 1 >= zero_below ? 0xFFFF0000u : 0u);
                 lo_out[q] &= keep;
@@ -393,8 +415,8 @@ __device__ void rope_role(const FwdParams& p, bool causal, uint8_t* smg, uint32_
             if (WINDOW) {
                 using G = RopeGeom<D>;
                 const int c = t / G::kRows;
-                // chunk c (pairs 8c..8c+7) is in 16-pair block c / 2; the blocks below m0 are not
-                // multiplied, and the pairs of block m0 below z are zeroed
+                // chunk c (pairs 8c..8c+7) is in 16-pair block c / 2; the blocks below m0 were not
+                // loaded and are not multiplied, and the pairs of block m0 below z are zeroed
                 if (c / 2 >= w.m0) rope_rotate_tile<D, true>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t, w.z);
             } else {
                 rope_rotate_tile<D, false>(smg + L::kK + ks * L::kTileBytes, k, cb, sb, t);
@@ -447,7 +469,8 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
     // operand descriptors, built once; each MMA step only advances the start address
     const uint64_t qdesc0 = sw128_desc(sm + L::kQ, 16u, 1024u);
     const uint64_t qdesc1 = sw128_desc(sm + L::kQ + L::kTileBytes, 16u, 1024u);
-    const uint64_t kdesc0 = sw128_desc(sm + L::kK, 16u, 1024u);
+    // windowed K: one 16-channel group of [128 rows][32 B] per K=16 step, 32-byte swizzle, 8-row atoms 256 B apart
+    const uint64_t kdesc0 = WINDOW ? sw32_desc(sm + L::kK, 256u) : sw128_desc(sm + L::kK, 16u, 1024u);
     const uint64_t vdesc0 = sw128_desc(sm + L::kV, kSubTileBytes, 1024u);
     const uint64_t vdesc1 = sw128_desc(sm + L::kV + L::kTileBytes, kSubTileBytes, 1024u);
     int kit = 0, vit = 0;
@@ -512,8 +535,8 @@ __device__ void mma_role(const FwdParams& p, bool causal, uint32_t sm, uint32_t 
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             if (kk % (D / 32) < m0) continue;
-                            const uint32_t units = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
-                            mma_ss(tS, desc_advance(qdesc, units), desc_advance(kdesc, units), kIdescQK, acc);
+                            const uint32_t qunits = (kk / 4) * (kSubTileBytes >> 4) + (kk % 4) * 2u;
+                            mma_ss(tS, desc_advance(qdesc, qunits), desc_advance(kdesc, kk * 256u), kIdescQK, acc);
                             acc = 1u;
                         }
                     } else {
@@ -666,16 +689,18 @@ __device__ __noinline__ void window_correct(uint32_t tS, const uint8_t* qtile, c
                                     (dx % 8) * 2);
             const float qy = f16_at(qtile + (dy / 64) * kSubTileBytes + t * 128 + ((((dy % 64) / 8) ^ (t & 7)) << 4) +
                                     (dy % 8) * 2);
-            // K as Q: channel d of key row j at (d/64)*kSubTileBytes + j*128 + ((((d%64)/8) ^ (j&7)) << 4)
-            // + (d%8)*2; cc is a multiple of 8, so the swizzle of key cc + j is j & 7
-            const uint8_t* kx = ktile + (dx / 64) * kSubTileBytes + (dx % 8) * 2 + cc * 128;
-            const uint8_t* ky = ktile + (dy / 64) * kSubTileBytes + (dy % 8) * 2 + cc * 128;
-            const int hx = (dx % 64) / 8, hy = (dy % 64) / 8;
+            // K in 16-channel groups with the 32-byte swizzle: channel d of key row j at
+            // (d/16)*4096 + j*32 + ((((d%16)/8) ^ ((j>>2)&1)) << 4) + (d%8)*2; cc is a multiple of 8,
+            // so the swizzle bit of key cc + j is (j >> 2) & 1
+            const uint8_t* kx = ktile + (dx / 16) * 4096 + (dx % 8) * 2 + cc * 32;
+            const uint8_t* ky = ktile + (dy / 16) * 4096 + (dy % 8) * 2 + cc * 32;
+            const int hx = ((dx % 16) / 8) << 4, hy = ((dy % 16) / 8) << 4;
             float kxv[32], kyv[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                kxv[j] = f16_at(kx + j * 128 + ((hx ^ (j & 7)) << 4));
-                kyv[j] = f16_at(ky + j * 128 + ((hy ^ (j & 7)) << 4));
+                const int sw = ((j >> 2) & 1) << 4;
+                kxv[j] = f16_at(kx + j * 32 + (hx ^ sw));
+                kyv[j] = f16_at(ky + j * 32 + (hy ^ sw));
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {

@@ -234,6 +234,19 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// Shared-memory matrix descriptor for a K-major operand with the 32-byte
+// swizzle: rows of 32 bytes (one K=16 step of 16-bit data), 8-row atoms of
+// 256 bytes; SBO = stride between 8-row groups (LBO is not used).
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(6) << 61;  // layout type 6: 32-byte swizzle
+    return d;
+}
+
 // A descriptor moved by `units` x 16 bytes: only the 14-bit start-address
 // field changes (callers keep the sum below 2^14, i.e. inside shared memory).
 __device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t units) {

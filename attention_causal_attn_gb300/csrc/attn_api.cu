@@ -835,6 +835,12 @@ extern "C" int attn_decode(const void* q, const void* k, const void* v, void* o,
 // Backward ("AttnFuse", sec. 4.4 Backward Pass: row reduction, dK/dV, dQ).
 namespace {
 DecodeScratch g_bwd[kMaxDevices];  // Dlt rows, [B][Hq][S] floats
+// RoPE: Q and K rotated once before the backward's tile kernels (fp16, the layouts of Q and K)
+struct RotScratch {
+    void* buf = nullptr;
+    size_t bytes = 0;
+};
+RotScratch g_bwd_rot[kMaxDevices];
 std::atomic<unsigned> g_bwd_configured[kMaxDevices];  // as DevInfo::configured, for the backward and block-sparse kernels
 
 template <int D, bool CAUSAL, bool ROPE>
@@ -889,6 +895,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     attn::BwdParams bp;
     float2* rope_tab = nullptr;
     float2* split_tab = nullptr;
+    float2* rot_tab = nullptr;  // the rotation pass's tables (128-row blocks)
+    uint8_t* qk_rot = nullptr;  // rotated Q, then rotated K
     float* dlt = nullptr;
     int* mask = nullptr;
     const int nnz = row_ptr != nullptr ? row_ptr[ntiles] : 0;
@@ -898,8 +906,23 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
         int rc = probe_device(dev);
         if (rc != ATTN_OK) return rc;
         if (rope && ((rc = get_rope(dev, S, D, rope_base, &rope_tab)) != ATTN_OK ||
-                     (rc = get_split(dev, S, D, rope_base, 32, &split_tab)) != ATTN_OK))
+                     (rc = get_split(dev, S, D, rope_base, 32, &split_tab)) != ATTN_OK ||
+                     (rc = get_split(dev, S, D, rope_base, 128, &rot_tab)) != ATTN_OK))
             return rc;
+        if (rope) {
+            RotScratch& rs = g_bwd_rot[dev];
+            const size_t need = static_cast<size_t>(B) * S * (Hq + Hkv) * D * 2;
+            if (rs.bytes < need) {
+                if (rs.buf != nullptr) cudaFree(rs.buf);
+                rs.buf = nullptr;
+                rs.bytes = 0;
+                cudaError_t e;
+                if ((e = cudaMalloc(&rs.buf, need)) != cudaSuccess)
+                    return cuda_fail("cudaMalloc(backward rotated Q, K)", e, ATTN_ERR_OOM);
+                rs.bytes = need;
+            }
+            qk_rot = static_cast<uint8_t*>(rs.buf);
+        }
         DecodeScratch& ds = g_bwd[dev];
         if (ds.floats < rows) {
             if (ds.buf != nullptr) cudaFree(ds.buf);
@@ -914,9 +937,15 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
         if (row_ptr != nullptr && (rc = get_mask(dev, row_ptr, col_idx, ntiles, &mask)) != ATTN_OK) return rc;
         bp.f.status = g_dev[dev].status;
     }
-    if (!encode_bshd(&bp.f.tm_q, q, B, S, Hq, D) || !encode_bshd(&bp.f.tm_k, k, B, S, Hkv, D) ||
+    // With RoPE the tile kernels read Q and K rotated once by the rotation pass (fp16): each Q tile
+    // is used by every key tile of its head and each K tile by every query tile, so rotating
+    // inside the loops would repeat each rotation about S/256 times ("AttnFuse", sec. 5.3).
+    const void* q_in = rope ? static_cast<const void*>(qk_rot) : q;
+    const void* k_in = rope ? static_cast<const void*>(qk_rot + static_cast<size_t>(B) * S * Hq * D * 2) : k;
+    if (!encode_bshd(&bp.f.tm_q, q_in, B, S, Hq, D) || !encode_bshd(&bp.f.tm_k, k_in, B, S, Hkv, D) ||
         !encode_bshd(&bp.f.tm_v, v, B, S, Hkv, D) || !encode_bshd(&bp.tm_do, dO, B, S, Hq, D))
         return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    bp.prerot = rope ? 1 : 0;
     bp.f.rope = rope_tab;
     bp.f.B = B;
     bp.f.Hq = Hq;
@@ -948,6 +977,21 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
                                                                static_cast<const __nv_bfloat16*>(dO), dlt, B, S, Hq);
     cudaError_t e;
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("backward row-reduction launch", e);
+    if (rope) {
+        const float2* row_tab = rot_tab + static_cast<size_t>(ntiles) * (D / 2);
+        for (int which = 0; which < 2; ++which) {
+            const int H = which ? Hkv : Hq;
+            const long long nrows = static_cast<long long>(B) * S * H;
+            const unsigned blocks = static_cast<unsigned>((nrows * (D / 16) + 255) / 256);
+            const uint4* src = static_cast<const uint4*>(which ? k : q);
+            uint4* dst = reinterpret_cast<uint4*>(const_cast<void*>(which ? k_in : q_in));
+            if (D == 128)
+                attn::rope_rotate_kernel<128><<<blocks, 256, 0, st>>>(src, dst, rot_tab, row_tab, nrows, S, H);
+            else
+                attn::rope_rotate_kernel<64><<<blocks, 256, 0, st>>>(src, dst, rot_tab, row_tab, nrows, S, H);
+            if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("backward rotation launch", e);
+        }
+    }
     if (D == 128) {
         if (causal) return rope ? launch_bwd<128, true, true>(bp, dev, ntiles, st) : launch_bwd<128, true, false>(bp, dev, ntiles, st);
         return rope ? launch_bwd<128, false, true>(bp, dev, ntiles, st) : launch_bwd<128, false, false>(bp, dev, ntiles, st);
@@ -1327,6 +1371,11 @@ extern "C" void attn_release_cache(void) {
     }
     g_masks.clear();
     for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_bwd_rot[d].buf != nullptr) {
+            cudaSetDevice(d);
+            cudaFree(g_bwd_rot[d].buf);
+            g_bwd_rot[d] = RotScratch();
+        }
         if (g_bwd[d].buf == nullptr) continue;
         cudaSetDevice(d);
         cudaFree(g_bwd[d].buf);

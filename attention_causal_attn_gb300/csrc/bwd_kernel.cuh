@@ -45,6 +45,9 @@ struct BwdParams {
     // CTA order: 1 = a head's tiles together (they share the streamed tiles in L2; dense masks),
     // 0 = tile by tile across heads (a mask's heavy rows or columns first)
     int head_major;
+    // RoPE: 1 = tm_q and tm_k hold Q and K already rotated (fp16, one rotation pass before the
+    // kernels), so no tile is rotated inside the loops; 0 = the RoPE warps rotate each tile
+    int prerot;
 };
 
 // (tile, batch-head) of CTA x among bh batch-heads x ntiles tiles, in the order p.head_major picks.
@@ -114,8 +117,10 @@ enum : int {
     BB_STR_FULL,      // [2] streamed tiles landed
     BB_STR_ROT = BB_STR_FULL + 2,    // [2] streamed RoPE tile rotated
     BB_STR_EMPTY = BB_STR_ROT + 2,   // [2] the MMAs reading the stage are done
-    BB_S_FULL = BB_STR_EMPTY + 2,    // S and dP of the iteration in TMEM
-    BB_P_FULL,        // P and dS written to TMEM
+    BB_S_FULL = BB_STR_EMPTY + 2,    // S (dQ kernel: and dP) of the iteration in TMEM
+    BB_P_FULL,        // P written to TMEM (dQ kernel: P and dS)
+    BB_DP_FULL,       // dK/dV kernel: dP of the iteration in TMEM
+    BB_DS_FULL,       // dK/dV kernel: dS written to TMEM
     BB_ACC_FULL,      // last accumulation done
     BB_DRAIN,
     BB_NUM
@@ -178,38 +183,49 @@ __device__ __forceinline__ void bwd_store_row(const BwdParams& p, uint32_t taddr
     }
 }
 
-// dK/dV kernel, one thread per key row and half of the columns (64 queries from tS, tdP): P^T =
-// exp2(S^T c - LSE2_col) (0 where the query is before the key) and dS^T = P^T (dP^T - Dlt_col),
-// 32 columns at a time; P^T (bf16) overwrites the half's S^T columns and dS^T (fp16 after RoPE,
-// else bf16) its dP^T columns, two per column, never a column still to be read.  Column c is
-// query q0 + c; c < lim is masked.
-template <bool ROPE, bool MASKED>
-__device__ __forceinline__ void bwd_ew_cols(uint32_t tS, uint32_t tdP, const float* ls, const float* dl, float c,
-                                            int lim) {
+// The dK/dV kernel's elementwise work in two phases, so that each overlaps tensor-core work:
+// the P phase needs only S^T, the dS phase only dP^T and P.  P phase: P^T = exp2(S^T c -
+// LSE2_col) (0 where the query is before the key), packed to bf16 over the half's S^T columns
+// (for dV) and kept in pp (for dS: the next S^T overwrites those columns meanwhile).
+template <bool MASKED>
+__device__ __forceinline__ void bwd_ew_p(uint32_t tS, const float* ls, float c, int lim, uint32_t (&pp)[32]) {
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t rs[32], rd[32];
-        tmem_load_32_async(tS + cc, rs);  // both loads in flight, one wait
-        tmem_load_32_async(tdP + cc, rd);
-        tmem_wait_ld_32(rs);
-        tmem_wait_ld_32(rd);
-        uint32_t pp[16], pd[16];
+        uint32_t rs[32];
+        tmem_load_32(tS + cc, rs);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
             const float2 l2 = *reinterpret_cast<const float2*>(ls + cc + e);
-            const float2 d2 = *reinterpret_cast<const float2*>(dl + cc + e);
             float p0 = ex2_approx(__uint_as_float(rs[e]) * c - l2.x);
             float p1 = ex2_approx(__uint_as_float(rs[e + 1]) * c - l2.y);
             if (MASKED) {
                 if (cc + e < lim) p0 = 0.f;
                 if (cc + e + 1 < lim) p1 = 0.f;
             }
-            const float s0 = p0 * (__uint_as_float(rd[e]) - d2.x);
-            const float s1 = p1 * (__uint_as_float(rd[e + 1]) - d2.y);
-            pp[e / 2] = pack_bf16x2(p0, p1);
+            pp[(cc + e) / 2] = pack_bf16x2(p0, p1);
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pp[cc / 2 + e];
+        tmem_store_16(tS + cc / 2, pk);
+    }
+}
+// dS phase: dS^T = P^T (dP^T - Dlt_col) from the bf16 P^T of the P phase (the value dV
+// accumulates), fp16 after RoPE, else bf16, over the half's dP^T columns.
+template <bool ROPE>
+__device__ __forceinline__ void bwd_ew_ds(uint32_t tdP, const float* dl, const uint32_t (&pp)[32]) {
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t rd[32];
+        tmem_load_32(tdP + cc, rd);
+        uint32_t pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const float2 d2 = *reinterpret_cast<const float2*>(dl + cc + e);
+            const float s0 = bf16_lo(pp[(cc + e) / 2]) * (__uint_as_float(rd[e]) - d2.x);
+            const float s1 = bf16_hi(pp[(cc + e) / 2]) * (__uint_as_float(rd[e + 1]) - d2.y);
             pd[e / 2] = ROPE ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
         }
-        tmem_store_16(tS + cc / 2, pp);
         tmem_store_16(tdP + cc / 2, pd);
     }
 }
@@ -278,6 +294,8 @@ __device__ __forceinline__ void bwd_init_bars(uint32_t bar0) {
     }
     mbar_init(bar_at(bar0, BB_S_FULL), 1);
     mbar_init(bar_at(bar0, BB_P_FULL), kBwdEw);
+    mbar_init(bar_at(bar0, BB_DP_FULL), 1);
+    mbar_init(bar_at(bar0, BB_DS_FULL), kBwdEw);
     mbar_init(bar_at(bar0, BB_ACC_FULL), 1);
     mbar_init(bar_at(bar0, BB_DRAIN), 1);
     fence_barrier_init();
@@ -350,13 +368,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             const float* ls = reinterpret_cast<const float*>(smg + L::kRows + s * 1024) + 64 * half;
             const int lim = kv0 + t - (q0 + 64 * half);  // query columns c < lim precede the key
             const uint32_t hS = tS + 64u * half, hdP = tdP + 64u * half;
+            uint32_t pp[32];
             if (CAUSAL && __any_sync(0xffffffffu, lim > 0))
-                bwd_ew_cols<ROPE, true>(hS, hdP, ls, ls + 128, c, lim);
+                bwd_ew_p<true>(hS, ls, c, lim, pp);
             else
-                bwd_ew_cols<ROPE, false>(hS, hdP, ls, ls + 128, c, lim);
+                bwd_ew_p<false>(hS, ls, c, lim, pp);
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
+            ok = bwd_wait(bar_at(bar0, BB_DP_FULL), it & 1, ctl, kStatusSoftmax);
+            if (!ok) break;
+            tc_fence_after();
+            bwd_ew_ds<ROPE>(hdP, ls + 128, pp);
+            tmem_store_wait();
+            tc_fence_before();
+            mbar_arrive(bar_at(bar0, BB_DS_FULL));
         }
         const bool none = iters == 0;  // no listed query tile: dK = dV = 0
         if (ok && (none || bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax))) {
@@ -371,7 +397,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         }
     } else if (warp < kBwdWarpTma) {
         // ---- RoPE warps: the resident K tile once, then each streamed Q tile
-        if (ROPE) {
+        if (ROPE && !p.prerot) {
             const int t = threadIdx.x - kBwdWarpRope * 32;
             RopeConsts k;
             rope_load_consts<D>(f, t, k);
@@ -458,42 +484,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         const uint32_t tS = tmem, tdP = tmem + 128u, tdV = tmem + 256u, tdK = tmem + 256u + D;
         const uint64_t kdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
         const uint64_t vdesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
-        bool ok = mbar_wait_warp(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
-        for (int it = 0; it < iters && ok; ++it) {
+        // Issue order dV(i), S^T(i+1), dK(i), dP^T(i+1): the elementwise warps turn dP^T(i) into
+        // dS^T(i) while dV(i) and S^T(i+1) run, and S^T(i+1) into P^T(i+1) while dK(i) and
+        // dP^T(i+1) run.  S^T(i+1) overwrites the columns of P^T(i) after dV(i) has read them,
+        // dP^T(i+1) those of dS^T(i) after dK(i).
+        auto stage_a = [&](int it) { return sm + L::kStr0 + (it & 1) * 2 * L::kTile; };  // Q; dO follows
+        auto issue_s = [&](int it) -> bool {  // the stage's tiles, its rotated Q, then S^T = K Q^T
             const int s = it & 1, n = it >> 1;
-            ok = mbar_wait_warp(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t qa = sm + L::kStr0 + s * 2 * L::kTile, da = qa + L::kTile;
-            const uint64_t qdesc = sw128_desc(qa, 16u, 1024u), ddesc = sw128_desc(da, 16u, 1024u);
-            // dP^T needs no rotated operand: it runs while the RoPE warps finish Q
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                umma_ss(tdP, desc_advance(vdesc, kmajor_units(kk)), desc_advance(ddesc, kmajor_units(kk)), kIdescDP,
-                        kk > 0 ? 1u : 0u);
-            if (ROPE) {
-                if (it == 0) ok = mbar_wait_warp(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
-                if (ok) ok = mbar_wait_warp(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
-                if (!ok) break;
-                tc_fence_after();
+            if (!mbar_wait_warp(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma)) return false;
+            if (ROPE && !p.prerot) {
+                if (it == 0 && !mbar_wait_warp(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma)) return false;
+                if (!mbar_wait_warp(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma)) return false;
             }
+            tc_fence_after();
+            const uint64_t qdesc = sw128_desc(stage_a(it), 16u, 1024u);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 umma_ss(tS, desc_advance(kdesc, kmajor_units(kk)), desc_advance(qdesc, kmajor_units(kk)), kIdescS,
                         kk > 0 ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_S_FULL));
+            return true;
+        };
+        auto issue_dp = [&](int it) {  // dP^T = V dO^T (the stage's tiles were waited for by issue_s)
+            const uint64_t ddesc = sw128_desc(stage_a(it) + L::kTile, 16u, 1024u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tdP, desc_advance(vdesc, kmajor_units(kk)), desc_advance(ddesc, kmajor_units(kk)), kIdescDP,
+                        kk > 0 ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_DP_FULL));
+        };
+        bool ok = mbar_wait_warp(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
+        if (ok && iters > 0) {
+            ok = issue_s(0);
+            if (ok) issue_dp(0);
+        }
+        for (int it = 0; it < iters && ok; ++it) {
+            const int s = it & 1;
+            const uint32_t qa = stage_a(it), da = qa + L::kTile;
+            const uint64_t dmn = sw128_desc(da, kSubTileBytes, 1024u), qmn = sw128_desc(qa, kSubTileBytes, 1024u);
             ok = mbar_wait_warp(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
             if (!ok) break;
             tc_fence_after();
-            const uint64_t dmn = sw128_desc(da, kSubTileBytes, 1024u), qmn = sw128_desc(qa, kSubTileBytes, 1024u);
             // 16 queries per k-step: 2048 bytes of the tile, 8 TMEM columns of P^T / dS^T
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 umma_ts(tdV, tS + packed_col(kk), desc_advance(dmn, kk * 128u), kIdescDV, (it > 0 || kk > 0) ? 1u : 0u);
+            if (it + 1 < iters && !(ok = issue_s(it + 1))) break;
+            ok = mbar_wait_warp(bar_at(bar0, BB_DS_FULL), it & 1, ctl, kStatusMma);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 umma_ts(tdK, tdP + packed_col(kk), desc_advance(qmn, kk * 128u), kIdescDK, (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
+            if (it + 1 < iters) issue_dp(it + 1);
         }
         if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));
         bwd_drain(bar0, ctl);
@@ -590,7 +634,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         }
     } else if (warp < kBwdWarpTma) {
         // ---- RoPE warps: the resident Q tile once, then each streamed K tile
-        if (ROPE) {
+        if (ROPE && !p.prerot) {
             const int t = threadIdx.x - kBwdWarpRope * 32;
             RopeConsts k;
             rope_load_consts<D>(f, t, k);
@@ -662,7 +706,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             for (int kk = 0; kk < D / 16; ++kk)
                 umma_ss(tdP, desc_advance(ddesc, kmajor_units(kk)), desc_advance(vdesc, kmajor_units(kk)), kIdescDP,
                         kk > 0 ? 1u : 0u);
-            if (ROPE) {
+            if (ROPE && !p.prerot) {
                 if (it == 0) ok = mbar_wait_warp(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
                 if (ok) ok = mbar_wait_warp(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
                 if (!ok) break;

@@ -13,12 +13,15 @@
 //   dQ_i  = R(i)^T dQ'_i,  dK_j = R(j)^T dK'_j  (the rotation run backwards)
 //
 // Both tile kernels follow the forward's GB300 structure: TMA loads into
-// 128-byte-swizzled shared memory, the RoPE warps rotate tiles in place, one
-// thread issues tcgen05 MMAs into TMEM, and one warpgroup (one thread per
-// TMEM lane) turns S and dP into P and dS in TMEM, which the next MMAs read
-// as their A operand.  Two warpgroups share that work, one per half of the
-// 128 columns, each writing its packed P / dS inside its own half.  Every
-// wait is bounded.
+// 128-byte-swizzled shared memory, one converged warp issues tcgen05 MMAs
+// into TMEM, and the elementwise warps (one thread per TMEM lane) turn S and
+// dP into P and dS in TMEM, which the next MMAs read as their A operand.  Two
+// warpgroups share that work, one per half of the 128 columns, each writing
+// its packed P / dS inside its own half.  The elementwise work runs in two
+// phases (P from S, then dS from dP and P), so each phase overlaps the tensor
+// cores' next products (see the MMA issuers).  With RoPE, Q and K arrive
+// rotated once by the rotation pass (prerot); the RoPE warps rotate tiles in
+// place only when they do not.  Every wait is bounded.
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -117,10 +120,10 @@ enum : int {
     BB_STR_FULL,      // [2] streamed tiles landed
     BB_STR_ROT = BB_STR_FULL + 2,    // [2] streamed RoPE tile rotated
     BB_STR_EMPTY = BB_STR_ROT + 2,   // [2] the MMAs reading the stage are done
-    BB_S_FULL = BB_STR_EMPTY + 2,    // S (dQ kernel: and dP) of the iteration in TMEM
-    BB_P_FULL,        // P written to TMEM (dQ kernel: P and dS)
-    BB_DP_FULL,       // dK/dV kernel: dP of the iteration in TMEM
-    BB_DS_FULL,       // dK/dV kernel: dS written to TMEM
+    BB_S_FULL = BB_STR_EMPTY + 2,    // S of the iteration in TMEM
+    BB_P_FULL,        // P formed (dK/dV kernel: written to TMEM; dQ kernel: S read)
+    BB_DP_FULL,       // dP of the iteration in TMEM
+    BB_DS_FULL,       // dS written to TMEM
     BB_ACC_FULL,      // last accumulation done
     BB_DRAIN,
     BB_NUM
@@ -230,19 +233,15 @@ __device__ __forceinline__ void bwd_ew_ds(uint32_t tdP, const float* dl, const u
     }
 }
 
-// dQ kernel, one thread per query row and half of the columns (64 keys): dS = P (dP - Dlt_row)
-// with P = exp2(S c - LSE2_row), 0 for keys after the query (columns c > lim); dS overwrites the
-// half's dP columns.
-template <bool ROPE, bool MASKED>
-__device__ __forceinline__ void bwd_ew_row(uint32_t tS, uint32_t tdP, float l2, float dl, float c, int lim) {
+// The dQ kernel's elementwise work in the same two phases, one thread per query row and half of
+// the columns (64 keys).  P phase: P = exp2(S c - LSE2_row), 0 for keys after the query (columns
+// c > lim), kept in pp as bf16 (the P of the dK/dV kernel's dS, so both kernels form one dS).
+template <bool MASKED>
+__device__ __forceinline__ void bwd_ew_p_row(uint32_t tS, float l2, float c, int lim, uint32_t (&pp)[32]) {
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t rs[32], rd[32];
-        tmem_load_32_async(tS + cc, rs);  // both loads in flight, one wait
-        tmem_load_32_async(tdP + cc, rd);
-        tmem_wait_ld_32(rs);
-        tmem_wait_ld_32(rd);
-        uint32_t pd[16];
+        uint32_t rs[32];
+        tmem_load_32(tS + cc, rs);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
             float p0 = ex2_approx(__uint_as_float(rs[e]) * c - l2);
@@ -251,8 +250,22 @@ __device__ __forceinline__ void bwd_ew_row(uint32_t tS, uint32_t tdP, float l2, 
                 if (cc + e > lim) p0 = 0.f;
                 if (cc + e + 1 > lim) p1 = 0.f;
             }
-            const float s0 = p0 * (__uint_as_float(rd[e]) - dl);
-            const float s1 = p1 * (__uint_as_float(rd[e + 1]) - dl);
+            pp[(cc + e) / 2] = pack_bf16x2(p0, p1);
+        }
+    }
+}
+// dS phase: dS = P (dP - Dlt_row) over the half's dP columns (fp16 after RoPE, else bf16).
+template <bool ROPE>
+__device__ __forceinline__ void bwd_ew_ds_row(uint32_t tdP, float dl, const uint32_t (&pp)[32]) {
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t rd[32];
+        tmem_load_32(tdP + cc, rd);
+        uint32_t pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const float s0 = bf16_lo(pp[(cc + e) / 2]) * (__uint_as_float(rd[e]) - dl);
+            const float s1 = bf16_hi(pp[(cc + e) / 2]) * (__uint_as_float(rd[e + 1]) - dl);
             pd[e / 2] = ROPE ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
         }
         tmem_store_16(tdP + cc / 2, pd);
@@ -614,13 +627,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             tc_fence_after();
             const int lim = q0 + t - (ktile(it) * 128 + 64 * half);  // key columns c > lim follow the query
             const uint32_t hS = tS + 64u * half, hdP = tdP + 64u * half;
+            uint32_t pp[32];
             if (CAUSAL && __any_sync(0xffffffffu, lim < 63))
-                bwd_ew_row<ROPE, true>(hS, hdP, l2, dl, c, lim);
+                bwd_ew_p_row<true>(hS, l2, c, lim, pp);
             else
-                bwd_ew_row<ROPE, false>(hS, hdP, l2, dl, c, lim);
+                bwd_ew_p_row<false>(hS, l2, c, lim, pp);
+            tc_fence_before();
+            mbar_arrive(bar_at(bar0, BB_P_FULL));  // S is read: the next S may overwrite it
+            ok = bwd_wait(bar_at(bar0, BB_DP_FULL), it & 1, ctl, kStatusSoftmax);
+            if (!ok) break;
+            tc_fence_after();
+            bwd_ew_ds_row<ROPE>(hdP, dl, pp);
             tmem_store_wait();
             tc_fence_before();
-            mbar_arrive(bar_at(bar0, BB_P_FULL));
+            mbar_arrive(bar_at(bar0, BB_DS_FULL));
         }
         const bool none = iters == 0;  // no listed key tile: dQ = 0
         if (ok && (none || bwd_wait(bar_at(bar0, BB_ACC_FULL), 0, ctl, kStatusSoftmax))) {
@@ -693,39 +713,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         const uint32_t tS = tmem, tdP = tmem + 128u, tdQ = tmem + 256u;
         const uint64_t qdesc = sw128_desc(sm + L::kRes0, 16u, 1024u);
         const uint64_t ddesc = sw128_desc(sm + L::kRes1, 16u, 1024u);
-        bool ok = mbar_wait_warp(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
-        for (int it = 0; it < iters && ok; ++it) {
+        // Issue order S(j+1), dQ(j), dP(j+1): the elementwise warps form dS(j) while S(j+1) runs and
+        // P(j+1) while dQ(j) and dP(j+1) run.  S(j+1) overwrites S(j) once P(j) is in registers,
+        // dP(j+1) overwrites dS(j) after dQ(j) has read it.
+        auto stage_a = [&](int it) { return sm + L::kStr0 + (it & 1) * 2 * L::kTile; };  // K; V follows
+        auto issue_s = [&](int it) -> bool {  // the stage's tiles, its rotated K, then S = Q K^T
             const int s = it & 1, n = it >> 1;
-            ok = mbar_wait_warp(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t ka = sm + L::kStr0 + s * 2 * L::kTile, va = ka + L::kTile;
-            const uint64_t kdesc = sw128_desc(ka, 16u, 1024u), vdesc = sw128_desc(va, 16u, 1024u);
-            // dP needs no rotated operand: it runs while the RoPE warps finish K
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                umma_ss(tdP, desc_advance(ddesc, kmajor_units(kk)), desc_advance(vdesc, kmajor_units(kk)), kIdescDP,
-                        kk > 0 ? 1u : 0u);
+            if (!mbar_wait_warp(bar_at(bar0, BB_STR_FULL + s), n & 1, ctl, kStatusMma)) return false;
             if (ROPE && !p.prerot) {
-                if (it == 0) ok = mbar_wait_warp(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma);
-                if (ok) ok = mbar_wait_warp(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma);
-                if (!ok) break;
-                tc_fence_after();
+                if (it == 0 && !mbar_wait_warp(bar_at(bar0, BB_RES_ROT), 0, ctl, kStatusMma)) return false;
+                if (!mbar_wait_warp(bar_at(bar0, BB_STR_ROT + s), n & 1, ctl, kStatusMma)) return false;
             }
+            tc_fence_after();
+            const uint64_t kdesc = sw128_desc(stage_a(it), 16u, 1024u);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
                         kk > 0 ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_S_FULL));
+            return true;
+        };
+        auto issue_dp = [&](int it) {  // dP = dO V^T (the stage's tiles were waited for by issue_s)
+            const uint64_t vdesc = sw128_desc(stage_a(it) + L::kTile, 16u, 1024u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tdP, desc_advance(ddesc, kmajor_units(kk)), desc_advance(vdesc, kmajor_units(kk)), kIdescDP,
+                        kk > 0 ? 1u : 0u);
+            tc_commit(bar_at(bar0, BB_DP_FULL));
+        };
+        bool ok = mbar_wait_warp(bar_at(bar0, BB_RES_FULL), 0, ctl, kStatusMma);
+        if (ok && iters > 0) {
+            ok = issue_s(0);
+            if (ok) issue_dp(0);
+        }
+        for (int it = 0; it < iters && ok; ++it) {
+            const int s = it & 1;
             ok = mbar_wait_warp(bar_at(bar0, BB_P_FULL), it & 1, ctl, kStatusMma);
             if (!ok) break;
+            if (it + 1 < iters && !(ok = issue_s(it + 1))) break;
+            ok = mbar_wait_warp(bar_at(bar0, BB_DS_FULL), it & 1, ctl, kStatusMma);
+            if (!ok) break;
             tc_fence_after();
-            const uint64_t kmn = sw128_desc(ka, kSubTileBytes, 1024u);
+            const uint64_t kmn = sw128_desc(stage_a(it), kSubTileBytes, 1024u);
             // 16 keys per k-step: 2048 bytes of K, 8 TMEM columns of dS
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 umma_ts(tdQ, tdP + packed_col(kk), desc_advance(kmn, kk * 128u), kIdescDQ, (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar_at(bar0, BB_STR_EMPTY + s));
+            if (it + 1 < iters) issue_dp(it + 1);
         }
         if (ok) tc_commit(bar_at(bar0, BB_ACC_FULL));
         bwd_drain(bar0, ctl);

@@ -230,10 +230,14 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
  *            (a KV head's gradients sum over its query heads).
  *   B, Hq, Hkv, S, D, causal, rope_base   as attn_fwd; the window is not
  *            supported here.
- * dS = P (dP - dO.O) is rounded to fp16 for the products with the rotated
- * fp16 Q and K (bf16 without RoPE), P to bf16 for dV; accumulation in fp32.
+ * P is rounded to bf16 (for dV, and as the P of dS = P (dP - dO.O)); dS is
+ * rounded to fp16 for the products with the rotated fp16 Q and K (bf16
+ * without RoPE); accumulation in fp32.  With RoPE, Q and K are rotated once
+ * by the rotation pass (as attn_rope_rotate) into library-owned fp16 buffers
+ * before the tile kernels, which then rotate nothing inside their loops.
  * Asynchronous on `stream`.  The library keeps a scratch of B*Hq*S floats
- * (dO.O per row) and the rotation tables until attn_release_cache().
+ * (dO.O per row), with RoPE B*S*(Hq+Hkv)*D fp16 values (the rotated Q and
+ * K), and the rotation tables until attn_release_cache().
  * Errors: as attn_fwd (ATTN_ERR_NULL also for dO, lse, dq, dk, dv).
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

@@ -37,8 +37,13 @@
 // scores stay raw in TMEM; with c = log2(e)/sqrt(D), P = exp2(S*c - m*c),
 // l = alpha*l + rowsum(P), O = alpha*O + P V, alpha = exp2((m_old - m_new)*c).
 // The running max used for P is only moved (and O, l rescaled) when the true
-// row max exceeds it by more than 8 in log2 units; P then stays below 2^8 and
-// the final O/l and LSE = ln2*(m*c + log2 l) are unchanged up to rounding.
+// row max exceeds it by more than 16 in log2 units; P then stays below 2^16 and
+// the final O/l and LSE = ln2*(m*c + log2 l) are unchanged up to rounding (P is
+// bf16 and l, O accumulate in fp32, all with fp32's exponent range, so the
+// bound only has to keep l * max|V| * S far below 2^128).
+// That test is made per 32-key chunk with the maximum that tcgen05.ld.red
+// (sm_103a) returns along with the chunk's scores, so each S tile is read from
+// TMEM once: no separate max pass.
 // One thread owns one query row (TMEM lane), so the row sums need no
 // cross-lane reduction at all.
 #pragma once
@@ -65,7 +70,7 @@ constexpr uint32_t kRegsSoftmax = 152, kRegsRope = 120, kRegsOther = 88;
 static_assert(128 * (2 * kRegsSoftmax + kRegsRope + kRegsOther) <= kNumThreads * 128, "register split");
 constexpr uint32_t kSubTileBytes = 128u * 128u;  // 128 rows x 128 B: one 64-wide bf16 column block
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleThreshold = 16.0f;  // log2 units
 
 // status word bits (OR-ed by the CTA whose wait ran out)
 constexpr int kStatusProducer = 1, kStatusRope = 2, kStatusMma = 4, kStatusSoftmax = 8, kStatusDrain = 16;
@@ -660,6 +665,104 @@ __device__ __forceinline__ float tile_exp_to_p(uint32_t taddr, int limit, float 
     return s0 + s1;
 }
 
+// Rare path of tile_exp_online, after the tile's P is formed: O_s's row is
+// multiplied by alpha (unless with_o is false: on the unit's first tile O_s
+// holds nothing yet) and the P of the tile's first three 32-key chunks (bf16
+// pairs in columns [16k, 16k+16)) by fac[k] (all 1 for rows whose maximum
+// stayed).  Called by the whole warp.
+template <int D>
+__device__ __forceinline__ void rescale_o_and_p(uint32_t tO, uint32_t tS, float alpha, float fac0, float fac1,
+                                                float fac2, bool with_o) {
+    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+    for (int oc = 0; oc < (with_o ? D : 0); oc += 32) {
+        uint32_t r[32];
+        tmem_load_32(tO + oc, r);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2), x0, x1);
+            r[j] = __float_as_uint(x0);
+            r[j + 1] = __float_as_uint(x1);
+        }
+        tmem_store_32(tO + oc, r);
+    }
+    tmem_store_wait();  // the P stores have landed before they are read back
+#pragma unroll 1
+    for (int k = 0; k < 3; ++k) {
+        const float f = k == 0 ? fac0 : (k == 1 ? fac1 : fac2);
+        const uint64_t f2 = f2_pack(f, f);
+        uint32_t r[16];
+        tmem_load_16(tS + 16 * k, r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r[j]));
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(x.x, x.y), f2), x0, x1);
+            r[j] = pack_bf16x2(x0, x1);
+        }
+        tmem_store_16(tS + 16 * k, r);
+    }
+}
+
+// One pass over a tile: P is formed against the running maximum m_used, and
+// each 32-key chunk's maximum comes with its load (tcgen05.ld.red; on the
+// masked tiles, the diagonal and the ragged last one, recomputed from the
+// visible keys), so no separate max pass is needed.  A chunk whose maximum
+// exceeds m_used by more than the rescale threshold moves m_used there before
+// its own P is formed (l and the tile's partial sum rescaled at once); O_s and
+// the P of the tile's earlier chunks are rescaled after the tile, by the
+// product of the factors that apply to each.  The unit's first chunk only sets
+// m_used (nothing is accumulated yet).  Keys [0, limit) are visible to this row;
+// `first` marks the unit's first tile.
+template <int D, bool MASKED>
+__device__ __forceinline__ void tile_exp_online(uint32_t tS, uint32_t tO, float c, int limit, bool first,
+                                                float& m_used, float& l) {
+    static_assert(kBlockN == 128, "four 32-key chunks");
+    const uint64_t c2 = f2_pack(c, c);
+    uint64_t nmc2 = f2_pack(-m_used * c, -m_used * c);
+    uint64_t sum2 = f2_pack(0.f, 0.f);
+    float alpha_all = 1.f, fac0 = 1.f, fac1 = 1.f, fac2 = 1.f;
+    bool moved = false;
+    auto step = [&](const uint32_t (&r)[32], float cm, int k) {
+        if (MASKED && 32 * k + 31 >= limit) cm = row_max32<true>(r, 32 * k, limit, -INFINITY);
+        if ((cm - m_used) * c > kRescaleThreshold) {
+            if (m_used != -INFINITY) {
+                const float alpha = ex2_approx((m_used - cm) * c);
+                l *= alpha;
+                sum2 = f2_mul(sum2, f2_pack(alpha, alpha));
+                alpha_all *= alpha;
+                if (k > 0) fac0 *= alpha;
+                if (k > 1) fac1 *= alpha;
+                if (k > 2) fac2 *= alpha;
+                moved = true;
+            }
+            m_used = cm;
+            nmc2 = f2_pack(-m_used * c, -m_used * c);
+        }
+        uint32_t pk[16];
+        exp_pack32<MASKED>(r, 32 * k, limit, c2, nmc2, sum2, pk);
+        tmem_store_16(tS + 16 * k, pk);  // keys 32k.. to columns 16k..: never a column still to be read
+    };
+    uint32_t a[32], b[32];
+    float ma, mb;
+    tmem_load_32_max(tS, a, ma);
+    tmem_load_32_max_async(tS + 32, b, mb);
+    step(a, ma, 0);
+    tmem_wait_ld_32_max(b, mb);
+    tmem_load_32_max_async(tS + 64, a, ma);
+    step(b, mb, 1);
+    tmem_wait_ld_32_max(a, ma);
+    tmem_load_32_max_async(tS + 96, b, mb);
+    step(a, ma, 2);
+    tmem_wait_ld_32_max(b, mb);
+    step(b, mb, 3);
+    float s0, s1;
+    f2_unpack(sum2, s0, s1);
+    l += s0 + s1;
+    if (__any_sync(0xffffffffu, moved)) rescale_o_and_p<D>(tO, tS, alpha_all, fac0, fac1, fac2, !first);
+}
+
 // Windowed variant, boundary pairs: pairs in [r_begin, r_end) are kept by the
 // QK^T product for this tile but dropped for some of its cells (distance
 // i - j > W_r).  Their exact terms q'_r k'_r + q'_{r+D/2} k'_{r+D/2} are
@@ -781,41 +884,13 @@ __device__ void softmax_loop(const FwdParams& p, int stage, uint8_t* smg, uint32
             // diagonal tile (causal) and the ragged last tile have a limit < 128
             const bool diag = CAUSAL && n == nhi;
             const bool tail = ragged && n == last_tile;
-            const bool masked = diag || tail;  // uniform across the warp
             int limit = kBlockN;
             if (diag) limit = t + 1;
             if (tail) limit = min(limit, p.S - n * kBlockN);
-            const float mx = masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit);
-            const float m_new = fmaxf(m_used, mx);
-            if (n == nhi) {
-                m_used = m_new;
-            } else {
-                const bool need = (m_new - m_used) * c > kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
-                    float alpha = 1.f;
-                    if (need) {
-                        alpha = ex2_approx((m_used - m_new) * c);
-                        m_used = m_new;
-                        l *= alpha;
-                    }
-                    const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
-                        uint32_t r[32];
-                        tmem_load_32(tO + cc, r);
-#pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            float x0, x1;
-                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2), x0, x1);
-                            r[j] = __float_as_uint(x0);
-                            r[j + 1] = __float_as_uint(x1);
-                        }
-                        tmem_store_32(tO + cc, r);
-                    }
-                }
-            }
-            const float mc = m_used * c;
-            l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
+            if (diag || tail)  // uniform across the warp
+                tile_exp_online<D, true>(tS, tO, c, limit, n == nhi, m_used, l);
+            else
+                tile_exp_online<D, false>(tS, tO, c, limit, n == nhi, m_used, l);
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BAR_P_FULL + stage));

@@ -144,19 +144,46 @@ def test_gqa_outliers_s16384_sampled():
 @pytest.mark.parametrize("base", [None, 10000.0])
 def test_late_large_score_rescales_running_max(base):
     """A key visited last (key 100: chunk 3 of tile 0, reverse traversal) whose
-    score exceeds every earlier one by ~10 in log2 units.  The running max must
-    move mid-tile: O, the P chunks already written and the partial sums are
-    rescaled (the softmax's rare path)."""
+    score exceeds every earlier one by ~24 in log2 units (the rescale threshold
+    is 16).  The running max must move mid-tile: O, the P chunks already written
+    and the partial sums are rescaled (the softmax's rare path)."""
     B, H, S, D = 1, 2, 640, 128
     q = si.bf16_bits_to_f64(si.bshd_bf16(31, 1, B, S, H, D)) * 0.3 + 1.0
     k = si.bf16_bits_to_f64(si.bshd_bf16(31, 2, B, S, H, D)) * 0.3
-    k[:, 100] = 0.7
+    k[:, 100] = 1.5
     v = si.bf16_bits_to_f64(si.bshd_bf16(31, 3, B, S, H, D))
     q, k, v = (si.f64_to_bf16_bits(x.reshape(-1)).reshape(x.shape) for x in (q, k, v))
     o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=True, rope_base=base)
     attn.attn_check()
     o_ref, lse_ref = oracle.attn_full(q, k, v, causal=True, rope_base=base)
     _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "late large score")
+
+
+@pytest.mark.parametrize("base", [None, 10000.0])
+def test_running_max_moves_inside_tiles(base):
+    """Planted keys that move a row's running max inside a tile, where the
+    softmax decides per 32-key chunk:
+    - key 40 (chunk 1 of the diagonal tile 0): rows 40..127 move on their
+      first tile, while rows 0..39 must not see it (masked chunk);
+    - keys 168 and 228 (chunks 1 and 3 of tile 1), each above the running max
+      by more than the threshold: two moves in one tile for rows 256..299;
+    - key 300 (chunk 1 of the diagonal tile 2) for rows 300..383.
+    (Scores in log2 units without RoPE: about 23, 21, 42 and 29 for the planted
+    keys against about 1 for the others; the rescale threshold is 16.)  Large scores on causally
+    hidden keys must never reach earlier rows."""
+    B, H, S, D = 1, 2, 512, 128
+    q = si.bf16_bits_to_f64(si.bshd_bf16(37, 1, B, S, H, D)) * 0.3 + 1.0
+    k = si.bf16_bits_to_f64(si.bshd_bf16(37, 2, B, S, H, D)) * 0.3
+    k[:, 40] = 1.4
+    k[:, 168] = 1.3
+    k[:, 228] = 2.6
+    k[:, 300] = 1.8
+    v = si.bf16_bits_to_f64(si.bshd_bf16(37, 3, B, S, H, D))
+    q, k, v = (si.f64_to_bf16_bits(x.reshape(-1)).reshape(x.shape) for x in (q, k, v))
+    o, lse = attn.attn_fwd(_dev(q), _dev(k), _dev(v), causal=True, rope_base=base)
+    attn.attn_check()
+    o_ref, lse_ref = oracle.attn_full(q, k, v, causal=True, rope_base=base)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "running max moves inside tiles")
 
 
 WINDOW_SMALL = [

@@ -712,15 +712,17 @@ __device__ __forceinline__ void rescale_o_and_p(uint32_t tO, uint32_t tS, float 
 // exceeds m_used by more than the rescale threshold moves m_used there before
 // its own P is formed (l and the tile's partial sum rescaled at once); O_s and
 // the P of the tile's earlier chunks are rescaled after the tile, by the
-// product of the factors that apply to each.  The unit's first chunk only sets
-// m_used (nothing is accumulated yet).  Keys [0, limit) are visible to this row;
-// `first` marks the unit's first tile.
+// product of the factors that apply to each.  While m_used is -inf (no key
+// seen yet) a chunk only sets it: nothing has been accumulated.  Keys
+// [0, limit) are visible to this row; `first` marks the unit's first tile.
 template <int D, bool MASKED>
 __device__ __forceinline__ void tile_exp_online(uint32_t tS, uint32_t tO, float c, int limit, bool first,
                                                 float& m_used, float& l) {
     static_assert(kBlockN == 128, "four 32-key chunks");
     const uint64_t c2 = f2_pack(c, c);
-    uint64_t nmc2 = f2_pack(-m_used * c, -m_used * c);
+    // a row that has seen no key yet forms P against 0: its masked keys give exp2(-inf) = 0
+    const float nmc0 = m_used == -INFINITY ? 0.f : -m_used * c;
+    uint64_t nmc2 = f2_pack(nmc0, nmc0);
     uint64_t sum2 = f2_pack(0.f, 0.f);
     float alpha_all = 1.f, fac0 = 1.f, fac1 = 1.f, fac2 = 1.f;
     bool moved = false;

@@ -328,47 +328,53 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                         b_lin = a_lin * static_cast<float>(rel0);
                     }
                 }
-                float mx;
-                if (EXT != 0 && kind == 0) mx = ext_row_max(tS, lo, limit, c, m2, static_cast<float>(rel0));
-                else if (EXT == 2 && kind == 2) mx = alibi_row_max(tS, c, a_lin, b_lin);
-                else mx = (masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit)) * (EXT ? c : 1.f);
-                const float m_new = fmaxf(m_used, mx);
-                const float unit = EXT ? 1.f : c;
-                if (it == 0) {
-                    m_used = m_new;
+                if constexpr (EXT == 0) {
+                    // the prefill's one-pass softmax (raw score units, chunk maxima from tcgen05.ld.red)
+                    if (masked) tile_exp_online<D, true>(tS, tO, c, limit, it == 0, m_used, l);
+                    else tile_exp_online<D, false>(tS, tO, c, limit, it == 0, m_used, l);
                 } else {
-                    const bool need = (m_new - m_used) * unit > kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, need)) {
-                        float alpha = 1.f;
-                        if (need) {
-                            alpha = m_used == -INFINITY ? 0.f : ex2_approx((m_used - m_new) * unit);
-                            m_used = m_new;
-                            l *= alpha;
-                        }
-                        const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-                        for (int cc = 0; cc < D; cc += 32) {
-                            uint32_t r[32];
-                            tmem_load_32(tO + cc, r);
-#pragma unroll
-                            for (int j = 0; j < 32; j += 2) {
-                                float x0, x1;
-                                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2), x0, x1);
-                                r[j] = __float_as_uint(x0);
-                                r[j + 1] = __float_as_uint(x1);
+                    float mx;
+                    if (EXT != 0 && kind == 0) mx = ext_row_max(tS, lo, limit, c, m2, static_cast<float>(rel0));
+                    else if (EXT == 2 && kind == 2) mx = alibi_row_max(tS, c, a_lin, b_lin);
+                    else mx = (masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit)) * (EXT ? c : 1.f);
+                    const float m_new = fmaxf(m_used, mx);
+                    const float unit = EXT ? 1.f : c;
+                    if (it == 0) {
+                        m_used = m_new;
+                    } else {
+                        const bool need = (m_new - m_used) * unit > kRescaleThreshold;
+                        if (__any_sync(0xffffffffu, need)) {
+                            float alpha = 1.f;
+                            if (need) {
+                                alpha = m_used == -INFINITY ? 0.f : ex2_approx((m_used - m_new) * unit);
+                                m_used = m_new;
+                                l *= alpha;
                             }
-                            tmem_store_32(tO + cc, r);
+                            const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                            for (int cc = 0; cc < D; cc += 32) {
+                                uint32_t r[32];
+                                tmem_load_32(tO + cc, r);
+#pragma unroll
+                                for (int j = 0; j < 32; j += 2) {
+                                    float x0, x1;
+                                    f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2), x0, x1);
+                                    r[j] = __float_as_uint(x0);
+                                    r[j + 1] = __float_as_uint(x1);
+                                }
+                                tmem_store_32(tO + cc, r);
+                            }
                         }
                     }
-                }
-                if (EXT != 0 && kind == 0) {
-                    l += ext_exp_to_p(tS, lo, limit, c, m2, static_cast<float>(rel0), m_used);
-                } else if (EXT == 2 && kind == 2) {
-                    l += alibi_exp_to_p(tS, c, a_lin, b_lin, m_used);  // m is finite: every key is seen
-                } else {
-                    // a row that has seen only masked keys so far (m = -inf) gets P = 0
-                    const float mc = m_used == -INFINITY ? 0.f : m_used * (EXT ? 1.f : c);
-                    l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
+                    if (EXT != 0 && kind == 0) {
+                        l += ext_exp_to_p(tS, lo, limit, c, m2, static_cast<float>(rel0), m_used);
+                    } else if (EXT == 2 && kind == 2) {
+                        l += alibi_exp_to_p(tS, c, a_lin, b_lin, m_used);  // m is finite: every key is seen
+                    } else {
+                        // a row that has seen only masked keys so far (m = -inf) gets P = 0
+                        const float mc = m_used == -INFINITY ? 0.f : m_used * (EXT ? 1.f : c);
+                        l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
+                    }
                 }
                 tmem_store_wait();
                 tc_fence_before();

@@ -177,6 +177,108 @@ __device__ __forceinline__ float alibi_exp_to_p(uint32_t tS, float c, float a, f
     return sum;
 }
 
+// One-pass softmax of a local tile, m in log2 units of the biased score: the
+// tiles with no lower edge and no bias (BIAS false; MASKED on the diagonal or
+// ragged tile) and the ALiBi tiles whose 128 keys the row sees all on one
+// side (BIAS: score = raw c + a j + b0, linear in the column j).  Each 32-key
+// chunk's reference is a bound on its largest score: the chunk maximum that
+// tcgen05.ld.red returns times c (recomputed from the visible keys on masked
+// chunks), plus the chunk's largest bias.  A bound at or above the true
+// maximum is as good a reference as the maximum itself (P is formed against
+// it and stays below 2^threshold); the moves and the deferred rescale of O and
+// earlier P chunks are those of tile_exp_online.
+template <int D, bool MASKED, bool BIAS>
+__device__ __forceinline__ void local_exp_online(uint32_t tS, uint32_t tO, float c, int limit, float a, float b0,
+                                                 bool first, float& m_used, float& l) {
+    static_assert(!(MASKED && BIAS), "ALiBi tiles are fully visible");
+    const uint64_t c2 = f2_pack(c, c);
+    float nm = m_used == -INFINITY ? 0.f : -m_used;  // a row that has seen no key forms P against 0
+    uint64_t sum2 = f2_pack(0.f, 0.f);
+    float alpha_all = 1.f, fac0 = 1.f, fac1 = 1.f, fac2 = 1.f;
+    bool moved = false;
+    auto step = [&](const uint32_t (&r)[32], float cm, int k) {
+        if (MASKED && 32 * k + 31 >= limit) cm = row_max32<true>(r, 32 * k, limit, -INFINITY);
+        float ub = cm * c;
+        if (BIAS) ub += fmaf(a, static_cast<float>(a > 0.f ? 32 * k + 31 : 32 * k), b0);
+        if (ub - m_used > kRescaleThreshold) {
+            if (m_used != -INFINITY) {
+                const float alpha = ex2_approx(m_used - ub);
+                l *= alpha;
+                sum2 = f2_mul(sum2, f2_pack(alpha, alpha));
+                alpha_all *= alpha;
+                if (k > 0) fac0 *= alpha;
+                if (k > 1) fac1 *= alpha;
+                if (k > 2) fac2 *= alpha;
+                moved = true;
+            }
+            m_used = ub;
+            nm = -m_used;
+        }
+        uint32_t pk[16];
+        if constexpr (BIAS) {
+            // x_j = raw_j c + (a j + b0 - m), the bias term advanced two columns at a time
+            const float bm = b0 + nm;
+            uint64_t bias2 = f2_pack(fmaf(a, static_cast<float>(32 * k), bm), fmaf(a, static_cast<float>(32 * k + 1), bm));
+            const uint64_t step2 = f2_pack(2.f * a, 2.f * a);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), c2, bias2), x0, x1);
+                bias2 = f2_add(bias2, step2);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                sum2 = f2_add(sum2, f2_pack(p0, p1));
+                pk[j / 2] = pack_bf16x2(p0, p1);
+            }
+        } else {
+            exp_pack32<MASKED>(r, 32 * k, limit, c2, f2_pack(nm, nm), sum2, pk);
+        }
+        tmem_store_16(tS + 16 * k, pk);
+    };
+    uint32_t ra[32], rb[32];
+    float ma, mb;
+    tmem_load_32_max(tS, ra, ma);
+    tmem_load_32_max_async(tS + 32, rb, mb);
+    step(ra, ma, 0);
+    tmem_wait_ld_32_max(rb, mb);
+    tmem_load_32_max_async(tS + 64, ra, ma);
+    step(rb, mb, 1);
+    tmem_wait_ld_32_max(ra, ma);
+    tmem_load_32_max_async(tS + 96, rb, mb);
+    step(ra, ma, 2);
+    tmem_wait_ld_32_max(rb, mb);
+    step(rb, mb, 3);
+    float s0, s1;
+    f2_unpack(sum2, s0, s1);
+    l += s0 + s1;
+    if (__any_sync(0xffffffffu, moved)) rescale_o_and_p<D>(tO, tS, alpha_all, fac0, fac1, fac2, !first);
+}
+
+// The general local tile (a lower window edge inside the tile, or an ALiBi bias
+// whose sign changes across it): two passes over S (the biased maximum, then
+// P), m in log2 units.  Rare per task, so it is kept out of line: the one-pass
+// paths then keep their registers.  Called by the whole warp.
+template <int D>
+__device__ __noinline__ void local_tile_general(uint32_t tS, uint32_t tO, int lo, int limit, float c, float m2,
+                                                float rel0f, bool first, float& m_used, float& l) {
+    const float mx = ext_row_max(tS, lo, limit, c, m2, rel0f);
+    const float m_new = fmaxf(m_used, mx);
+    if (first) {
+        m_used = m_new;
+    } else {
+        const bool need = m_new - m_used > kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+            float alpha = 1.f;
+            if (need) {
+                alpha = m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new);
+                m_used = m_new;
+                l *= alpha;
+            }
+            rescale_o_and_p<D>(tO, tS, alpha, 1.f, 1.f, 1.f, true);  // no P formed yet: its factors are 1
+        }
+    }
+    l += ext_exp_to_p(tS, lo, limit, c, m2, rel0f, m_used);
+}
+
 // One task: query tile i of batch b, head h (KV head g); its listed key tiles are
 // col_idx[e0 .. e0 + nblk), visited last first.
 struct BsTask {
@@ -332,49 +434,13 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                     // the prefill's one-pass softmax (raw score units, chunk maxima from tcgen05.ld.red)
                     if (masked) tile_exp_online<D, true>(tS, tO, c, limit, it == 0, m_used, l);
                     else tile_exp_online<D, false>(tS, tO, c, limit, it == 0, m_used, l);
-                } else {
-                    float mx;
-                    if (EXT != 0 && kind == 0) mx = ext_row_max(tS, lo, limit, c, m2, static_cast<float>(rel0));
-                    else if (EXT == 2 && kind == 2) mx = alibi_row_max(tS, c, a_lin, b_lin);
-                    else mx = (masked ? tile_row_max<true>(tS, limit) : tile_row_max<false>(tS, limit)) * (EXT ? c : 1.f);
-                    const float m_new = fmaxf(m_used, mx);
-                    const float unit = EXT ? 1.f : c;
-                    if (it == 0) {
-                        m_used = m_new;
-                    } else {
-                        const bool need = (m_new - m_used) * unit > kRescaleThreshold;
-                        if (__any_sync(0xffffffffu, need)) {
-                            float alpha = 1.f;
-                            if (need) {
-                                alpha = m_used == -INFINITY ? 0.f : ex2_approx((m_used - m_new) * unit);
-                                m_used = m_new;
-                                l *= alpha;
-                            }
-                            const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-                            for (int cc = 0; cc < D; cc += 32) {
-                                uint32_t r[32];
-                                tmem_load_32(tO + cc, r);
-#pragma unroll
-                                for (int j = 0; j < 32; j += 2) {
-                                    float x0, x1;
-                                    f2_unpack(f2_mul(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2), x0, x1);
-                                    r[j] = __float_as_uint(x0);
-                                    r[j + 1] = __float_as_uint(x1);
-                                }
-                                tmem_store_32(tO + cc, r);
-                            }
-                        }
-                    }
-                    if (EXT != 0 && kind == 0) {
-                        l += ext_exp_to_p(tS, lo, limit, c, m2, static_cast<float>(rel0), m_used);
-                    } else if (EXT == 2 && kind == 2) {
-                        l += alibi_exp_to_p(tS, c, a_lin, b_lin, m_used);  // m is finite: every key is seen
-                    } else {
-                        // a row that has seen only masked keys so far (m = -inf) gets P = 0
-                        const float mc = m_used == -INFINITY ? 0.f : m_used * (EXT ? 1.f : c);
-                        l += masked ? tile_exp_to_p<true>(tS, limit, c, mc) : tile_exp_to_p<false>(tS, limit, c, mc);
-                    }
+                } else if (EXT == 1 && kind == 1) {
+                    if (masked) local_exp_online<D, true, false>(tS, tO, c, limit, 0.f, 0.f, it == 0, m_used, l);
+                    else local_exp_online<D, false, false>(tS, tO, c, limit, 0.f, 0.f, it == 0, m_used, l);
+                } else if (EXT == 2 && kind == 2) {
+                    local_exp_online<D, false, true>(tS, tO, c, 128, a_lin, b_lin, it == 0, m_used, l);
+                } else {  // the general local tile: a lower edge or a bias across the row
+                    local_tile_general<D>(tS, tO, lo, limit, c, m2, static_cast<float>(rel0), it == 0, m_used, l);
                 }
                 tmem_store_wait();
                 tc_fence_before();

@@ -640,49 +640,65 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* 
     const char* hk = static_cast<const char*>(k);
     const char* hv = static_cast<const char*>(v);
     char* ho = static_cast<char*>(o);
-    cudaError_t e = cudaSuccess;
-    int c = 0;
-    for (int b = 0; b < B && rc == ATTN_OK; ++b) {
-        for (int gi = 0; gi < groups && rc == ATTN_OK; ++gi, ++c) {
+    // The chunk list: equal chunks, except that the last is cut into up to four
+    // pieces.  The input copies run back to back on one copy engine and the kernels
+    // hide behind them, so what shows is the last chunk's compute and copy out.
+    struct Chunk {
+        int b, g0, g1;
+    };
+    std::vector<Chunk> chunks;
+    for (int b = 0; b < B; ++b)
+        for (int gi = 0; gi < groups; ++gi) {
             const int g0 = Hkv * gi / groups, g1 = Hkv * (gi + 1) / groups;
-            if (g1 <= g0) continue;
-            const int hkv = g1 - g0, hq_n = hkv * G, h0 = g0 * G;
-            const int slot = c & 1;
-            uint8_t* base = hp.buf + slot * hp.slot_bytes;
-            uint8_t* dq = base;
-            uint8_t* dout = base + q_bytes;
-            uint8_t* dk = base + 2 * q_bytes;
-            uint8_t* dv = dk + kv_bytes;
-            float* dl = reinterpret_cast<float*>(dv + kv_bytes);
-            const size_t row_q = static_cast<size_t>(Hq) * D * e2, row_kv = static_cast<size_t>(Hkv) * D * e2;
-            const size_t w_q = static_cast<size_t>(hq_n) * D * e2, w_kv = static_cast<size_t>(hkv) * D * e2;
-            const size_t off_q = (static_cast<size_t>(b) * S * Hq + h0) * D * e2;
-            const size_t off_kv = (static_cast<size_t>(b) * S * Hkv + g0) * D * e2;
-            // in: the slot's previous chunk must have been read by its kernel
-            if (c >= 2 && (e = cudaStreamWaitEvent(hp.s_in, hp.ev_comp[slot], 0)) != cudaSuccess) break;
-            if ((e = copy_rows(dq, hq + off_q, w_q, row_q, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
-                (e = copy_rows(dk, hk + off_kv, w_kv, row_kv, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
-                (e = copy_rows(dv, hv + off_kv, w_kv, row_kv, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
-                (e = cudaEventRecord(hp.ev_in[slot], hp.s_in)) != cudaSuccess)
-                break;
-            // compute: after the inputs landed and the slot's previous outputs left
-            if ((e = cudaStreamWaitEvent(hp.s_comp, hp.ev_in[slot], 0)) != cudaSuccess) break;
-            if (c >= 2 && (e = cudaStreamWaitEvent(hp.s_comp, hp.ev_out[slot], 0)) != cudaSuccess) break;
-            rc = attn_fwd(dq, dk, dv, dout, lse != nullptr ? dl : nullptr, 1, hq_n, hkv, S, D, causal, rope_base,
-                          window_k, hp.s_comp);
-            if (rc != ATTN_OK) break;
-            if ((e = cudaEventRecord(hp.ev_comp[slot], hp.s_comp)) != cudaSuccess) break;
-            // out
-            if ((e = cudaStreamWaitEvent(hp.s_out, hp.ev_comp[slot], 0)) != cudaSuccess ||
-                (e = copy_rows_out(ho + off_q, row_q, dout, w_q, S, hp.s_out)) != cudaSuccess)
-                break;
-            if (lse != nullptr &&
-                (e = cudaMemcpyAsync(lse + (static_cast<size_t>(b) * Hq + h0) * S, dl,
-                                     static_cast<size_t>(hq_n) * S * sizeof(float), cudaMemcpyDeviceToHost,
-                                     hp.s_out)) != cudaSuccess)
-                break;
-            if ((e = cudaEventRecord(hp.ev_out[slot], hp.s_out)) != cudaSuccess) break;
+            if (g1 > g0) chunks.push_back({b, g0, g1});
         }
+    if (!chunks.empty()) {
+        const Chunk last = chunks.back();
+        const int pieces = std::min(4, last.g1 - last.g0);
+        chunks.pop_back();
+        for (int i = 0; i < pieces; ++i)
+            chunks.push_back({last.b, last.g0 + (last.g1 - last.g0) * i / pieces,
+                              last.g0 + (last.g1 - last.g0) * (i + 1) / pieces});
+    }
+    cudaError_t e = cudaSuccess;
+    for (int c = 0; c < static_cast<int>(chunks.size()) && rc == ATTN_OK; ++c) {
+        const int b = chunks[c].b, g0 = chunks[c].g0, g1 = chunks[c].g1;
+        const int hkv = g1 - g0, hq_n = hkv * G, h0 = g0 * G;
+        const int slot = c & 1;
+        uint8_t* base = hp.buf + slot * hp.slot_bytes;
+        uint8_t* dq = base;
+        uint8_t* dout = base + q_bytes;
+        uint8_t* dk = base + 2 * q_bytes;
+        uint8_t* dv = dk + kv_bytes;
+        float* dl = reinterpret_cast<float*>(dv + kv_bytes);
+        const size_t row_q = static_cast<size_t>(Hq) * D * e2, row_kv = static_cast<size_t>(Hkv) * D * e2;
+        const size_t w_q = static_cast<size_t>(hq_n) * D * e2, w_kv = static_cast<size_t>(hkv) * D * e2;
+        const size_t off_q = (static_cast<size_t>(b) * S * Hq + h0) * D * e2;
+        const size_t off_kv = (static_cast<size_t>(b) * S * Hkv + g0) * D * e2;
+        // in: the slot's previous chunk must have been read by its kernel
+        if (c >= 2 && (e = cudaStreamWaitEvent(hp.s_in, hp.ev_comp[slot], 0)) != cudaSuccess) break;
+        if ((e = copy_rows(dq, hq + off_q, w_q, row_q, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
+            (e = copy_rows(dk, hk + off_kv, w_kv, row_kv, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
+            (e = copy_rows(dv, hv + off_kv, w_kv, row_kv, S, cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess ||
+            (e = cudaEventRecord(hp.ev_in[slot], hp.s_in)) != cudaSuccess)
+            break;
+        // compute: after the inputs landed and the slot's previous outputs left
+        if ((e = cudaStreamWaitEvent(hp.s_comp, hp.ev_in[slot], 0)) != cudaSuccess) break;
+        if (c >= 2 && (e = cudaStreamWaitEvent(hp.s_comp, hp.ev_out[slot], 0)) != cudaSuccess) break;
+        rc = attn_fwd(dq, dk, dv, dout, lse != nullptr ? dl : nullptr, 1, hq_n, hkv, S, D, causal, rope_base,
+                      window_k, hp.s_comp);
+        if (rc != ATTN_OK) break;
+        if ((e = cudaEventRecord(hp.ev_comp[slot], hp.s_comp)) != cudaSuccess) break;
+        // out
+        if ((e = cudaStreamWaitEvent(hp.s_out, hp.ev_comp[slot], 0)) != cudaSuccess ||
+            (e = copy_rows_out(ho + off_q, row_q, dout, w_q, S, hp.s_out)) != cudaSuccess)
+            break;
+        if (lse != nullptr &&
+            (e = cudaMemcpyAsync(lse + (static_cast<size_t>(b) * Hq + h0) * S, dl,
+                                 static_cast<size_t>(hq_n) * S * sizeof(float), cudaMemcpyDeviceToHost,
+                                 hp.s_out)) != cudaSuccess)
+            break;
+        if ((e = cudaEventRecord(hp.ev_out[slot], hp.s_out)) != cudaSuccess) break;
     }
     // the call returns once every chunk is back in host memory
     const cudaError_t e_sync = cudaStreamSynchronize(hp.s_out);

@@ -191,46 +191,68 @@ __device__ __forceinline__ void bwd_store_row(const BwdParams& p, uint32_t taddr
 // LSE2_col) (0 where the query is before the key), packed to bf16 over the half's S^T columns
 // (for dV) and kept in pp (for dS: the next S^T overwrites those columns meanwhile).
 template <bool MASKED>
-__device__ __forceinline__ void bwd_ew_p(uint32_t tS, const float* ls, float c, int lim, uint32_t (&pp)[32]) {
+__device__ __forceinline__ void bwd_ew_p(uint32_t tS, const float* nls, float c, int lim, uint32_t (&pp)[32]) {
+    // nls: -LSE2 of the half's 64 query columns (-inf for padded queries: P = 0)
+    const uint64_t c2 = f2_pack(c, c);
+    auto chunk = [&](const uint32_t (&rs)[32], int cc) {
 #pragma unroll
-    for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t rs[32];
-        tmem_load_32(tS + cc, rs);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            const float2 l2 = *reinterpret_cast<const float2*>(ls + cc + e);
-            float p0 = ex2_approx(__uint_as_float(rs[e]) * c - l2.x);
-            float p1 = ex2_approx(__uint_as_float(rs[e + 1]) * c - l2.y);
+        for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nls + cc + e);
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, f2_pack(l4.x, l4.y)), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[e + 2]), __uint_as_float(rs[e + 3])), c2, f2_pack(l4.z, l4.w)),
+                      x2, x3);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
             if (MASKED) {
                 if (cc + e < lim) p0 = 0.f;
                 if (cc + e + 1 < lim) p1 = 0.f;
+                if (cc + e + 2 < lim) p2 = 0.f;
+                if (cc + e + 3 < lim) p3 = 0.f;
             }
             pp[(cc + e) / 2] = pack_bf16x2(p0, p1);
+            pp[(cc + e) / 2 + 1] = pack_bf16x2(p2, p3);
         }
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pp[cc / 2 + e];
-        tmem_store_16(tS + cc / 2, pk);
-    }
+        tmem_store_16(tS + cc / 2, pk);  // columns [cc/2, cc/2 + 16): never a column still to be read
+    };
+    // the second chunk's load is in flight while the first is processed
+    uint32_t ra[32], rb[32];
+    tmem_load_32(tS, ra);
+    tmem_load_32_async(tS + 32, rb);
+    chunk(ra, 0);
+    tmem_wait_ld_32(rb);
+    chunk(rb, 32);
 }
 // dS phase: dS^T = P^T (dP^T - Dlt_col) from the bf16 P^T of the P phase (the value dV
 // accumulates), fp16 after RoPE, else bf16, over the half's dP^T columns.
 template <bool ROPE>
 __device__ __forceinline__ void bwd_ew_ds(uint32_t tdP, const float* dl, const uint32_t (&pp)[32]) {
-#pragma unroll
-    for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t rd[32];
-        tmem_load_32(tdP + cc, rd);
+    auto chunk = [&](const uint32_t (&rd)[32], int cc) {
         uint32_t pd[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            const float2 d2 = *reinterpret_cast<const float2*>(dl + cc + e);
-            const float s0 = bf16_lo(pp[(cc + e) / 2]) * (__uint_as_float(rd[e]) - d2.x);
-            const float s1 = bf16_hi(pp[(cc + e) / 2]) * (__uint_as_float(rd[e + 1]) - d2.y);
+        for (int e = 0; e < 32; e += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dl + cc + e);
+            const uint32_t pa = pp[(cc + e) / 2], pb = pp[(cc + e) / 2 + 1];
+            float s0, s1, s2, s3;
+            f2_unpack(f2_mul(f2_pack(bf16_lo(pa), bf16_hi(pa)),
+                             f2_sub(f2_pack(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])), f2_pack(d4.x, d4.y))),
+                      s0, s1);
+            f2_unpack(f2_mul(f2_pack(bf16_lo(pb), bf16_hi(pb)),
+                             f2_sub(f2_pack(__uint_as_float(rd[e + 2]), __uint_as_float(rd[e + 3])), f2_pack(d4.z, d4.w))),
+                      s2, s3);
             pd[e / 2] = ROPE ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
+            pd[e / 2 + 1] = ROPE ? pack_f16x2(s2, s3) : pack_bf16x2(s2, s3);
         }
         tmem_store_16(tdP + cc / 2, pd);
-    }
+    };
+    uint32_t ra[32], rb[32];
+    tmem_load_32(tdP, ra);
+    tmem_load_32_async(tdP + 32, rb);
+    chunk(ra, 0);
+    tmem_wait_ld_32(rb);
+    chunk(rb, 32);
 }
 
 // The dQ kernel's elementwise work in the same two phases, one thread per query row and half of
@@ -238,38 +260,50 @@ __device__ __forceinline__ void bwd_ew_ds(uint32_t tdP, const float* dl, const u
 // c > lim), kept in pp as bf16 (the P of the dK/dV kernel's dS, so both kernels form one dS).
 template <bool MASKED>
 __device__ __forceinline__ void bwd_ew_p_row(uint32_t tS, float l2, float c, int lim, uint32_t (&pp)[32]) {
-#pragma unroll
-    for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t rs[32];
-        tmem_load_32(tS + cc, rs);
+    const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-l2, -l2);  // -inf for a padded row: P = 0
+    auto chunk = [&](const uint32_t (&rs)[32], int cc) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-            float p0 = ex2_approx(__uint_as_float(rs[e]) * c - l2);
-            float p1 = ex2_approx(__uint_as_float(rs[e + 1]) * c - l2);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, nl2), x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             if (MASKED) {
                 if (cc + e > lim) p0 = 0.f;
                 if (cc + e + 1 > lim) p1 = 0.f;
             }
             pp[(cc + e) / 2] = pack_bf16x2(p0, p1);
         }
-    }
+    };
+    uint32_t ra[32], rb[32];
+    tmem_load_32(tS, ra);
+    tmem_load_32_async(tS + 32, rb);
+    chunk(ra, 0);
+    tmem_wait_ld_32(rb);
+    chunk(rb, 32);
 }
 // dS phase: dS = P (dP - Dlt_row) over the half's dP columns (fp16 after RoPE, else bf16).
 template <bool ROPE>
 __device__ __forceinline__ void bwd_ew_ds_row(uint32_t tdP, float dl, const uint32_t (&pp)[32]) {
-#pragma unroll
-    for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t rd[32];
-        tmem_load_32(tdP + cc, rd);
+    const uint64_t dl2 = f2_pack(dl, dl);
+    auto chunk = [&](const uint32_t (&rd)[32], int cc) {
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-            const float s0 = bf16_lo(pp[(cc + e) / 2]) * (__uint_as_float(rd[e]) - dl);
-            const float s1 = bf16_hi(pp[(cc + e) / 2]) * (__uint_as_float(rd[e + 1]) - dl);
+            const uint32_t pa = pp[(cc + e) / 2];
+            float s0, s1;
+            f2_unpack(f2_mul(f2_pack(bf16_lo(pa), bf16_hi(pa)),
+                             f2_sub(f2_pack(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])), dl2)),
+                      s0, s1);
             pd[e / 2] = ROPE ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
         }
         tmem_store_16(tdP + cc / 2, pd);
-    }
+    };
+    uint32_t ra[32], rb[32];
+    tmem_load_32(tdP, ra);
+    tmem_load_32_async(tdP + 32, rb);
+    chunk(ra, 0);
+    tmem_wait_ld_32(rb);
+    chunk(rb, 32);
 }
 
 // TMEM column of k-step kk (16 rows of the streamed tile) of packed P / dS: each half of 64
@@ -456,7 +490,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             for (int q = 0; q < 4; ++q) {
                 const int r = q0 + lane + 32 * q;
                 const bool in = r < f.S;
-                lv[q] = in ? __ldg(lse_row + r) * 1.4426950408889634f : INFINITY;  // padded queries get P = 0
+                lv[q] = in ? -(__ldg(lse_row + r) * 1.4426950408889634f) : -INFINITY;  // -LSE2; padded queries: P = 0
                 dv4[q] = in ? __ldg(dlt_row + r) : 0.f;
             }
             if (n >= 1 && !bwd_wait(bar_at(bar0, BB_STR_EMPTY + s), (n - 1) & 1, ctl, kStatusProducer)) break;

@@ -180,3 +180,14 @@ def test_build_tables_rejects_bad_arguments(lib):
         attn.attn_build_tables(16, 128, 0.0)
     with pytest.raises(attn.AttnError):
         attn.attn_build_tables(16, 80, 10000.0)
+
+
+def test_tmem_io_matches_its_generator(tmp_path):
+    """tmem_io.inc (the tcgen05.ld / ld.red / st wrappers with long operand lists) is what
+    gen_tmem_io.py writes: an edit of either alone fails here."""
+    import sys
+    from pathlib import Path
+    csrc = Path(__file__).resolve().parents[1] / "attention_causal_attn_gb300" / "csrc"
+    out = tmp_path / "tmem_io.inc"
+    subprocess.run([sys.executable, str(csrc / "gen_tmem_io.py"), str(out)], check=True)
+    assert out.read_text() == (csrc / "tmem_io.inc").read_text()

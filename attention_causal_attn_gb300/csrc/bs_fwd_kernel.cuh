@@ -139,65 +139,33 @@ __device__ __forceinline__ float ext_exp_to_p(uint32_t tS, int lo, int hi, float
     return sum;
 }
 
-// ALiBi on a tile whose 128 keys this row all sees and which lies on one side of the row:
-// |rel0 + j| = sgn (rel0 + j), so the biased score is raw c + a j + b0 with a = -m2 sgn and
-// b0 = a rel0, linear in the column.
-__device__ __forceinline__ float alibi_row_max(uint32_t tS, float c, float a, float b0) {
-    float mx = -INFINITY;
-    tmem_stream_128(tS, [&](const uint32_t (&r)[32], int cc) {
-        float m0 = mx, m1 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            float v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                v[q] = fmaf(__uint_as_float(r[j + q]), c, fmaf(a, static_cast<float>(cc + j + q), b0));
-            m0 = fmax3(m0, v[0], v[1]);
-            m1 = fmax3(m1, v[2], v[3]);
-        }
-        mx = fmaxf(m0, m1);
-    });
-    return mx;
-}
-
-__device__ __forceinline__ float alibi_exp_to_p(uint32_t tS, float c, float a, float b0, float m) {
-    const float bm = b0 - m;
-    float sum = 0.f;
-    tmem_stream_128(tS, [&](const uint32_t (&r)[32], int cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(r[j]), c, fmaf(a, static_cast<float>(cc + j), bm)));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(r[j + 1]), c, fmaf(a, static_cast<float>(cc + j + 1), bm)));
-            sum += p0 + p1;
-            pk[j / 2] = pack_bf16x2(p0, p1);
-        }
-        tmem_store_16(tS + cc / 2, pk);
-    });
-    return sum;
-}
-
 // One-pass softmax of a local tile, m in log2 units of the biased score: the
-// tiles with no lower edge and no bias (BIAS false; MASKED on the diagonal or
-// ragged tile) and the ALiBi tiles whose 128 keys the row sees all on one
-// side (BIAS: score = raw c + a j + b0, linear in the column j).  Each 32-key
-// chunk's reference is a bound on its largest score: the chunk maximum that
-// tcgen05.ld.red returns times c (recomputed from the visible keys on masked
-// chunks), plus the chunk's largest bias.  A bound at or above the true
-// maximum is as good a reference as the maximum itself (P is formed against
-// it and stays below 2^threshold); the moves and the deferred rescale of O and
-// earlier P chunks are those of tile_exp_online.
+// window tiles with no bias (BIAS false) and the ALiBi tiles whose visible keys
+// all lie on one side of the row (BIAS: score = raw c + a j + b0, linear in the
+// column j).  MASKED: the row sees only the keys [lo, limit) of the tile (a
+// lower window edge, the diagonal, a ragged end); the hidden scores become
+// -inf before the exponential, so their P is exactly 0.  Each 32-key chunk's
+// reference is a bound on its largest score: the chunk maximum that
+// tcgen05.ld.red returns times c (recomputed from the visible keys on chunks
+// with hidden ones), plus the chunk's largest bias.  A bound at or above the
+// true maximum is as good a reference as the maximum itself (P is formed
+// against it and stays below 2^threshold); the moves and the deferred rescale
+// of O and earlier P chunks are those of tile_exp_online.
 template <int D, bool MASKED, bool BIAS>
-__device__ __forceinline__ void local_exp_online(uint32_t tS, uint32_t tO, float c, int limit, float a, float b0,
-                                                 bool first, float& m_used, float& l) {
-    static_assert(!(MASKED && BIAS), "ALiBi tiles are fully visible");
+__device__ __forceinline__ void local_exp_online(uint32_t tS, uint32_t tO, float c, int lo, int limit, float a,
+                                                 float b0, bool first, float& m_used, float& l) {
     const uint64_t c2 = f2_pack(c, c);
     float nm = m_used == -INFINITY ? 0.f : -m_used;  // a row that has seen no key forms P against 0
     uint64_t sum2 = f2_pack(0.f, 0.f);
     float alpha_all = 1.f, fac0 = 1.f, fac1 = 1.f, fac2 = 1.f;
     bool moved = false;
-    auto step = [&](const uint32_t (&r)[32], float cm, int k) {
-        if (MASKED && 32 * k + 31 >= limit) cm = row_max32<true>(r, 32 * k, limit, -INFINITY);
+    auto step = [&](uint32_t (&r)[32], float cm, int k) {
+        if (MASKED && (32 * k < lo || 32 * k + 31 >= limit)) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (32 * k + j < lo || 32 * k + j >= limit) r[j] = __float_as_uint(-INFINITY);
+            cm = row_max32<false>(r, 0, 0, -INFINITY);
+        }
         float ub = cm * c;
         if (BIAS) ub += fmaf(a, static_cast<float>(a > 0.f ? 32 * k + 31 : 32 * k), b0);
         if (ub - m_used > kRescaleThreshold) {
@@ -230,7 +198,7 @@ __device__ __forceinline__ void local_exp_online(uint32_t tS, uint32_t tO, float
                 pk[j / 2] = pack_bf16x2(p0, p1);
             }
         } else {
-            exp_pack32<MASKED>(r, 32 * k, limit, c2, f2_pack(nm, nm), sum2, pk);
+            exp_pack32<false>(r, 32 * k, limit, c2, f2_pack(nm, nm), sum2, pk);
         }
         tmem_store_16(tS + 16 * k, pk);
     };
@@ -253,10 +221,11 @@ __device__ __forceinline__ void local_exp_online(uint32_t tS, uint32_t tO, float
     if (__any_sync(0xffffffffu, moved)) rescale_o_and_p<D>(tO, tS, alpha_all, fac0, fac1, fac2, !first);
 }
 
-// The general local tile (a lower window edge inside the tile, or an ALiBi bias
-// whose sign changes across it): two passes over S (the biased maximum, then
-// P), m in log2 units.  Rare per task, so it is kept out of line: the one-pass
-// paths then keep their registers.  Called by the whole warp.
+// The general local tile (an ALiBi bias whose sign changes across a row's
+// visible keys: the diagonal tile of a two-sided window): two passes over S
+// (the biased maximum, then P), m in log2 units.  Rare per task, so it is kept
+// out of line: the one-pass paths then keep their registers.  Called by the
+// whole warp.
 template <int D>
 __device__ __noinline__ void local_tile_general(uint32_t tS, uint32_t tO, int lo, int limit, float c, float m2,
                                                 float rel0f, bool first, float& m_used, float& l) {
@@ -416,17 +385,18 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                 }
                 const int rel0 = kv0 - row;
                 const bool masked = __any_sync(0xffffffffu, limit < 128);
-                // EXT tile kinds (uniform across the warp): 1 = no bias and no lower edge (the plain
-                // path, in log2 units), 2 = ALiBi on fully visible keys on one side of every row,
-                // 0 = the general form
+                const bool edged = EXT != 0 && __any_sync(0xffffffffu, lo > 0 || limit < 128);
+                // EXT tile kinds (uniform across the warp): 1 = no bias (window edges as masks, in
+                // log2 units), 2 = ALiBi whose visible keys lie on one side of every row, 0 = the
+                // general form (an ALiBi tile that a row's visible keys straddle)
                 int kind = 0;
                 float a_lin = 0.f, b_lin = 0.f;
                 if constexpr (EXT == 1) {
-                    if (__all_sync(0xffffffffu, lo <= 0)) kind = 1;
+                    kind = 1;
                 } else if constexpr (EXT == 2) {
-                    if (__all_sync(0xffffffffu, lo <= 0 && limit >= 128 && (kv0 >= row || kv0 + 127 <= row))) {
+                    if (__all_sync(0xffffffffu, kv0 + lo >= row || kv0 + limit - 1 <= row)) {
                         kind = 2;
-                        a_lin = kv0 >= row ? -m2 : m2;
+                        a_lin = kv0 + lo >= row ? -m2 : m2;
                         b_lin = a_lin * static_cast<float>(rel0);
                     }
                 }
@@ -435,10 +405,11 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                     if (masked) tile_exp_online<D, true>(tS, tO, c, limit, it == 0, m_used, l);
                     else tile_exp_online<D, false>(tS, tO, c, limit, it == 0, m_used, l);
                 } else if (EXT == 1 && kind == 1) {
-                    if (masked) local_exp_online<D, true, false>(tS, tO, c, limit, 0.f, 0.f, it == 0, m_used, l);
-                    else local_exp_online<D, false, false>(tS, tO, c, limit, 0.f, 0.f, it == 0, m_used, l);
+                    if (edged) local_exp_online<D, true, false>(tS, tO, c, lo, limit, 0.f, 0.f, it == 0, m_used, l);
+                    else local_exp_online<D, false, false>(tS, tO, c, 0, 128, 0.f, 0.f, it == 0, m_used, l);
                 } else if (EXT == 2 && kind == 2) {
-                    local_exp_online<D, false, true>(tS, tO, c, 128, a_lin, b_lin, it == 0, m_used, l);
+                    if (edged) local_exp_online<D, true, true>(tS, tO, c, lo, limit, a_lin, b_lin, it == 0, m_used, l);
+                    else local_exp_online<D, false, true>(tS, tO, c, 0, 128, a_lin, b_lin, it == 0, m_used, l);
                 } else {  // the general local tile: a lower edge or a bias across the row
                     local_tile_general<D>(tS, tO, lo, limit, c, m2, static_cast<float>(rel0), it == 0, m_used, l);
                 }

@@ -535,6 +535,8 @@ LOCAL = [
     (2, 4, 2, 700, 128, True, 10000.0, 0, True),     # ALiBi over the whole causal range, RoPE, GQA
     (1, 2, 2, 640, 64, False, None, 100, True),      # both, non-causal window
     (1, 3, 3, 300, 128, True, 10000.0, 1, True),     # a window of one key: O_i = V_i
+    (1, 2, 2, 520, 128, True, None, 45, False),      # both window edges inside one tile and one 32-key chunk
+    (1, 4, 2, 900, 64, True, 10000.0, 200, True),    # causal window and ALiBi: masked biased tiles, ragged
 ]
 
 

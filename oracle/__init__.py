@@ -52,6 +52,9 @@ def _load():
             lib.oracle_rope_rotate.argtypes = [u16p] + [ctypes.c_int] * 4 + [ctypes.c_double, f64p]
             lib.oracle_attn_bwd.restype = ctypes.c_int
             lib.oracle_attn_bwd.argtypes = [f64p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_double] + [f64p] * 3
+            lib.oracle_attn_bwd_local.restype = ctypes.c_int
+            lib.oracle_attn_bwd_local.argtypes = [f64p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int,
+                                                                                   ctypes.c_int] + [f64p] * 3
             lib.oracle_attn_bwd_bs.restype = ctypes.c_int
             lib.oracle_attn_bwd_bs.argtypes = [f64p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int,
                                                                                   i32p, i32p] + [f64p] * 3
@@ -143,11 +146,12 @@ def bf16_to_f64(x) -> np.ndarray:
     return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def attn_bwd(q, k, v, dO, *, causal=True, rope_base=None, block_mask=None, block=128):
+def attn_bwd(q, k, v, dO, *, causal=True, rope_base=None, block_mask=None, block=128, window=0, alibi=False):
     """dQ [B,S,Hq,D], dK, dV [B,S,Hkv,D] (float64) of sum(O * dO) for the attention forward.
 
     q, k, v, dO: uint16 bf16 bits (widened exactly) or float64 arrays, BSHD.
     block_mask: optional CSR (row_ptr, col_idx) over block x block tiles.
+    window / alibi: the local forward's sliding window (|i-j| < window) and ALiBi bias.
     """
     def f64(a):
         return bf16_to_f64(a) if a.dtype == np.uint16 else np.ascontiguousarray(a, dtype=np.float64)
@@ -160,7 +164,11 @@ def attn_bwd(q, k, v, dO, *, causal=True, rope_base=None, block_mask=None, block
     args = (_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
             _ptr(dO, ctypes.c_double), B, Hq, Hkv, S, D, 1 if causal else 0, float(rope_base) if rope_base else 0.0)
     outs = (_ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double))
-    if block_mask is None:
+    if window or alibi:
+        if block_mask is not None:
+            raise ValueError("a block mask does not combine with window / alibi here")
+        rc = _load().oracle_attn_bwd_local(*args, int(window), 1 if alibi else 0, *outs)
+    elif block_mask is None:
         rc = _load().oracle_attn_bwd(*args, *outs)
     else:
         rp = np.ascontiguousarray(block_mask[0], dtype=np.int32)

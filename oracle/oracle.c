@@ -237,14 +237,17 @@ long long oracle_pruned_terms(int S, int D, double rope_base, double window_k) {
 }
 
 /*
- * Gradients of the attention above (RoPE, causal or full, GQA; window off)
+ * Gradients of the attention above (RoPE, causal or full, GQA; the pair
+ * window off; optionally a block mask, a sliding window and ALiBi, below)
  * for a scalar loss whose gradient with respect to O is dO ("AttnFuse",
  * sec. 4.4 Backward Pass: the backward re-derives the softmax probabilities
  * from the forward's per-row L = m + log l).  Written from the chain rule on
  * the definitions, one (batch, KV head) group at a time, with every
  * probability row materialised:
  *
- *   p_ij   = exp(s_ij - LSE_i)                  (s as in the forward)
+ *   p_ij   = exp(s_ij - LSE_i)                  (s as in the forward, with
+ *            the local forward's -m_h |i - j| when ALiBi is on: a constant in
+ *            q and k, so dS keeps its form)
  *   dV_j   = sum_i p_ij dO_i                    (summed over the group's heads)
  *   dP_ij  = dO_i . V_j
  *   Dlt_i  = sum_j p_ij dP_ij                   (= dO_i . O_i)
@@ -261,9 +264,10 @@ long long oracle_pruned_terms(int S, int D, double rope_base, double window_k) {
  */
 static int attn_bwd_masked(const double* q, const double* k, const double* v, const double* dO,
                            int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
-                           const char* active, int block, int nb,
+                           const char* active, int block, int nb, int window, int alibi,
                            double* dq, double* dk, double* dv) {
-    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 1024) return -1;
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 2 || D % 2 != 0 || D > 1024 || window < 0)
+        return -1;
     const int rope_on = rope_base > 0.0;
     const int G = Hq / Hkv;
     const int half = D / 2;
@@ -300,10 +304,14 @@ static int attn_bwd_masked(const double* q, const double* k, const double* v, co
             }
         }
         for (int h = g * G; h < (g + 1) * G; ++h) {
+            const double slope = alibi ? pow(2.0, -8.0 * (double)(h + 1) / (double)Hq) : 0.0;
             for (int i = 0; i < S; ++i) {
                 const int last = causal ? i : S - 1;
-                /* key j is visible iff j <= last and (no mask, or block (i/block, j/block) listed) */
-#define VISIBLE(j) (active == NULL || active[(size_t)(i / block) * nb + (j) / block])
+                /* key j is visible iff j <= last, (no mask, or block (i/block, j/block) listed) and
+                 * (no window, or |i - j| < window) */
+#define DIST(j) ((i) >= (j) ? (i) - (j) : (j) - (i))
+#define VISIBLE(j) ((active == NULL || active[(size_t)(i / block) * nb + (j) / block]) && \
+                    (window == 0 || DIST(j) < window))
                 const double* qi = q + (((size_t)b * S + i) * Hq + h) * D;
                 const double* doi = dO + (((size_t)b * S + i) * Hq + h) * D;
                 for (int r = 0; r < half; ++r) {
@@ -323,7 +331,7 @@ static int attn_bwd_masked(const double* q, const double* k, const double* v, co
                     if (!VISIBLE(j)) continue;
                     double acc = 0.0;
                     for (int d = 0; d < D; ++d) acc += qr[d] * kr[(size_t)j * D + d];
-                    p[j] = acc * inv_sqrt_d;
+                    p[j] = acc * inv_sqrt_d - slope * (double)DIST(j);
                     if (p[j] > m) m = p[j];
                 }
                 double l = 0.0;
@@ -399,13 +407,29 @@ static int attn_bwd_masked(const double* q, const double* k, const double* v, co
         free(dp);
     }
 #undef VISIBLE
+#undef DIST
     return 0;
 }
 
 int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dO,
                     int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
                     double* dq, double* dk, double* dv) {
-    return attn_bwd_masked(q, k, v, dO, B, Hq, Hkv, S, D, causal, rope_base, NULL, 1, 1, dq, dk, dv);
+    return attn_bwd_masked(q, k, v, dO, B, Hq, Hkv, S, D, causal, rope_base, NULL, 1, 1, 0, 0, dq, dk, dv);
+}
+
+/*
+ * The same gradients with a sliding window and/or ALiBi ("AttnFuse", sec. 3:
+ * the sliding_window and alibi combinators; sec. 4.4: the backward re-derives
+ * P from the forward's statistics): key j is visible to query i iff j <= i
+ * when causal and |i - j| < window when window > 0, and the score carries
+ * -m_h |i - j| (m_h = 2^(-8 (h+1) / Hq)) when alibi is 1, as in
+ * oracle_attn_rows_local.  Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_bwd_local(const double* q, const double* k, const double* v, const double* dO,
+                          int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                          int window, int alibi, double* dq, double* dk, double* dv) {
+    if (alibi != 0 && alibi != 1) return -1;
+    return attn_bwd_masked(q, k, v, dO, B, Hq, Hkv, S, D, causal, rope_base, NULL, 1, 1, window, alibi, dq, dk, dv);
 }
 
 /*
@@ -429,7 +453,8 @@ int oracle_attn_bwd_bs(const double* q, const double* k, const double* v, const 
     char* active = (char*)calloc((size_t)nb * nb, 1);
     for (int r = 0; r < nb; ++r)
         for (int e = row_ptr[r]; e < row_ptr[r + 1]; ++e) active[(size_t)r * nb + col_idx[e]] = 1;
-    const int rc = attn_bwd_masked(q, k, v, dO, B, Hq, Hkv, S, D, causal, rope_base, active, block, nb, dq, dk, dv);
+    const int rc = attn_bwd_masked(q, k, v, dO, B, Hq, Hkv, S, D, causal, rope_base, active, block, nb, 0, 0,
+                                   dq, dk, dv);
     free(active);
     return rc;
 }

@@ -213,3 +213,90 @@ def test_block_sparse_backward_with_every_block_is_dense():
     b = oracle.attn_bwd(q, k, v, dO, causal=True, rope_base=10000.0)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+def _local_autograd_ref(q, k, v, dO, causal, base, window, alibi):
+    """torch autograd through float64 SDPA whose float mask carries the band (-inf outside
+    |i - j| < window, and j > i when causal) and the ALiBi bias -m_h |i - j|, m_h = 2^(-8 (h+1) / Hq)."""
+    B, S, Hq, D = q.shape
+    G = Hq // k.shape[2]
+    qt, kt, vt = (torch.from_numpy(oracle.bf16_to_f64(a)).requires_grad_(True) for a in (q, k, v))
+    qr = _rope_torch(qt, base) if base else qt
+    kr = _rope_torch(kt, base) if base else kt
+    qh = qr.permute(0, 2, 1, 3)
+    kh = kr.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    vh = vt.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    i = torch.arange(S)[:, None]
+    j = torch.arange(S)[None, :]
+    dist = (i - j).abs().to(torch.float64)
+    ok = torch.ones(S, S, dtype=torch.bool)
+    if causal:
+        ok &= j <= i
+    if window:
+        ok &= dist < window
+    slopes = (2.0 ** (-8.0 * (torch.arange(Hq, dtype=torch.float64) + 1) / Hq)) if alibi else torch.zeros(Hq,
+                                                                                                          dtype=torch.float64)
+    bias = torch.where(ok[None], -slopes[:, None, None] * dist[None], torch.tensor(float("-inf"), dtype=torch.float64))
+    o = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=bias[None])
+    loss = (o.permute(0, 2, 1, 3) * torch.from_numpy(oracle.bf16_to_f64(dO))).sum()
+    loss.backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+@pytest.mark.parametrize("causal,window,alibi,base", [(True, 7, False, 10000.0), (False, 5, False, None),
+                                                      (True, 0, True, 500000.0), (False, 0, True, 10000.0),
+                                                      (True, 9, True, None), (False, 6, True, 37.0)])
+def test_local_backward_equals_banded_biased_autograd(causal, window, alibi, base):
+    """Sliding window and/or ALiBi ("AttnFuse", sec. 3 combinators): torch autograd with the band and bias."""
+    q, k, v, dO = _inputs(2, 4, 2, 29, 16, seed=41)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dO, causal=causal, rope_base=base, window=window, alibi=alibi)
+    rq, rk, rv = _local_autograd_ref(q, k, v, dO, causal, base, window, alibi)
+    np.testing.assert_allclose(dq, rq, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, rk, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, rv, rtol=0, atol=1e-11)
+
+
+def test_local_backward_matches_finite_differences():
+    """Window 3 and ALiBi on a tiny causal case: central differences of sum(O * dO), forward written out."""
+    rng = np.random.default_rng(4)
+    B, Hq, Hkv, S, D, W = 1, 2, 1, 6, 4, 3
+    q = rng.standard_normal((B, S, Hq, D))
+    k = rng.standard_normal((B, S, Hkv, D))
+    v = rng.standard_normal((B, S, Hkv, D))
+    dO = rng.standard_normal((B, S, Hq, D))
+
+    def loss(q, k, v):
+        total = 0.0
+        for hh in range(Hq):
+            m = 2.0 ** (-8.0 * (hh + 1) / Hq)
+            for a in range(S):
+                keys = [b for b in range(S) if b <= a and a - b < W]
+                s = np.array([q[0, a, hh] @ k[0, b, 0] / math.sqrt(D) - m * (a - b) for b in keys])
+                p = np.exp(s - s.max())
+                p /= p.sum()
+                total += float((p @ v[0, keys, 0]) @ dO[0, a, hh])
+        return total
+
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dO, causal=True, window=W, alibi=True)
+    eps = 1e-6
+    for x, grad in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            up = loss(q, k, v)
+            x[idx] = old - eps
+            dn = loss(q, k, v)
+            x[idx] = old
+            num[idx] = (up - dn) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-8)
+
+
+def test_local_backward_window_of_one_key_passes_dO_to_V():
+    """A window of one key: O_i = V_i, so dV_j = dO_j (summed over the group's heads) and dQ = dK = 0."""
+    q, k, v, dO = _inputs(1, 4, 2, 21, 16, seed=42)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dO, causal=True, rope_base=10000.0, window=1, alibi=True)
+    dOf = oracle.bf16_to_f64(dO)
+    np.testing.assert_array_equal(dq, 0.0)
+    np.testing.assert_array_equal(dk, 0.0)
+    np.testing.assert_allclose(dv, dOf.reshape(1, 21, 2, 2, 16).sum(axis=3), rtol=0, atol=1e-12)

@@ -17,7 +17,7 @@ import numpy as np
 from ._build import INCLUDE, LIB, build
 
 __all__ = ["attn_fwd", "attn_fwd_host", "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse",
-           "attn_fwd_local", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_mask_schedule", "attn_fwd_schedule", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
+           "attn_fwd_local", "attn_bwd_local", "create_block_mask", "attn_rope_rotate", "attn_fwd_rotated", "attn_mask_schedule", "attn_fwd_schedule", "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache",
            "AttnError", "build", "load_library", "header_functions", "ATTN_STATUS"]
 
 ATTN_STATUS = {
@@ -69,6 +69,8 @@ def load_library(path: str | None = None):
         lib.attn_bwd_blocksparse.argtypes = [vp] * 9 + [i] * 6 + [d, vp, vp, vp]
         lib.attn_fwd_local.restype = i
         lib.attn_fwd_local.argtypes = [vp] * 5 + [i] * 6 + [d, i, i, vp]
+        lib.attn_bwd_local.restype = i
+        lib.attn_bwd_local.argtypes = [vp] * 9 + [i] * 6 + [d, i, i, vp]
         lib.attn_build_tables.restype = i
         lib.attn_build_tables.argtypes = [i, i, d, d, ctypes.c_longlong, vp, vp, vp]
         lib.attn_mask_schedule.restype = i
@@ -212,10 +214,12 @@ def attn_decode(q, k, v, o=None, lse=None, *, rope_base=None, window_k=None, ret
     return o, lse
 
 
-def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream=None, block_mask=None):
+def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream=None, block_mask=None,
+             window: int = 0, alibi: bool = False):
     """Gradients (dq, dk, dv) of the forward for upstream gradient dO; o and lse are the forward's outputs.
 
     block_mask: the (row_ptr, col_idx) of attn_fwd_blocksparse, or None for the dense forward.
+    window / alibi: those of attn_fwd_local (its backward, attn_bwd_local); not with block_mask.
     """
     import torch
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
@@ -235,8 +239,12 @@ def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream
     lib = load_library()
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(), dq.data_ptr(),
             dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S, D, 1 if causal else 0, float(rope_base) if rope_base else 0.0)
+    if (window or alibi) and block_mask is not None:
+        raise ValueError("block_mask does not combine with window / alibi")
     with torch.cuda.device(q.device):
-        if block_mask is None:
+        if window or alibi:
+            rc = lib.attn_bwd_local(*args, int(window), 1 if alibi else 0, _stream_handle(stream, q.device))
+        elif block_mask is None:
             rc = lib.attn_bwd(*args, _stream_handle(stream, q.device))
         else:
             import numpy as np
@@ -249,6 +257,17 @@ def attn_bwd(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, stream
     if rc != 0:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_bwd_local(q, k, v, o, lse, dO, *, causal: bool = True, rope_base=None, window: int = 0,
+                   alibi: bool = False, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd_local with the same window and alibi; o, lse: its outputs."""
+    if window < 0:
+        raise ValueError("window must be >= 0")
+    if not window and not alibi:
+        return attn_bwd(q, k, v, o, lse, dO, causal=causal, rope_base=rope_base, stream=stream)
+    return attn_bwd(q, k, v, o, lse, dO, causal=causal, rope_base=rope_base, stream=stream, window=window,
+                    alibi=alibi)
 
 
 def _check_bshd(q, k, v):

@@ -857,16 +857,17 @@ struct RotScratch {
     size_t bytes = 0;
 };
 RotScratch g_bwd_rot[kMaxDevices];
-std::atomic<unsigned> g_bwd_configured[kMaxDevices];  // as DevInfo::configured, for the backward and block-sparse kernels
+// as DevInfo::configured, for the backward (bits 0-7, local 32-39) and block-sparse (8-31) kernels
+std::atomic<unsigned long long> g_bwd_configured[kMaxDevices];
 
-template <int D, bool CAUSAL, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
 int launch_bwd(const attn::BwdParams& bp, int dev, int ntiles, cudaStream_t st) {
     using L = attn::BwdLayout<D>;
     // at least 120 KB so that one CTA fits on an SM: each CTA takes all 512 TMEM columns
     constexpr int smem = static_cast<int>(L::kAlloc) > 120 * 1024 ? static_cast<int>(L::kAlloc) : 120 * 1024;
-    constexpr unsigned bit = 1u << ((D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0));
-    auto kv = attn::bwd_dkdv_kernel<D, CAUSAL, ROPE>;
-    auto kq = attn::bwd_dq_kernel<D, CAUSAL, ROPE>;
+    constexpr unsigned long long bit = 1ull << ((EXT ? 32 : 0) + ((D == 128 ? 2 : 0) | (CAUSAL ? 1 : 0) | (ROPE ? 4 : 0)));
+    auto kv = attn::bwd_dkdv_kernel<D, CAUSAL, ROPE, EXT>;
+    auto kq = attn::bwd_dq_kernel<D, CAUSAL, ROPE, EXT>;
     cudaError_t e;
     if (!(g_bwd_configured[dev].load(std::memory_order_acquire) & bit)) {
         if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
@@ -889,10 +890,11 @@ struct MaskEntry;
 }
 int get_mask(int dev, const int* row_ptr, const int* col_idx, int nrows, int** out, MaskEntry** entry = nullptr);
 
-// The backward; row_ptr / col_idx: an optional host CSR block mask (null: dense).
+// The backward; row_ptr / col_idx: an optional host CSR block mask (null: dense); ext: the local
+// kernels, with the sliding window (window > 0) and ALiBi (alibi = 1) of the local forward.
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
              void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
-             const int* row_ptr, const int* col_idx, void* stream) {
+             const int* row_ptr, const int* col_idx, void* stream, bool ext = false, int window = 0, int alibi = 0) {
     int arc = check_args(q, k, v, o, B, Hq, Hkv, S, D, causal, rope_base, 0.0);
     const int ntiles = (S + 127) / 128;
     if (arc == ATTN_OK && row_ptr != nullptr) arc = check_mask(row_ptr, col_idx, ntiles, causal != 0);
@@ -982,6 +984,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     bp.q_idx = mask != nullptr ? mask + ntiles + 1 : nullptr;
     bp.k_ptr = mask != nullptr ? mask + ntiles + 1 + nnz : nullptr;
     bp.k_idx = mask != nullptr ? mask + 2 * (ntiles + 1) + nnz : nullptr;
+    bp.window = window;
+    bp.alibi = alibi;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned dot_blocks = static_cast<unsigned>((rows + 7) / 8);
@@ -1007,6 +1011,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
                 attn::rope_rotate_kernel<64><<<blocks, 256, 0, st>>>(src, dst, rot_tab, row_tab, nrows, S, H);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail("backward rotation launch", e);
         }
+    }
+    if (ext) {
+        if (D == 128) {
+            if (causal) return rope ? launch_bwd<128, true, true, true>(bp, dev, ntiles, st) : launch_bwd<128, true, false, true>(bp, dev, ntiles, st);
+            return rope ? launch_bwd<128, false, true, true>(bp, dev, ntiles, st) : launch_bwd<128, false, false, true>(bp, dev, ntiles, st);
+        }
+        if (causal) return rope ? launch_bwd<64, true, true, true>(bp, dev, ntiles, st) : launch_bwd<64, true, false, true>(bp, dev, ntiles, st);
+        return rope ? launch_bwd<64, false, true, true>(bp, dev, ntiles, st) : launch_bwd<64, false, false, true>(bp, dev, ntiles, st);
     }
     if (D == 128) {
         if (causal) return rope ? launch_bwd<128, true, true>(bp, dev, ntiles, st) : launch_bwd<128, true, false>(bp, dev, ntiles, st);
@@ -1119,7 +1131,7 @@ template <int D, bool CAUSAL, bool ROPE, int EXT = 0>
 int launch_bs(const attn::BsParams& bp, int dev, int ctas, cudaStream_t st) {
     constexpr int kMin = 120 * 1024;  // one CTA per SM: each takes all 512 TMEM columns
     constexpr int smem = static_cast<int>(attn::BsLayout<D>::kAlloc) > kMin ? static_cast<int>(attn::BsLayout<D>::kAlloc) : kMin;
-    constexpr unsigned bit = 1u << (8 + 8 * EXT + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0) + (ROPE ? 4 : 0));
+    constexpr unsigned long long bit = 1ull << (8 + 8 * EXT + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0) + (ROPE ? 4 : 0));
     auto kern = attn::bs_fwd_kernel<D, CAUSAL, ROPE, EXT>;
     cudaError_t e;
     if (!(g_bwd_configured[dev].load(std::memory_order_acquire) & bit)) {
@@ -1215,14 +1227,13 @@ extern "C" int attn_fwd_blocksparse(const void* q, const void* k, const void* v,
     return bs_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base, row_ptr, col_idx, false, 0, 0, stream);
 }
 
-extern "C" int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                              int Hkv, int S, int D, int causal, double rope_base, int window, int alibi,
-                              void* stream) {
-    if (window < 0 || (alibi != 0 && alibi != 1)) return ATTN_ERR_UNSUPPORTED;
-    if (S < 1 || S > kMaxS) return ATTN_ERR_SHAPE;
-    // the tiles any row of a query tile can see: keys in [128 i - window + 1, 128 i + 127 (+ window - 1)]
+namespace {
+// The key tiles that any row of query tile i can see under the window (keys in
+// [128 i - window + 1, 128 i + 127 (+ window - 1 without the causal mask)]), as a CSR block mask.
+void local_tiles(int S, int causal, int window, std::vector<int>& row_ptr, std::vector<int>& col_idx) {
     const int nrows = (S + 127) / 128;
-    std::vector<int> row_ptr(1, 0), col_idx;
+    row_ptr.assign(1, 0);
+    col_idx.clear();
     for (int i = 0; i < nrows; ++i) {
         long long lo = 0, hi = causal ? 128LL * i + 127 : S - 1LL;
         if (window > 0) {
@@ -1233,8 +1244,31 @@ extern "C" int attn_fwd_local(const void* q, const void* k, const void* v, void*
         for (long long t = lo / 128; t <= hi / 128; ++t) col_idx.push_back(static_cast<int>(t));
         row_ptr.push_back(static_cast<int>(col_idx.size()));
     }
+}
+}  // namespace
+
+extern "C" int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                              int Hkv, int S, int D, int causal, double rope_base, int window, int alibi,
+                              void* stream) {
+    if (window < 0 || (alibi != 0 && alibi != 1)) return ATTN_ERR_UNSUPPORTED;
+    if (S < 1 || S > kMaxS) return ATTN_ERR_SHAPE;
+    if (window >= S) window = 0;  // every distance is below S: the same as no window (and no overflow)
+    std::vector<int> row_ptr, col_idx;
+    local_tiles(S, causal, window, row_ptr, col_idx);
     return bs_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base, row_ptr.data(),
                    col_idx.empty() ? nullptr : col_idx.data(), true, window, alibi, stream);
+}
+
+extern "C" int attn_bwd_local(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D,
+                              int causal, double rope_base, int window, int alibi, void* stream) {
+    if (window < 0 || (alibi != 0 && alibi != 1)) return ATTN_ERR_UNSUPPORTED;
+    if (S < 1 || S > kMaxS) return ATTN_ERR_SHAPE;
+    if (window >= S) window = 0;
+    std::vector<int> row_ptr, col_idx;
+    local_tiles(S, causal, window, row_ptr, col_idx);
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, rope_base, row_ptr.data(),
+                    col_idx.empty() ? nullptr : col_idx.data(), stream, true, window, alibi);
 }
 
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

@@ -51,7 +51,25 @@ struct BwdParams {
     // RoPE: 1 = tm_q and tm_k hold Q and K already rotated (fp16, one rotation pass before the
     // kernels), so no tile is rotated inside the loops; 0 = the RoPE warps rotate each tile
     int prerot;
+    // the local kernels (EXT): key j is visible to query i only if |i - j| < window (window > 0),
+    // and alibi = 1 adds -m_h |i - j| to the score, as the local forward did
+    int window;
+    int alibi;
 };
+
+// A local tile's elementwise terms for one thread's 64 columns x: visible iff lo <= x < hi, and
+// the score in log2 units gains -m2 |rel0 + sgn x| (the query - key distance of column x;
+// m2 = m_h log2(e), 0 without ALiBi).
+struct BwdLocal {
+    int lo, hi;
+    float m2, rel0, sgn;
+};
+
+// The ALiBi slope of query head h in log2 units, the local forward's expression.
+__device__ __forceinline__ float bwd_alibi_m2(const BwdParams& p, int h) {
+    return p.alibi ? exp2f(-8.f * static_cast<float>(h + 1) / static_cast<float>(p.f.Hq)) * 1.4426950408889634f
+                   : 0.f;
+}
 
 // (tile, batch-head) of CTA x among bh batch-heads x ntiles tiles, in the order p.head_major picks.
 __device__ __forceinline__ void bwd_cta_coords(const BwdParams& p, int bh, int ntiles, int& tile, int& bhi) {
@@ -190,8 +208,9 @@ __device__ __forceinline__ void bwd_store_row(const BwdParams& p, uint32_t taddr
 // the P phase needs only S^T, the dS phase only dP^T and P.  P phase: P^T = exp2(S^T c -
 // LSE2_col) (0 where the query is before the key), packed to bf16 over the half's S^T columns
 // (for dV) and kept in pp (for dS: the next S^T overwrites those columns meanwhile).
-template <bool MASKED>
-__device__ __forceinline__ void bwd_ew_p(uint32_t tS, const float* nls, float c, int lim, uint32_t (&pp)[32]) {
+template <bool MASKED, bool LOCAL = false>
+__device__ __forceinline__ void bwd_ew_p(uint32_t tS, const float* nls, float c, int lim, uint32_t (&pp)[32],
+                                         const BwdLocal& lc = BwdLocal{0, 64, 0.f, 0.f, 1.f}) {
     // nls: -LSE2 of the half's 64 query columns (-inf for padded queries: P = 0)
     const uint64_t c2 = f2_pack(c, c);
     auto chunk = [&](const uint32_t (&rs)[32], int cc) {
@@ -202,12 +221,24 @@ __device__ __forceinline__ void bwd_ew_p(uint32_t tS, const float* nls, float c,
             f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, f2_pack(l4.x, l4.y)), x0, x1);
             f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[e + 2]), __uint_as_float(rs[e + 3])), c2, f2_pack(l4.z, l4.w)),
                       x2, x3);
+            if (LOCAL) {
+                x0 = fmaf(-lc.m2, fabsf(fmaf(lc.sgn, static_cast<float>(cc + e), lc.rel0)), x0);
+                x1 = fmaf(-lc.m2, fabsf(fmaf(lc.sgn, static_cast<float>(cc + e + 1), lc.rel0)), x1);
+                x2 = fmaf(-lc.m2, fabsf(fmaf(lc.sgn, static_cast<float>(cc + e + 2), lc.rel0)), x2);
+                x3 = fmaf(-lc.m2, fabsf(fmaf(lc.sgn, static_cast<float>(cc + e + 3), lc.rel0)), x3);
+            }
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
             if (MASKED) {
                 if (cc + e < lim) p0 = 0.f;
                 if (cc + e + 1 < lim) p1 = 0.f;
                 if (cc + e + 2 < lim) p2 = 0.f;
                 if (cc + e + 3 < lim) p3 = 0.f;
+            }
+            if (LOCAL) {
+                if (cc + e < lc.lo || cc + e >= lc.hi) p0 = 0.f;
+                if (cc + e + 1 < lc.lo || cc + e + 1 >= lc.hi) p1 = 0.f;
+                if (cc + e + 2 < lc.lo || cc + e + 2 >= lc.hi) p2 = 0.f;
+                if (cc + e + 3 < lc.lo || cc + e + 3 >= lc.hi) p3 = 0.f;
             }
             pp[(cc + e) / 2] = pack_bf16x2(p0, p1);
             pp[(cc + e) / 2 + 1] = pack_bf16x2(p2, p3);
@@ -258,18 +289,27 @@ __device__ __forceinline__ void bwd_ew_ds(uint32_t tdP, const float* dl, const u
 // The dQ kernel's elementwise work in the same two phases, one thread per query row and half of
 // the columns (64 keys).  P phase: P = exp2(S c - LSE2_row), 0 for keys after the query (columns
 // c > lim), kept in pp as bf16 (the P of the dK/dV kernel's dS, so both kernels form one dS).
-template <bool MASKED>
-__device__ __forceinline__ void bwd_ew_p_row(uint32_t tS, float l2, float c, int lim, uint32_t (&pp)[32]) {
+template <bool MASKED, bool LOCAL = false>
+__device__ __forceinline__ void bwd_ew_p_row(uint32_t tS, float l2, float c, int lim, uint32_t (&pp)[32],
+                                             const BwdLocal& lc = BwdLocal{0, 64, 0.f, 0.f, 1.f}) {
     const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-l2, -l2);  // -inf for a padded row: P = 0
     auto chunk = [&](const uint32_t (&rs)[32], int cc) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, nl2), x0, x1);
+            if (LOCAL) {
+                x0 = fmaf(-lc.m2, fabsf(fmaf(lc.sgn, static_cast<float>(cc + e), lc.rel0)), x0);
+                x1 = fmaf(-lc.m2, fabsf(fmaf(lc.sgn, static_cast<float>(cc + e + 1), lc.rel0)), x1);
+            }
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             if (MASKED) {
                 if (cc + e > lim) p0 = 0.f;
                 if (cc + e + 1 > lim) p1 = 0.f;
+            }
+            if (LOCAL) {
+                if (cc + e < lc.lo || cc + e >= lc.hi) p0 = 0.f;
+                if (cc + e + 1 < lc.lo || cc + e + 1 >= lc.hi) p1 = 0.f;
             }
             pp[(cc + e) / 2] = pack_bf16x2(p0, p1);
         }
@@ -354,7 +394,7 @@ __device__ __forceinline__ void bwd_init_bars(uint32_t bar0) {
 // head-major order the CTAs of one KV head run together and read the Q and dO tiles they all
 // stream from L2 rather than HBM.
 // TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).
-template <int D, bool CAUSAL, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using L = BwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -416,10 +456,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             const int lim = kv0 + t - (q0 + 64 * half);  // query columns c < lim precede the key
             const uint32_t hS = tS + 64u * half, hdP = tdP + 64u * half;
             uint32_t pp[32];
-            if (CAUSAL && __any_sync(0xffffffffu, lim > 0))
+            if constexpr (EXT) {
+                // query column x is q0 + 64 half + x: its distance to the key is x - lim
+                int lo = CAUSAL ? lim : -(1 << 30), hi = 1 << 30;
+                if (p.window > 0) {
+                    hi = lim + p.window;
+                    if (!CAUSAL) lo = lim - p.window + 1;
+                }
+                const BwdLocal lc{lo, hi, bwd_alibi_m2(p, g * G + it / per_head), static_cast<float>(-lim), 1.f};
+                if (p.alibi || __any_sync(0xffffffffu, lo > 0 || hi < 64))
+                    bwd_ew_p<false, true>(hS, ls, c, 0, pp, lc);
+                else
+                    bwd_ew_p<false>(hS, ls, c, 0, pp);
+            } else if (CAUSAL && __any_sync(0xffffffffu, lim > 0)) {
                 bwd_ew_p<true>(hS, ls, c, lim, pp);
-            else
+            } else {
                 bwd_ew_p<false>(hS, ls, c, lim, pp);
+            }
             tmem_store_wait();
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));
@@ -602,7 +655,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 // (all of them without the causal mask); the heaviest tiles go first under the causal mask
 // (i = ntiles-1-y).
 // TMEM: S [0,128), dP [128,256), dQ [256, 256+D).
-template <int D, bool CAUSAL, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE, bool EXT = false>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using L = BwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -654,6 +707,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         const size_t rix = (static_cast<size_t>(b) * f.Hq + h) * f.S + (row < f.S ? row : 0);
         const float l2 = row < f.S ? p.lse[rix] * 1.4426950408889634f : INFINITY;  // padded rows get P = 0
         const float dl = row < f.S ? p.dlt[rix] : 0.f;
+        const float m2 = EXT ? bwd_alibi_m2(p, h) : 0.f;
         bool ok = true;
         for (int it = 0; it < iters && ok; ++it) {
             ok = bwd_wait(bar_at(bar0, BB_S_FULL), it & 1, ctl, kStatusSoftmax);
@@ -662,10 +716,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             const int lim = q0 + t - (ktile(it) * 128 + 64 * half);  // key columns c > lim follow the query
             const uint32_t hS = tS + 64u * half, hdP = tdP + 64u * half;
             uint32_t pp[32];
-            if (CAUSAL && __any_sync(0xffffffffu, lim < 63))
+            if constexpr (EXT) {
+                // key column x is ktile * 128 + 64 half + x: the query's distance to it is lim - x
+                int lo = -(1 << 30), hi = CAUSAL ? lim + 1 : 1 << 30;
+                if (p.window > 0) {
+                    lo = lim - p.window + 1;
+                    if (!CAUSAL) hi = lim + p.window;
+                }
+                const BwdLocal lc{lo, hi, m2, static_cast<float>(lim), -1.f};
+                if (p.alibi || __any_sync(0xffffffffu, lo > 0 || hi < 64))
+                    bwd_ew_p_row<false, true>(hS, l2, c, 0, pp, lc);
+                else
+                    bwd_ew_p_row<false>(hS, l2, c, 0, pp);
+            } else if (CAUSAL && __any_sync(0xffffffffu, lim < 63)) {
                 bwd_ew_p_row<true>(hS, l2, c, lim, pp);
-            else
+            } else {
                 bwd_ew_p_row<false>(hS, l2, c, lim, pp);
+            }
             tc_fence_before();
             mbar_arrive(bar_at(bar0, BB_P_FULL));  // S is read: the next S may overwrite it
             ok = bwd_wait(bar_at(bar0, BB_DP_FULL), it & 1, ctl, kStatusSoftmax);

@@ -478,7 +478,14 @@ def run_backward(args, w, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     kw = dict(causal=w["causal"], rope_base=w["rope_base"], stream=stream)
     mask = None
-    if args.blocksparse:  # the backward of the block-sparse forward, over the workload's mask
+    local = None
+    if args.local:  # the backward of the sliding-window / ALiBi forward
+        if "local" not in w:
+            raise SystemExit("--local needs a workload with a window or ALiBi (sliding_window_s4096, alibi_s4096)")
+        local = (w["local"]["window"], w["local"]["alibi"])
+        kw.update(window=local[0], alibi=local[1])
+        o, lse = attn.attn_fwd_local(q, k, v, **kw)
+    elif args.blocksparse:  # the backward of the block-sparse forward, over the workload's mask
         if "block_mask" not in w:
             raise SystemExit("--blocksparse needs a workload with a block mask (bigbird_s4096)")
         mask = si.bigbird_block_mask(S, causal=w["causal"], **w["block_mask"])
@@ -486,8 +493,9 @@ def run_backward(args, w, rank, world, local_rank):
         kw["block_mask"] = mask
     else:
         o, lse = attn.attn_fwd(q, k, v, **kw)
+    bwd = attn.attn_bwd_local if local is not None else attn.attn_bwd
     for _ in range(max(args.warmup, 3)):
-        attn.attn_bwd(q, k, v, o, lse, dO, **kw)
+        bwd(q, k, v, o, lse, dO, **kw)
     attn.attn_check(stream=stream, device=dev)
     times = []
     with ClockSampler(local_rank) as clocks:
@@ -495,7 +503,7 @@ def run_backward(args, w, rank, world, local_rank):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            attn.attn_bwd(q, k, v, o, lse, dO, **kw)
+            bwd(q, k, v, o, lse, dO, **kw)
             e1.record(stream)
             times.append((e0, e1))
         torch.cuda.synchronize(dev)
@@ -503,7 +511,12 @@ def run_backward(args, w, rank, world, local_rank):
     ms = float(np.median([a.elapsed_time(b) for a, b in times]))
     # useful backward work: 2.5 x the forward's 4*D FLOPs per visible (query, key) pair (dV, dP, dQ, dK
     # and the recomputed S); the kernels execute 7/5 of it, S and dP being formed in both tile kernels
-    pairs = visible_pairs(S, *mask, w["causal"]) if mask is not None else S * S * (0.5 if w["causal"] else 1.0)
+    if local is not None:
+        pairs = local_pairs(S, w["causal"], local[0])
+    elif mask is not None:
+        pairs = visible_pairs(S, *mask, w["causal"])
+    else:
+        pairs = S * S * (0.5 if w["causal"] else 1.0)
     flops = 2.5 * 4.0 * D * pairs * B * Hq
     tf = flops / (ms * 1e-3) / 1e12
     peaks, _ = load_peaks()
@@ -512,6 +525,9 @@ def run_backward(args, w, rank, world, local_rank):
     if mask is not None:
         cfg["step"] += ", over the block mask"
         cfg["active_blocks"] = int(mask[0][-1])
+    if local is not None:
+        cfg["step"] += ", with the sliding window / ALiBi bias"
+        cfg["window"], cfg["alibi"] = local
     cfg["l2"] = "inputs larger than L2" if 4 * q.numel() * 2 > (256 << 20) else "inputs may stay in L2 between steps"
     return {
         "metric": "attention backward TFLOP/s", "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -601,6 +617,14 @@ def run_blocksparse(args, w, rank, world, local_rank):
 
 
 # --------------------------------------------------------------------- sliding window / ALiBi
+def local_pairs(S, causal, win):
+    """Visible (query, key) pairs under the sliding window |i - j| < win (win 0: none) and the causal mask."""
+    i = np.arange(S, dtype=np.int64)
+    if causal:
+        return int(np.minimum(i + 1, win).sum()) if win else S * (S + 1) // 2
+    return int((np.minimum(i + win, S) - np.maximum(i - win + 1, 0)).sum()) if win else S * S
+
+
 def run_local(args, w, rank, world, local_rank):
     """One step = one attn_fwd_local call (sliding window and/or ALiBi) on the workload."""
     import torch
@@ -635,12 +659,7 @@ def run_local(args, w, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
     ms = float(np.median([a.elapsed_time(b) for a, b in times]))
-    i = np.arange(S, dtype=np.int64)
-    if w["causal"]:
-        pairs = int(np.minimum(i + 1, win).sum()) if win else S * (S + 1) // 2
-    else:
-        pairs = int((np.minimum(i + win, S) - np.maximum(i - win + 1, 0)).sum()) if win else S * S
-    tf = 4.0 * D * pairs * B * Hq / (ms * 1e-3) / 1e12
+    tf = 4.0 * D * local_pairs(S, w["causal"], win) * B * Hq / (ms * 1e-3) / 1e12
     peaks, _ = load_peaks()
     cfg = workload_config(args.workload, w)
     cfg["step"] = "forward with the sliding window / ALiBi bias"
@@ -708,7 +727,8 @@ def main():
     ap.add_argument("--decode", action="store_true",
                     help="time one decode step (attn_decode) on the workload's cache shape instead of the prefill")
     ap.add_argument("--local", action="store_true",
-                    help="time the sliding-window / ALiBi forward (sliding_window_s4096, alibi_s4096)")
+                    help="time the sliding-window / ALiBi forward (sliding_window_s4096, alibi_s4096); "
+                         "with --backward, its backward")
     ap.add_argument("--blocksparse", action="store_true",
                     help="time the block-sparse forward on a workload with a block mask (bigbird_s4096)")
     ap.add_argument("--backward", action="store_true",

@@ -292,10 +292,27 @@ int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void
  * The library lists the 128 x 128 tiles the window reaches and runs the
  * block-sparse kernel over them, masking and biasing cell by cell.
  * q, k, v, o, lse, B, Hq, Hkv, S, D, causal, rope_base: as attn_fwd.
+ * A window of S or more keys is no window (every distance is below S).
  * Errors: as attn_fwd; ATTN_ERR_UNSUPPORTED for window < 0 or alibi not 0/1.
  */
 int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
                    int D, int causal, double rope_base, int window, int alibi, void* stream);
+
+/*
+ * attn_bwd_local — attn_bwd for attn_fwd_local's attention ("AttnFuse",
+ * sec. 3 sliding_window and alibi combinators; sec. 4.4: the backward
+ * re-derives P from the forward's LSE and visits only the active blocks).
+ * The library lists the window's tiles as attn_fwd_local does and runs the
+ * block-sparse backward over them; each cell's P is exp(s + bias - LSE),
+ * 0 outside the window, with the same bias -m_h |i - j| (alibi = 1), so
+ * dS = P (dP - Dlt) keeps its form.  o and lse are attn_fwd_local's outputs
+ * for the same window and alibi.
+ * Arguments: as attn_bwd, plus window and alibi as attn_fwd_local.
+ * Errors: as attn_bwd; ATTN_ERR_UNSUPPORTED for window < 0 or alibi not 0/1.
+ */
+int attn_bwd_local(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D, int causal, double rope_base,
+                   int window, int alibi, void* stream);
 
 /*
  * attn_mask_schedule — the static task schedule attn_fwd_blocksparse and

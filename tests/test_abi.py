@@ -19,7 +19,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = attn.header_functions()
     assert set(names) == {"attn_fwd", "attn_fwd_noalloc", "attn_fwd_host", "attn_rope_rotate", "attn_fwd_rotated",
-                          "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "attn_fwd_local", "attn_mask_schedule", "attn_fwd_schedule", "attn_selftest_wait_timeout",
+                          "attn_decode", "attn_bwd", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "attn_fwd_local", "attn_bwd_local", "attn_mask_schedule", "attn_fwd_schedule", "attn_selftest_wait_timeout",
                           "attn_build_tables", "attn_check", "attn_error_string", "attn_release_cache"}
     out = subprocess.run(["nm", "-D", "--defined-only", attn._build.LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -140,6 +140,12 @@ def test_local_entry_checks_arguments_on_the_host(lib):
     assert call(alibi=2) == E["ATTN_ERR_UNSUPPORTED"]
     assert call(D=80) == E["ATTN_ERR_SHAPE"]
     assert call(S=0) == E["ATTN_ERR_SHAPE"]
+    bwd = lambda **kw: lib.attn_bwd_local(*([16] * 9), 1, 2, 2, kw.get("S", 256), kw.get("D", 128),
+                                          kw.get("causal", 1), 1e4, kw.get("window", 64), kw.get("alibi", 0), None)
+    assert bwd(window=-1) == E["ATTN_ERR_UNSUPPORTED"]
+    assert bwd(alibi=2) == E["ATTN_ERR_UNSUPPORTED"]
+    assert bwd(D=80) == E["ATTN_ERR_SHAPE"]
+    assert bwd(S=0) == E["ATTN_ERR_SHAPE"]
 
 
 def test_create_block_mask_lists_the_predicate():

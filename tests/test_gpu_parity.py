@@ -560,3 +560,48 @@ def test_local_forward_matches_oracle(B, Hq, Hkv, S, D, causal, base, window, al
     kr = np.repeat(kr, Hq // Hkv, axis=2)
     bound = 2 * 2.0 ** -11 * np.abs(qr * kr).sum(-1).transpose(0, 2, 1) / np.sqrt(D) + 1e-5
     assert np.all(np.abs(lse.cpu().numpy() - lse_ref) <= bound), f"{tag}: LSE beyond the fp16 rounding bound"
+
+
+def test_local_window_of_s_or_more_is_no_window():
+    """|i - j| < window holds for every pair once window >= S: the host treats it as no window."""
+    q, k, v = si.make_qkv(1, 2, 2, 600, 64, seed=977)
+    qd, kd, vd = _dev(q), _dev(k), _dev(v)
+    for alibi in (False, True):
+        o0, l0 = attn.attn_fwd_local(qd, kd, vd, causal=True, window=0, alibi=alibi)
+        o1, l1 = attn.attn_fwd_local(qd, kd, vd, causal=True, window=2 ** 31 - 1, alibi=alibi)
+        o2, l2 = attn.attn_fwd_local(qd, kd, vd, causal=True, window=600, alibi=alibi)
+        attn.attn_check()
+        assert torch.equal(o0, o1) and torch.equal(l0, l1) and torch.equal(o0, o2) and torch.equal(l0, l2)
+
+
+LOCAL_BWD = [
+    # B, Hq, Hkv, S, D, causal, rope_base, window, alibi
+    (1, 4, 4, 1000, 64, True, None, 256, False),     # causal sliding window, ragged tail
+    (2, 4, 2, 700, 128, True, 10000.0, 0, True),     # ALiBi over the whole causal range, RoPE, GQA
+    (1, 2, 2, 640, 64, False, None, 100, True),      # both, non-causal window (bias changes sign in a tile)
+    (1, 4, 2, 900, 64, True, 10000.0, 200, True),    # causal window and ALiBi, ragged
+    (1, 2, 2, 520, 128, True, None, 45, False),      # both window edges inside one tile
+    (1, 3, 3, 300, 128, True, 10000.0, 1, True),     # a window of one key: dV = dO, dQ = dK = 0
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,base,window,alibi", LOCAL_BWD)
+def test_local_backward_matches_oracle(B, Hq, Hkv, S, D, causal, base, window, alibi):
+    """attn_bwd_local on attn_fwd_local's own O and LSE against the float64 chain rule with the band and bias."""
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=1900 + S)
+    dO = si.bshd_bf16(1901 + S, 9, B, S, Hq, D)
+    qd, kd, vd, dOd = _dev(q), _dev(k), _dev(v), _dev(dO)
+    o, lse = attn.attn_fwd_local(qd, kd, vd, causal=causal, rope_base=base, window=window, alibi=alibi)
+    dq, dk, dv = attn.attn_bwd_local(qd, kd, vd, o, lse, dOd, causal=causal, rope_base=base, window=window,
+                                     alibi=alibi)
+    attn.attn_check()
+    rq, rk, rv = oracle.attn_bwd(q, k, v, dO, causal=causal, rope_base=base, window=window, alibi=alibi)
+    tag = f"local backward w={window} alibi={alibi} S={S}"
+    _check_grad(dv.float().cpu().numpy(), rv, tag + " dV")
+    if window == 1:
+        # P = 1 up to its bf16 rounding, so dS = P dO.(V - O) is a rounding residue, not 0
+        bound = 2e-2 * np.abs(rv).max()
+        assert np.abs(dq.float().cpu().numpy()).max() <= bound and np.abs(dk.float().cpu().numpy()).max() <= bound
+        return
+    _check_grad(dk.float().cpu().numpy(), rk, tag + " dK")
+    _check_grad(dq.float().cpu().numpy(), rq, tag + " dQ")

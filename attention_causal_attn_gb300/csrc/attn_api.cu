@@ -988,7 +988,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     bp.alibi = alibi;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const unsigned dot_blocks = static_cast<unsigned>((rows + 7) / 8);
+    const long long dot_rows = D == 128 ? attn::dot_rows_per_block<128>() : attn::dot_rows_per_block<64>();
+    const unsigned dot_blocks = static_cast<unsigned>((static_cast<long long>(rows) + dot_rows - 1) / dot_rows);
     if (D == 128)
         attn::bwd_dot_kernel<128><<<dot_blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
                                                                 static_cast<const __nv_bfloat16*>(dO), dlt, B, S, Hq);

@@ -83,30 +83,49 @@ __device__ __forceinline__ void bwd_cta_coords(const BwdParams& p, int bh, int n
     }
 }
 
-// Dlt for every row: one warp per (b, s, h) row of O and dO; dlt is [B][H][S].
+// Dlt for every row i = (b, s, h): dO_i . O_i, dlt [B][H][S].  Each thread reads 16-byte pieces
+// (8 values) of a row and the D/8 threads of a row add up through shuffles; a thread takes
+// kDotPasses rows, one block row-count apart, and issues all their loads first, so that enough
+// bytes are in flight per SM to stream O and dO at HBM rate.
+constexpr int kDotPasses = 4;
+template <int D>
+__host__ __device__ constexpr int dot_rows_per_block() { return 256 / (D / 8) * kDotPasses; }
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dot_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO, float* __restrict__ dlt,
                                                       int B, int S, int H) {
-    const long long row = blockIdx.x * 8LL + threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    if (row >= static_cast<long long>(B) * S * H) return;
-    float acc = 0.f;
-    if constexpr (D == 128) {
-        const uint2 a = __ldg(reinterpret_cast<const uint2*>(o + row * D) + lane);
-        const uint2 b = __ldg(reinterpret_cast<const uint2*>(dO + row * D) + lane);
-        acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) + bf16_lo(a.y) * bf16_lo(b.y) +
-              bf16_hi(a.y) * bf16_hi(b.y);
-    } else {
-        const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(o + row * D) + lane);
-        const uint32_t b = __ldg(reinterpret_cast<const uint32_t*>(dO + row * D) + lane);
-        acc = bf16_lo(a) * bf16_lo(b) + bf16_hi(a) * bf16_hi(b);
+    constexpr int kLanes = D / 8;              // threads per row
+    constexpr int kRowsPerPass = 256 / kLanes;
+    const long long nrows = static_cast<long long>(B) * S * H;
+    const long long base = static_cast<long long>(blockIdx.x) * dot_rows_per_block<D>();
+    const int sub = threadIdx.x % kLanes, rloc = threadIdx.x / kLanes;
+    uint4 a[kDotPasses], b[kDotPasses];
+#pragma unroll
+    for (int k = 0; k < kDotPasses; ++k) {
+        const long long row = base + k * kRowsPerPass + rloc;
+        a[k] = b[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < nrows) {
+            a[k] = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
+            b[k] = __ldg(reinterpret_cast<const uint4*>(dO + row * D) + sub);
+        }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        const long long h = row % H, s = (row / H) % S, b = row / (static_cast<long long>(H) * S);
-        dlt[(b * H + h) * S + s] = acc;
+    for (int k = 0; k < kDotPasses; ++k) {
+        const uint32_t av[4] = {a[k].x, a[k].y, a[k].z, a[k].w}, bv[4] = {b[k].x, b[k].y, b[k].z, b[k].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(bf16_lo(av[e]), bf16_lo(bv[e]), acc);
+            acc = fmaf(bf16_hi(av[e]), bf16_hi(bv[e]), acc);
+        }
+#pragma unroll
+        for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const long long row = base + k * kRowsPerPass + rloc;
+        if (sub == 0 && row < nrows) {
+            const long long h = row % H, s = (row / H) % S, bb = row / (static_cast<long long>(H) * S);
+            dlt[(bb * H + h) * S + s] = acc;
+        }
     }
 }
 

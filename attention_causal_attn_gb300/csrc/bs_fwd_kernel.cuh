@@ -47,9 +47,12 @@ constexpr int kBsMaxSlots = 5;  // barrier room per ring
 
 template <int D>
 struct BsLayout {
-    // ring depths: with D = 128 this is what fits beside the two Q slots in 227 KB; deeper rings
-    // (up to five slots at D = 64) measured no faster
-    static constexpr int KS = 3, VS = 2;
+    // Paired ring (D = 64): a tile's K and V share a slot index, land on one barrier (K_FULL) and
+    // are released together after its P V (K_EMPTY), so the issuer waits once and commits once
+    // less per tile.  D = 128 has room only for K and V rings of 3 and 2 slots (with the two Q
+    // slots in 227 KB): separate barriers.
+    static constexpr bool kPairKV = D == 64;
+    static constexpr int KS = kPairKV ? 4 : 3, VS = kPairKV ? 4 : 2;
     static_assert(KS <= kBsMaxSlots && VS <= kBsMaxSlots, "ring depth");
     static constexpr uint32_t kTile = 128u * D * 2u;
     static constexpr uint32_t kQ0 = 0;                 // Q slot of stream s at kQ0 + s kTile
@@ -518,11 +521,17 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
                 if (n >= 1 && !mbar_wait(bar_at(bar0, BS_K_EMPTY + r), (n - 1) & 1, ctl, kStatusProducer)) return false;
                 ++kq;
                 const uint32_t kb = bar_at(bar0, BS_K_FULL + r);
-                mbar_arrive_expect_tx(kb, L::kTile);
+                mbar_arrive_expect_tx(kb, L::kPairKV ? 2 * L::kTile : L::kTile);
 #pragma unroll
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_4d(sm + L::kK0 + r * L::kTile + sub * kSubTileBytes, &f.tm_k, kb, sub * 64, cu.k.g,
                                 cu.ktile(p) * 128, cu.k.b);
+                if constexpr (L::kPairKV) {  // the tile's V into the same slot index, on the same barrier
+#pragma unroll
+                    for (int sub = 0; sub < D / 64; ++sub)
+                        tma_load_4d(sm + L::kV0 + r * L::kTile + sub * kSubTileBytes, &f.tm_v, kb, sub * 64, cu.k.g,
+                                    cu.ktile(p) * 128, cu.k.b);
+                }
                 return true;
             };
             auto load_v = [&](const BsCursor& cu) -> bool {
@@ -544,7 +553,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             while (ok && (c0.valid() || c1.valid())) {
                 if (c0.valid()) {
                     if (go0) {
-                        ok = load_v(c0);
+                        if (!L::kPairKV) ok = load_v(c0);
                         c0.next(p);
                     }
                     go0 = true;
@@ -560,7 +569,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             drain_ring(bar_at(bar0, BS_Q_FULL + s), 1, ql0, ctl, kStatusDrain);
             drain_ring(bar_at(bar0, BS_Q_FULL + (s ^ 1)), 1, ql1, ctl, kStatusDrain);
             drain_ring(bar_at(bar0, BS_K_FULL), L::KS, kq, ctl, kStatusDrain);
-            drain_ring(bar_at(bar0, BS_V_FULL), L::VS, vq, ctl, kStatusDrain);
+            if (!L::kPairKV) drain_ring(bar_at(bar0, BS_V_FULL), L::VS, vq, ctl, kStatusDrain);
         }
         __syncwarp();
     } else if (warp == kBsWarpMma) {  // the whole warp: one elected thread issues
@@ -575,7 +584,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
         c0.init(p, tb0, tb1);
         c1.init(p, tb1, te1);
         int kq = 0, vq = 0, qn0 = 0, qn1 = 0, pq0 = 0, pq1 = 0, dn0 = 0, dn1 = 0;
-        auto issue_s = [&](const BsCursor& cu, int s, int& qn) -> bool {
+        auto issue_s = [&](const BsCursor& cu, int s, int& qn, int& kt) -> bool {
             if (cu.first()) {
                 if (!mbar_wait_warp(bar_at(bar0, BS_Q_FULL + s), qn & 1, ctl, kStatusMma)) return false;
                 if (ROPE && !mbar_wait_warp(bar_at(bar0, BS_Q_ROT + s), qn & 1, ctl, kStatusMma)) return false;
@@ -584,7 +593,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             const int r = kq % L::KS, n = kq / L::KS;
             if (!mbar_wait_warp(bar_at(bar0, BS_K_FULL + r), n & 1, ctl, kStatusMma)) return false;
             if (ROPE && !mbar_wait_warp(bar_at(bar0, BS_K_ROT + r), n & 1, ctl, kStatusMma)) return false;
-            ++kq;
+            kt = kq++;  // the tile's ticket: with the paired ring its P V reads V slot kt % VS
             tc_fence_after();
             const uint64_t qdesc = sw128_desc(sm + L::kQ0 + s * L::kTile, 16u, 1024u);
             const uint64_t kdesc = sw128_desc(sm + L::kK0 + r * L::kTile, 16u, 1024u);
@@ -593,16 +602,17 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
             for (int kk = 0; kk < D / 16; ++kk)
                 umma_ss(tS, desc_advance(qdesc, kmajor_units(kk)), desc_advance(kdesc, kmajor_units(kk)), kIdescS,
                         kk > 0 ? 1u : 0u);
-            tc_commit(bar_at(bar0, BS_K_EMPTY + r));         // the K slot refills once this S is formed
+            if (!L::kPairKV) tc_commit(bar_at(bar0, BS_K_EMPTY + r));  // the K slot refills once this S is formed
             if (cu.last()) tc_commit(bar_at(bar0, BS_Q_EMPTY + s));  // and Q_s after the task's last S
             tc_commit(bar_at(bar0, BS_S_FULL + s));
             return true;
         };
-        auto issue_pv = [&](const BsCursor& cu, int s, int& pq, int& dn) -> bool {
+        auto issue_pv = [&](const BsCursor& cu, int s, int& pq, int& dn, int kt) -> bool {
             if (!mbar_wait_warp(bar_at(bar0, BS_P_FULL + s), pq & 1, ctl, kStatusMma)) return false;
             ++pq;
-            const int r = vq % L::VS, n = vq / L::VS;
-            if (!mbar_wait_warp(bar_at(bar0, BS_V_FULL + r), n & 1, ctl, kStatusMma)) return false;
+            // paired ring: V landed with the tile's K (waited before its S)
+            const int r = L::kPairKV ? kt % L::VS : vq % L::VS, n = vq / L::VS;
+            if (!L::kPairKV && !mbar_wait_warp(bar_at(bar0, BS_V_FULL + r), n & 1, ctl, kStatusMma)) return false;
             if (cu.first() && dn >= 1 && !mbar_wait_warp(bar_at(bar0, BS_O_FREE + s), (dn - 1) & 1, ctl, kStatusMma))
                 return false;
             ++vq;
@@ -613,7 +623,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 umma_ts(tO, tS + kk * 8u, desc_advance(vdesc, kk * 128u), kIdescPV, (!cu.first() || kk > 0) ? 1u : 0u);
-            tc_commit(bar_at(bar0, BS_V_EMPTY + r));
+            tc_commit(bar_at(bar0, L::kPairKV ? BS_K_EMPTY + r : BS_V_EMPTY + r));  // K and V, or V, refill
             if (cu.last()) {
                 tc_commit(bar_at(bar0, BS_O_FULL + s));
                 ++dn;
@@ -623,21 +633,22 @@ __global__ void __launch_bounds__(kBsThreads, 1) bs_fwd_kernel(const __grid_cons
         // c0 is the stream whose turn it is (s): its first turn forms S only, each later turn
         // accumulates P V of its last S and forms its next S
         bool ok = true, go0 = false, go1 = false;
-        int s = 0;
+        int s = 0, kt0 = 0, kt1 = 0;  // ticket of each stream's last S
         while (ok && (c0.valid() || c1.valid())) {
             if (c0.valid()) {
                 if (go0) {
-                    ok = issue_pv(c0, s, pq0, dn0);
+                    ok = issue_pv(c0, s, pq0, dn0, kt0);
                     c0.next(p);
                 }
                 go0 = true;
-                if (ok && c0.valid()) ok = issue_s(c0, s, qn0);
+                if (ok && c0.valid()) ok = issue_s(c0, s, qn0, kt0);
             }
             bs_swap(c0, c1);
             bs_swap(qn0, qn1);
             bs_swap(pq0, pq1);
             bs_swap(dn0, dn1);
             bs_swap(go0, go1);
+            bs_swap(kt0, kt1);
             s ^= 1;
         }
         tc_commit(bar_at(bar0, BS_DRAIN));

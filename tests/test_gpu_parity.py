@@ -379,6 +379,27 @@ def test_backward_matches_oracle(B, Hq, Hkv, S, D, causal, base):
     _check_grad(dq.float().cpu().numpy(), rq, tag + " dQ")
 
 
+def test_backward_rope_causal_s8192_two_heads():
+    """The timed backward's own shape (B=4, H=32, S=8192, D=128, RoPE, causal): every gradient row of
+    two heads of the last batch against the chain rule on those heads alone (heads are independent
+    when Hq = Hkv, and the rotation does not depend on the head)."""
+    B, Hq, Hkv, S, D, base = 4, 32, 32, 8192, 128, 10000.0
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=2024)
+    dO = si.bshd_bf16(2025, 9, B, S, Hq, D)
+    qd, kd, vd, dOd = _dev(q), _dev(k), _dev(v), _dev(dO)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=True, rope_base=base)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dOd, causal=True, rope_base=base)
+    attn.attn_check()
+    b, heads = B - 1, [5, 30]
+    sl = lambda a: np.ascontiguousarray(a[b:b + 1][:, :, heads])
+    rq, rk, rv = oracle.attn_bwd(sl(q), sl(k), sl(v), sl(dO), causal=True, rope_base=base)
+    got = lambda t: t[b:b + 1][:, :, heads].float().cpu().numpy()
+    tag = "rope_causal_s8192 backward, batch 3, heads 5 and 30"
+    _check_grad(got(dv), rv, tag + " dV")
+    _check_grad(got(dk), rk, tag + " dK")
+    _check_grad(got(dq), rq, tag + " dQ")
+
+
 # ---------------------------------------------------------------- block-sparse forward
 BS = [
     # B, Hq, Hkv, S, D, causal, rope_base, mask
@@ -605,3 +626,25 @@ def test_local_backward_matches_oracle(B, Hq, Hkv, S, D, causal, base, window, a
         return
     _check_grad(dk.float().cpu().numpy(), rk, tag + " dK")
     _check_grad(dq.float().cpu().numpy(), rq, tag + " dQ")
+
+
+@pytest.mark.parametrize("window,alibi", [(512, False), (0, True)])
+def test_local_backward_full_shape_one_batch(window, alibi):
+    """The timed local backward's own shape (B=4, H=12, S=4096, D=64, causal; the sliding window of 512
+    keys, or ALiBi): every gradient row of one batch element, all heads, against the chain rule on that
+    batch element alone (batch elements are independent; the ALiBi slopes depend only on h and Hq)."""
+    B, Hq, Hkv, S, D = 4, 12, 12, 4096, 64
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=2030)
+    dO = si.bshd_bf16(2031, 9, B, S, Hq, D)
+    qd, kd, vd, dOd = _dev(q), _dev(k), _dev(v), _dev(dO)
+    o, lse = attn.attn_fwd_local(qd, kd, vd, causal=True, window=window, alibi=alibi)
+    dq, dk, dv = attn.attn_bwd_local(qd, kd, vd, o, lse, dOd, causal=True, window=window, alibi=alibi)
+    attn.attn_check()
+    b = 2
+    sl = lambda a: np.ascontiguousarray(a[b:b + 1])
+    rq, rk, rv = oracle.attn_bwd(sl(q), sl(k), sl(v), sl(dO), causal=True, window=window, alibi=alibi)
+    got = lambda t: t[b:b + 1].float().cpu().numpy()
+    tag = f"local backward S=4096 window={window} alibi={alibi}, batch 2"
+    _check_grad(got(dv), rv, tag + " dV")
+    _check_grad(got(dk), rk, tag + " dK")
+    _check_grad(got(dq), rq, tag + " dQ")

@@ -648,3 +648,27 @@ def test_local_backward_full_shape_one_batch(window, alibi):
     _check_grad(got(dv), rv, tag + " dV")
     _check_grad(got(dk), rk, tag + " dK")
     _check_grad(got(dq), rq, tag + " dQ")
+
+
+def test_blocksparse_backward_bigbird_full_shape_two_heads():
+    """The timed block-sparse backward's own shape (bigbird_s4096: B=4, H=32, S=4096, D=128, full
+    attention over the BigBird-style mask): every gradient row of two heads of one batch element against
+    the masked chain rule on those heads alone (the mask is shared by every head)."""
+    w = si.WORKLOADS["bigbird_s4096"]
+    B, Hq, Hkv, S, D = w["B"], w["Hq"], w["Hkv"], w["S"], w["D"]
+    rp, ci = si.bigbird_block_mask(S, causal=w["causal"], **w["block_mask"])
+    q, k, v = si.make_qkv(B, Hq, Hkv, S, D, seed=2040)
+    dO = si.bshd_bf16(2041, 9, B, S, Hq, D)
+    qd, kd, vd, dOd = _dev(q), _dev(k), _dev(v), _dev(dO)
+    o, lse = attn.attn_fwd_blocksparse(qd, kd, vd, rp, ci, causal=w["causal"])
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dOd, causal=w["causal"], block_mask=(rp, ci))
+    attn.attn_check()
+    b, heads = 1, [0, 19]
+    sl = lambda a: np.ascontiguousarray(a[b:b + 1][:, :, heads])
+    rq, rk, rv = oracle.attn_bwd(sl(q), sl(k), sl(v), sl(dO), causal=w["causal"], block_mask=(rp, ci))
+    got = lambda t: t[b:b + 1][:, :, heads].float().cpu().numpy()
+    tag = "bigbird_s4096 backward, batch 1, heads 0 and 19"
+    _check_grad(got(dv), rv, tag + " dV")
+    _check_grad(got(dk), rk, tag + " dK")
+    _check_grad(got(dq), rq, tag + " dQ")
+

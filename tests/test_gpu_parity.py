@@ -558,6 +558,9 @@ LOCAL = [
     (1, 3, 3, 300, 128, True, 10000.0, 1, True),     # a window of one key: O_i = V_i
     (1, 2, 2, 520, 128, True, None, 45, False),      # both window edges inside one tile and one 32-key chunk
     (1, 4, 2, 900, 64, True, 10000.0, 200, True),    # causal window and ALiBi: masked biased tiles, ragged
+    (1, 8, 2, 777, 128, True, 10000.0, 128, False),  # a window of exactly one tile, GQA group of 4, RoPE
+    (1, 2, 2, 513, 64, False, None, 512, False),     # non-causal window of S - 1 keys, ragged
+    (2, 2, 1, 384, 64, False, 500000.0, 0, True),    # non-causal ALiBi over the whole range, GQA, RoPE
 ]
 
 
@@ -603,6 +606,9 @@ LOCAL_BWD = [
     (1, 4, 2, 900, 64, True, 10000.0, 200, True),    # causal window and ALiBi, ragged
     (1, 2, 2, 520, 128, True, None, 45, False),      # both window edges inside one tile
     (1, 3, 3, 300, 128, True, 10000.0, 1, True),     # a window of one key: dV = dO, dQ = dK = 0
+    (1, 8, 2, 777, 128, True, 10000.0, 128, False),  # a window of exactly one tile, GQA group of 4, RoPE
+    (1, 2, 2, 513, 64, False, None, 512, False),     # non-causal window of S - 1 keys, ragged
+    (2, 2, 1, 384, 64, False, 500000.0, 0, True),    # non-causal ALiBi over the whole range, GQA, RoPE
 ]
 
 

@@ -333,8 +333,17 @@ def run_ours(args, w, rank, world, local_rank):
                 "ms_per_step": round(e2e_ms, 4), "entry": "attn_fwd_host (RoPE fused at load)"},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
+        "timing_ms": timing_stats(launch_ms),
     }
     return line
+
+
+def timing_stats(samples_ms):
+    """min / p10 / median / p90 / max of the per-step CUDA-event times (ms) and their count."""
+    a = np.asarray(samples_ms, dtype=np.float64)
+    q = np.percentile(a, [0, 10, 50, 90, 100])
+    return {"n": int(a.size), "min": round(float(q[0]), 4), "p10": round(float(q[1]), 4),
+            "median": round(float(q[2]), 4), "p90": round(float(q[3]), 4), "max": round(float(q[4]), 4)}
 
 
 def load_traffic(workload, kernel="attn_fwd_kernel"):
@@ -438,7 +447,8 @@ def run_decode(args, w, rank, world, local_rank):
             times.append((e0, e1))
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
-    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    ms = float(np.median(step_ms))
     same_shape = args.batch is None and args.seq is None and args.window_k is None and args.l2_fetch_bytes is None
     nbytes = decode_bytes(w)
     peaks, peak_kind = load_peaks()
@@ -457,7 +467,7 @@ def run_decode(args, w, rank, world, local_rank):
                      "traffic": load_traffic(args.workload, "decode_split_kernel") if same_shape else None,
                      "kernel": "decode_split_kernel + decode_combine_kernel",
                      "algorithmic": "K/V bytes read per step (window-skipped K chunks excluded), median step time"},
-        "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
+        "gpu_launches": 2 * args.steps, "clocks": clocks.summary(), "timing_ms": timing_stats(step_ms),
     }
 
 
@@ -508,7 +518,8 @@ def run_backward(args, w, rank, world, local_rank):
             times.append((e0, e1))
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
-    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    ms = float(np.median(step_ms))
     # useful backward work: 2.5 x the forward's 4*D FLOPs per visible (query, key) pair (dV, dP, dQ, dK
     # and the recomputed S); the kernels execute 7/5 of it, S and dP being formed in both tile kernels
     if local is not None:
@@ -535,10 +546,13 @@ def run_backward(args, w, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": float(peaks["bf16_tflops"]),
                      "unit": "TFLOP/s", "frac": round(tf / float(peaks["bf16_tflops"]), 4), "traffic": None,
-                     "kernel": "bwd_dot_kernel + bwd_dkdv_kernel + bwd_dq_kernel",
+                     "kernel": ("bwd_dot_kernel + 2 x rope_rotate_kernel + bwd_dkdv_kernel + bwd_dq_kernel"
+                                if w["rope_base"] else "bwd_dot_kernel + bwd_dkdv_kernel + bwd_dq_kernel"),
                      "algorithmic": "10*D FLOPs per visible (query, key) pair and head (2.5 x the forward's), "
                                     "median step time"},
-        "gpu_launches": 3 * args.steps, "clocks": clocks.summary(),
+        # the row reduction, the dK/dV and dQ kernels, and with RoPE the two rotation passes
+        "gpu_launches": (5 if w["rope_base"] else 3) * args.steps, "clocks": clocks.summary(),
+        "timing_ms": timing_stats(step_ms),
     }
 
 
@@ -591,7 +605,8 @@ def run_blocksparse(args, w, rank, world, local_rank):
             times.append((e0, e1))
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
-    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    ms = float(np.median(step_ms))
     pairs = visible_pairs(S, rp, ci, w["causal"])
     flops = 4.0 * D * pairs * B * Hq
     tf = flops / (ms * 1e-3) / 1e12
@@ -612,7 +627,7 @@ def run_blocksparse(args, w, rank, world, local_rank):
                      "traffic": load_traffic(args.workload, "bs_fwd_kernel") if same_shape(args) else None,
                      "kernel": "bs_fwd_kernel",
                      "algorithmic": "4*D FLOPs per visible (query, key) pair of the mask, median step time"},
-        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "gpu_launches": args.steps, "clocks": clocks.summary(), "timing_ms": timing_stats(step_ms),
     }
 
 
@@ -658,7 +673,8 @@ def run_local(args, w, rank, world, local_rank):
             times.append((e0, e1))
         torch.cuda.synchronize(dev)
     attn.attn_check(stream=stream, device=dev)
-    ms = float(np.median([a.elapsed_time(b) for a, b in times]))
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    ms = float(np.median(step_ms))
     tf = 4.0 * D * local_pairs(S, w["causal"], win) * B * Hq / (ms * 1e-3) / 1e12
     peaks, _ = load_peaks()
     cfg = workload_config(args.workload, w)
@@ -674,7 +690,7 @@ def run_local(args, w, rank, world, local_rank):
                      "traffic": load_traffic(args.workload, "bs_fwd_kernel") if same_shape(args) else None,
                      "kernel": "bs_fwd_kernel (EXT)",
                      "algorithmic": "4*D FLOPs per visible (query, key) pair, median step time"},
-        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "gpu_launches": args.steps, "clocks": clocks.summary(), "timing_ms": timing_stats(step_ms),
     }
 
 
@@ -768,6 +784,8 @@ def main():
     else:
         line = run_ours(args, w, rank, world, local_rank)
     if line is not None:
+        if args.impl != "reference":
+            line["source_sha"] = kernel_source_sha()  # hash of the CUDA and host sources that ran
         print(json.dumps(line), flush=True)
 
 

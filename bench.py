@@ -16,6 +16,12 @@ path shards by batch and head with no exchange), `value` is the job total.
 
 --impl reference times the float64 CPU oracle on the host cores instead, one
 bounded sample of query rows per step, on the same metric.
+
+Besides the contract's keys, each line of ours carries `timing_ms` (min, p10,
+median, p90, max and count of the per-step CUDA-event times) and `source_sha`
+(the hash of the CUDA and host sources that ran; the DRAM traffic records in
+profiles/ are matched against it).  Other legs: --decode, --backward,
+--blocksparse, --local (and --backward with either of the last two).
 """
 from __future__ import annotations
 
